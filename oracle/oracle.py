@@ -1,0 +1,297 @@
+"""The oracle: a plain, slow FP64 CPU forward MoE layer.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and bench.py's
+CPU-baseline / reference legs may import this module.  It shares no code with the
+CUDA library.
+
+The element-wise and combinatorial steps (number formats, softmax/top-k/gates,
+layout, SwiGLU, combine) are plain C loops in ``moe_oracle.c``; the contractions
+(router logits, expert GEMMs) use numpy's FP64 matmul as a library primitive.
+Steps run in the order the pages give for the layer ([MoK-2.37x] = "Cursor's MoK
+achieves 2.37x performance boost on NVIDIA GB300 NVL72", section 03: schedule,
+dispatch, expert FFN, combine, final weighted merge):
+
+  1. logits  = x . W_r (+ b)                          FP64 over the stored values
+  2. p = softmax(logits); top-k; g = p_sel / sum p_sel
+  3. layout: counts, offsets, (shard, row) schedule, inverse map
+  4. dispatch: each slot takes its token's row (MXFP8-quantised along H for the
+     MXFP8 workloads)
+  5. expert FFN: u = a . W_gate, v = a . W_up, h = silu(u) * v, h rounded to the
+     workload's intermediate format, y = h . W_down rounded to the staging format
+  6. combine: out[n] = sum_j g[n,j] * y[slot(n,j)] in j order, rounded once.
+
+Rounding points per workload dtype:
+  f32   : operands FP32 values; h, y and out rounded to FP32
+  bf16  : operands BF16 values; h, y and out rounded to BF16
+  mxfp8 : x, W_gate/W_up (along H) and W_down (along I) MXFP8-quantised; h
+          MXFP8-quantised along I per slot row; y and out rounded to BF16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (plain -O2, IEEE semantics, OpenMP over rows)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        L.orc_round_bf16.restype = ctypes.c_double
+        L.orc_round_bf16.argtypes = [ctypes.c_double]
+        L.orc_round_f32.restype = ctypes.c_double
+        L.orc_round_f32.argtypes = [ctypes.c_double]
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_encode.argtypes = [ctypes.c_double]
+        L.orc_round_bf16_array.argtypes = [_f64p, _i64, _f64p]
+        L.orc_round_f32_array.argtypes = [_f64p, _i64, _f64p]
+        L.orc_e4m3_encode_array.argtypes = [_f64p, _i64, _u8p]
+        L.orc_quantize_mxfp8.argtypes = [_f64p, _i64, _i64, _u8p, _u8p]
+        L.orc_dequantize_mxfp8.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
+        L.orc_route_topk.argtypes = [_f64p, _i64, _int, _int, _i32p, _f64p, ctypes.c_void_p]
+        L.orc_layout.argtypes = [_i32p, _i64, _int, _int, _int, _i32p, _i32p, _i32p, _i32p]
+        L.orc_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
+        L.orc_combine.argtypes = [_f64p, _i32p, _f64p, _i64, _int, _i64, _f64p]
+        _lib = L
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Host FP64 copy of a numpy array or torch tensor (exact for f32/bf16 values)."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        if str(a.dtype) == "torch.bfloat16":
+            a = a.float()
+        a = a.numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+# --------------------------------------------------------------------------- formats
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    out = np.empty_like(a)
+    lib().orc_round_bf16_array(a.ravel(), a.size, out.ravel())
+    return out
+
+
+def round_f32(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    out = np.empty_like(a)
+    lib().orc_round_f32_array(a.ravel(), a.size, out.ravel())
+    return out
+
+
+def e4m3_encode(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint8)
+    lib().orc_e4m3_encode_array(a.ravel(), a.size, out.ravel())
+    return out
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    f = lib().orc_e4m3_decode
+    table = np.array([f(c) for c in range(256)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def quantize_mxfp8(a: np.ndarray):
+    """[rows, K] FP64 -> (codes [rows, K] u8, scales [rows, K/32] u8)."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    rows, K = a.shape
+    assert K % 32 == 0
+    codes = np.empty((rows, K), dtype=np.uint8)
+    scales = np.empty((rows, K // 32), dtype=np.uint8)
+    lib().orc_quantize_mxfp8(a, rows, K, codes, scales)
+    return codes, scales
+
+
+def dequantize_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, K = codes.shape
+    out = np.empty((rows, K), dtype=np.float64)
+    lib().orc_dequantize_mxfp8(codes, scales, rows, K, out)
+    return out
+
+
+def mxfp8_values(a: np.ndarray) -> np.ndarray:
+    """The values an MXFP8 operand holds after quantising a along its last axis."""
+    return dequantize_mxfp8(*quantize_mxfp8(a))
+
+
+def round_to(a: np.ndarray, fmt: str) -> np.ndarray:
+    """Round an FP64 array to the storage format of a tensor: f32, bf16, mxfp8."""
+    if fmt == "f32":
+        return round_f32(a)
+    if fmt == "bf16":
+        return round_bf16(a)
+    if fmt == "mxfp8":
+        return mxfp8_values(a)
+    raise ValueError(fmt)
+
+
+# --------------------------------------------------------------------------- steps
+def router_logits(x, w_router, bias=None) -> np.ndarray:
+    """logits[n, e] = sum_h x[n, h] W_r[h, e] (+ b_e), FP64 (w_router stored [E, H])."""
+    lg = _f64(x) @ _f64(w_router).T
+    if bias is not None:
+        lg = lg + _f64(bias)[None, :]
+    return np.ascontiguousarray(lg)
+
+
+def route_topk(logits: np.ndarray, k: int, want_probs: bool = False):
+    """Softmax, top-k (descending logit, lower index first on ties), renormalised gates."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    n, E = logits.shape
+    idx = np.empty((n, k), dtype=np.int32)
+    gate = np.empty((n, k), dtype=np.float64)
+    probs = np.empty((n, E), dtype=np.float64) if want_probs else None
+    lib().orc_route_topk(logits, n, E, k, idx, gate,
+                         None if probs is None else probs.ctypes.data_as(ctypes.c_void_p))
+    return (idx, gate, probs) if want_probs else (idx, gate)
+
+
+def topk_gap(logits: np.ndarray, k: int) -> np.ndarray:
+    """Per token: k-th largest logit minus the (k+1)-th (inf when k == E).  Used to
+    set aside near-ties, where FP32 and FP64 logits may pick different experts."""
+    E = logits.shape[1]
+    if k >= E:
+        return np.full(logits.shape[0], np.inf)
+    s = -np.sort(-logits, axis=1)
+    return s[:, k - 1] - s[:, k]
+
+
+def layout(idx: np.ndarray, E: int, S: int):
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    N, k = idx.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    sched = np.empty((N * k, 2), dtype=np.int32)
+    inv = np.empty((N, k), dtype=np.int32)
+    lib().orc_layout(idx, N, k, E, S, counts, offsets, sched, inv)
+    return counts, offsets, sched, inv
+
+
+def swiglu(u: np.ndarray, v: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    h = np.empty_like(u)
+    lib().orc_swiglu(u.ravel(), v.ravel(), u.size, h.ravel())
+    return h
+
+
+def combine(y: np.ndarray, inv: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    inv = np.ascontiguousarray(inv, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float64)
+    n, k = inv.shape
+    H = y.shape[1]
+    out = np.empty((n, H), dtype=np.float64)
+    lib().orc_combine(y, inv, gate, n, k, H, out)
+    return out
+
+
+# Storage formats of the FFN operands and outputs per workload dtype.
+FORMATS = {
+    #          operands  h        y       out
+    "f32":   ("f32",     "f32",   "f32",  "f32"),
+    "bf16":  ("bf16",    "bf16",  "bf16", "bf16"),
+    "mxfp8": ("mxfp8",   "mxfp8", "bf16", "bf16"),
+}
+
+
+def expert_operands(w_gate_up_e, w_down_e, dtype: str):
+    """FP64 values of one expert's weights as the GEMMs see them: (Wg^T [I,H],
+    Wu^T [I,H], Wd^T [H,I]); MXFP8 quantises each output column along K."""
+    wgu = _f64(w_gate_up_e)
+    wd = _f64(w_down_e)
+    I = wgu.shape[0] // 2
+    if dtype == "mxfp8":
+        wgu = mxfp8_values(wgu)
+        wd = mxfp8_values(wd)
+    return wgu[:I], wgu[I:], wd
+
+
+def expert_ffn(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, dtype: str) -> np.ndarray:
+    """y = round_y( round_h( silu(a Wg) * (a Wu) ) Wd ) for the rows a of one expert."""
+    _, fmt_h, fmt_y, _ = FORMATS[dtype]
+    u = a @ wg.T
+    v = a @ wu.T
+    h = round_to(swiglu(u, v), fmt_h)
+    return round_to(h @ wd.T, fmt_y)
+
+
+def forward(inp: dict, E: int, k: int, S: int, dtype: str, tokens=None, expert_fn=None,
+            weights=None) -> dict:
+    """The forward layer on the oracle.
+
+    inp: dict with x [N,H], w_router [E,H], bias [E] or None, w_gate_up [E,2I,H],
+         w_down [E,H,I] (numpy arrays or torch tensors; values are read as stored).
+    tokens: optional list of token indices; only their outputs are computed
+         (routing and layout always cover all N tokens).
+    expert_fn: optional hook (e, a) -> y replacing the SwiGLU FFN (closed-form tests).
+    weights: optional callable e -> (wg, wu, wd) FP64 operand values (lets callers
+         stream experts); defaults to expert_operands over inp's tensors.
+    Returns dict(logits, idx, gate, gap, counts, offsets, sched, inv, tokens, out).
+    """
+    fmt_a, _, _, fmt_out = FORMATS[dtype]
+    x = _f64(inp["x"])
+    N = x.shape[0]
+    logits = router_logits(x, inp["w_router"], inp.get("bias"))
+    idx, gate = route_topk(logits, k)
+    counts, offsets, sched, inv = layout(idx, E, S)
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+
+    # dispatch: the operand rows the experts read (MXFP8: quantised along H per row)
+    a_rows = x[toks]
+    if fmt_a == "mxfp8":
+        a_rows = mxfp8_values(a_rows)
+
+    # expert FFN, one expert at a time, over the (token, choice) pairs of toks
+    pair_tok, pair_j = np.meshgrid(np.arange(len(toks)), np.arange(k), indexing="ij")
+    pair_e = idx[toks][:, :k]
+    H = x.shape[1]
+    y = np.zeros((len(toks) * k, H), dtype=np.float64)
+    for e in np.unique(pair_e):
+        sel = np.nonzero(pair_e.ravel() == e)[0]
+        a = a_rows[pair_tok.ravel()[sel]]
+        if expert_fn is not None:
+            y[sel] = expert_fn(int(e), a)
+        else:
+            wg, wu, wd = weights(int(e)) if weights is not None else expert_operands(
+                inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
+            y[sel] = expert_ffn(a, wg, wu, wd, dtype)
+
+    # combine: y rows of this call are numbered token-major (t*k + j)
+    local_inv = (np.arange(len(toks) * k, dtype=np.int32)).reshape(len(toks), k)
+    out = combine(y, local_inv, gate[toks])
+    out = round_to(out, fmt_out)
+    return dict(logits=logits, idx=idx, gate=gate, gap=topk_gap(logits, k), counts=counts,
+                offsets=offsets, sched=sched, inv=inv, tokens=toks, out=out, y=y)

@@ -1,0 +1,104 @@
+"""The pins catch plausible oracle mistakes.
+
+Each case plants one mistake in the oracle (on the CPU, by swapping one oracle
+function for a wrong variant) and checks that at least one pin test then fails.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import test_oracle_formats as F
+import test_oracle_layer as L
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def _topk_ties_to_higher_index(orig):
+    def f(logits, k, want_probs=False):
+        rev = np.ascontiguousarray(logits[:, ::-1])
+        res = orig(rev, k, want_probs)
+        idx = (logits.shape[1] - 1 - res[0]).astype(np.int32)
+        return (idx,) + tuple(res[1:])
+    return f
+
+
+def _gates_not_renormalised(orig):
+    def f(logits, k, want_probs=False):
+        idx, gate, probs = orig(logits, k, True)
+        gate = np.take_along_axis(probs, idx.astype(np.int64), 1)
+        return (idx, gate, probs) if want_probs else (idx, gate)
+    return f
+
+
+def _layout_descending_tokens(orig):
+    def f(idx, E, S):
+        counts, offsets, sched, inv = orig(idx, E, S)
+        T = inv.size
+        slot_expert = np.empty(T, dtype=np.int64)
+        slot_expert[inv.ravel()] = idx.ravel()
+        new = inv.copy().ravel()
+        for e in range(E):       # reverse the order inside each expert segment
+            a, b = offsets[e], offsets[e + 1]
+            new = np.where((inv.ravel() >= a) & (inv.ravel() < b), a + b - 1 - inv.ravel(), new)
+        sched2 = np.empty_like(sched)
+        sched2[new] = sched[inv.ravel()]
+        return counts, offsets, sched2, new.reshape(inv.shape).astype(np.int32)
+    return f
+
+
+def _swiglu_swapped(orig):
+    return lambda u, v: orig(v, u)
+
+
+def _combine_drops_last_choice(orig):
+    def f(y, inv, gate):
+        g = gate.copy()
+        g[:, -1] = 0.0
+        return orig(y, inv, g)
+    return f
+
+
+def _quantize_wrong_emax(orig):
+    def f(a):
+        codes, scales = orig(a)          # scale one binade too large (emax 7 for 8)
+        return codes, scales + 1
+    return f
+
+
+def _round_bf16_truncates(orig):
+    def f(a):
+        a = np.ascontiguousarray(a, dtype=np.float64)
+        bits = a.astype(np.float32).view(np.uint32) & np.uint32(0xFFFF0000)
+        return bits.view(np.float32).astype(np.float64)
+    return f
+
+
+def _ffn_transposed_down(orig):
+    def f(a, wg, wu, wd, dtype):
+        return orig(a, wg, wu, wd.T.copy() if wd.shape[0] == wd.shape[1] else wd[::-1].copy(), dtype)
+    return f
+
+
+CASES = [
+    ("route_topk", _topk_ties_to_higher_index, [L.test_topk_matches_numpy_stable_argsort]),
+    ("route_topk", _gates_not_renormalised, [L.test_gates_renormalised_softmax]),
+    ("layout", _layout_descending_tokens, [lambda: L.test_layout_invariants(64, 8, 2, 2)]),
+    ("swiglu", _swiglu_swapped, [L.test_silu_closed_forms]),
+    ("combine", _combine_drops_last_choice, [L.test_combine_constant_rows_closed_form]),
+    ("quantize_mxfp8", _quantize_wrong_emax, [F.test_mxfp8_scale_for_power_of_two_amax]),
+    ("round_bf16", _round_bf16_truncates, [F.test_bf16_rounding_matches_torch_on_ties_and_near_ties]),
+    ("expert_ffn", _ffn_transposed_down,
+     [lambda: L.test_single_expert_top1_is_a_dense_ffn("bf16", lambda t: t.bfloat16().double(), 1e-2)]),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pins", CASES, ids=[c[1].__name__.strip("_") for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, name, mutant, pins):
+    monkeypatch.setattr(O, name, mutant(getattr(O, name)))
+    assert any(_fails(p) for p in pins), f"no pin caught the planted mistake in {name}"
