@@ -1,0 +1,239 @@
+/*
+ * moe.h -- C ABI of libmoe, a single-GPU forward Mixture-of-Experts layer for
+ * GB300 (sm_103a): top-k routing, sort-free token layout, pull-style gather from
+ * virtual source shards into a ring of token slots, grouped SwiGLU expert FFN
+ * (FP32, BF16 or block-scaled MXFP8 on tcgen05 tensor cores), and a gate-weighted
+ * combine back to token order; plus one persistent kernel that runs gather,
+ * expert FFN and combine as roles on separate SMs.
+ *
+ * The method is the one described on
+ *   [MoK-2.37x] "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+ *               NVL72" (KuCoin news flash; Spanish, Vietnamese, Hindi and
+ *               Traditional Chinese editions; sections 01, 02, 03)
+ *   [Kittens]   "Смесь котят: как Cursor создал открытое ядро, ускоряющее обучение
+ *               ИИ до 2.4 раз" (qubstore.ru; paragraphs on pull dispatch, the ring
+ *               buffer and the megakernel)
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller (typically a
+ *     PyTorch allocation).  The library never allocates device memory; scratch
+ *     space comes from a caller-owned workspace sized by moe_workspace_bytes().
+ *   - Shapes and parameters are passed in HOST structs and read during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call only enqueues work and returns; none synchronises the
+ *     host except moe_last_device_status().
+ *   - Argument errors (null pointers, unsupported shapes, a workspace that is too
+ *     small) are detected on the host before anything is launched and returned as
+ *     a moe_status_t; nothing is enqueued in that case.  A failed launch returns
+ *     MOE_ERR_CUDA.
+ *   - Errors only the device can see (an expert index out of range, a schedule
+ *     entry outside its shard, a bounded wait that ran out) are recorded in a
+ *     status word at the start of the workspace (first error wins) and read with
+ *     moe_last_device_status().  Kernels that detect one skip the offending work
+ *     and return; they never trap.
+ *   - Row-major layouts throughout.  Weights are K-major per expert: each output
+ *     column's K values are contiguous (the GEMMs' B operands).
+ *
+ * Number formats (moe_shape_t.dtype)
+ *   MOE_F32   : x, router weight, expert weights, y and out are FP32.
+ *   MOE_BF16  : x, router weight, expert weights, h, y and out are BF16; every
+ *               contraction accumulates in FP32.
+ *   MOE_MXFP8 : x, router weight and out are BF16; the expert GEMM operands (the
+ *               gathered token rows, W_gate/W_up, h, W_down) are MXFP8: E4M3 codes
+ *               plus one UE8M0 scale byte per 32 consecutive elements along K
+ *               (OCP MX v1.0; scale exponent floor(log2(amax)) - 8, saturating
+ *               round-to-nearest-even codes).  Scales are stored row-major next to
+ *               their codes: [rows][K/32] bytes.  y is BF16.  Accumulation FP32.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
+    MOE_ERR_UNSUPPORTED = 2,   /* a shape or dtype this build has no kernel for */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_bytes() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (see moe_params_t.timeout_ns) */
+    MOE_ERR_DEVICE_CHECK = 6   /* device: an index was out of range; the item was skipped */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP8 = 2 } moe_dtype_t;
+
+/* Layer shape.  N tokens of hidden size H, E experts of intermediate size I,
+ * k experts per token, S virtual source shards of N/S consecutive tokens each
+ * (N must be a multiple of S).  T = N*k token slots. */
+typedef struct {
+    int N, H, I, E, k, S;
+    int dtype; /* moe_dtype_t */
+} moe_shape_t;
+
+/* Tuning of the persistent forward kernel (moe_forward_fused); zero fields take
+ * defaults.  The ring holds `ring_slots` token slots; slots are handed from the
+ * gather role to the compute role in minibatches of `minibatch` slots
+ * ([MoK-2.37x] section 02: SM split, GPU-local counters, minibatch of at least
+ * two full GEMM waves, fixed-size ring token buffer reused as soon as a slot's
+ * results have left).  timeout_ns bounds every device-side wait. */
+typedef struct {
+    int ring_slots;        /* ring capacity in token slots; 0 = T (no reuse)          */
+    int minibatch;         /* slots per handoff; 0 = two waves of GEMM1 tiles          */
+    int gather_ctas;       /* CTAs in the gather + combine role; 0 = default           */
+    int compute_ctas;      /* CTAs in the expert-FFN role; 0 = all remaining SMs       */
+    long long timeout_ns;  /* bound on each device-side wait; 0 = 2e9 (two seconds)    */
+    int test_skip_ready;   /* test hook, 0 = off.  When m+1 > 0, the gather role never
+                              publishes minibatch m, so the compute role's bounded
+                              wait runs out and the call reports MOE_ERR_TIMEOUT.  */
+} moe_params_t;
+
+/* Bytes of workspace every entry point below needs for this shape and these
+ * params (params may be NULL: defaults).  Its first 256 bytes hold the device
+ * status word and must be zeroed once with moe_workspace_init() before first use. */
+size_t moe_workspace_bytes(const moe_shape_t* shape, const moe_params_t* params);
+
+/* Zero the workspace header (status word and counters) on `stream`. */
+int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, read the device status word of `workspace`, reset it to
+ * MOE_OK and return what it held.  The only entry point that blocks the host. */
+int moe_last_device_status(void* workspace, void* stream);
+
+/* Human-readable name of a moe_status_t value (static string). */
+const char* moe_status_string(int status);
+
+/* MXFP8 quantisation along K of a row-major [rows][K] matrix (OCP MX v1.0 block
+ * rule; the layer's configuration names it for GEMM operands; [MoK-2.37x]
+ * section 02 fuses it into the data path for activations).  Used for the
+ * expert weights (once, offline) and as a stand-alone test of the rule.
+ *   in      : [rows][K], in_dtype MOE_F32 or MOE_BF16
+ *   codes   : [rows][K] E4M3 bytes          (out)
+ *   scales  : [rows][K/32] UE8M0 bytes      (out)
+ * K must be a multiple of 32.  Bit-exact with the oracle on identical input. */
+int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
+                       uint8_t* codes, uint8_t* scales, void* stream);
+
+/* Router + top-k ([MoK-2.37x] section 01: every token picks a few experts each
+ * step; configuration: softmax over the router logits, top-k, gates renormalised
+ * to sum 1).
+ *   x          : [N][H]  FP32 (MOE_F32) or BF16 (otherwise)
+ *   w_router   : [E][H]  same dtype as x (W_r transposed: expert-major)
+ *   bias       : [E] FP32 added to the logits, or NULL
+ *   idx        : [N][k] int32, the k experts by descending logit; equal logits
+ *                keep the lower expert index first                   (out)
+ *   gate       : [N][k] FP32, softmax of the selected logits (= the full
+ *                softmax renormalised over the k choices)            (out)
+ *   logits_out : [N][E] FP32 logits as the kernel computed them, or NULL
+ *   xq_codes, xq_scales : for MOE_MXFP8, [N][H] and [N][H/32] MXFP8 copy of x
+ *                (the dispatch operand), or NULL to skip
+ * Logits accumulate in FP32 (BF16 products on tensor cores when E%16==0,
+ * E<=256 and H%64==0; FP32 SIMT otherwise). */
+int moe_route_topk(const void* x, const void* w_router, const float* bias,
+                   const moe_shape_t* shape, int32_t* idx, float* gate, float* logits_out,
+                   uint8_t* xq_codes, uint8_t* xq_scales,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Sort-free layout ("schedule"; [MoK-2.37x] section 01 and [Kittens] pull
+ * paragraph: count tokens per expert, place them expert-contiguously, a
+ * two-column schedule built without sorting).
+ *   idx     : [N][k] int32 expert choices
+ *   counts  : [E] tokens per expert                                  (out)
+ *   offsets : [E+1] exclusive scan of counts, offsets[E] = T, unpadded (out)
+ *   sched   : [T][2] int32 (source shard, row within shard) per slot  (out)
+ *   inv     : [N][k] int32 slot of choice (n, j)                      (out)
+ * Inside an expert, slots follow ascending token index (a stable counting
+ * placement: per-chunk expert counts via warp match + shared-memory atomics, an
+ * exclusive scan, then a warp-ballot rank).  Bit-exact with the oracle. */
+int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, int32_t* offsets,
+               int32_t* sched, int32_t* inv, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/* Pull dispatch ([MoK-2.37x] section 02: the expert side reads the rows it needs,
+ * knowing only the source shard and the row; it picks the local placement).
+ * Copies slots [slot_begin, slot_begin + slot_count) into the ring: slot t goes
+ * to ring row t % ring_slots.
+ *   shard_rows   : DEVICE array of S device pointers; shard s holds N/S rows of
+ *                  H elements (FP32 / BF16) or H E4M3 codes (MXFP8)
+ *   shard_scales : DEVICE array of S device pointers to [N/S][H/32] scales
+ *                  (MXFP8 only; NULL otherwise)
+ *   sched        : [T][2] from moe_layout
+ *   ring, ring_scales : [ring_slots][row] destination (ring_scales MXFP8 only)
+ * 16-byte vector loads and stores, one warp per slot row. */
+int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
+                      const moe_shape_t* shape, const int32_t* sched, int slot_begin,
+                      int slot_count, void* ring, void* ring_scales, int ring_slots,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Grouped SwiGLU expert FFN over expert-contiguous slot rows ([MoK-2.37x]
+ * sections 01-02: grouped GEMM fed expert-contiguous input; SwiGLU and MXFP8
+ * quantisation of activations inside the GEMM data path).  For each expert e and
+ * each row r in [offsets[e], offsets[e+1]):
+ *   [u v] = a_r . [W_gate,e W_up,e];  h = silu(u) * v  (rounded to BF16, or
+ *   MXFP8-quantised along I, or kept FP32);  y_r = h . W_down,e
+ *   a, a_scales : [T][H] slot rows in slot order (+ [T][H/32] scales, MXFP8)
+ *   offsets     : [E+1] DEVICE exclusive scan of expert counts (read on device;
+ *                 the host never learns the counts)
+ *   w_gate_up   : [E][2I][H]: rows 0..I-1 are W_gate^T, rows I..2I-1 W_up^T
+ *   w_gu_scales : [E][2I][H/32] (MXFP8) or NULL
+ *   w_down      : [E][H][I] (W_down^T);  w_d_scales: [E][H][I/32] or NULL
+ *   y           : [T][H] FP32 (MOE_F32) or BF16                        (out)
+ * BF16 / MXFP8 run on tcgen05 tensor cores (128x256 tiles, TMA-fed, accumulators
+ * in tensor memory) and need H % 256 == 0 and I % 128 == 0; MOE_F32 runs a SIMT
+ * kernel. */
+int moe_expert_ffn(const void* a, const void* a_scales, const int32_t* offsets,
+                   const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                   const void* w_d_scales, const moe_shape_t* shape, void* y,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Combine and final weighted merge ([MoK-2.37x] sections 02-03: every result
+ * returns to its token; the gate-weighted merge is part of the layer).
+ *   out[n] = sum_{j=0..k-1} gate[n][j] * y[inv[n][j]], FP32 accumulation in j
+ *   order, rounded once to out's dtype (FP32 for MOE_F32, BF16 otherwise).
+ *   y: [T][H] slot rows;  inv, gate: [N][k];  out: [N][H]. */
+int moe_combine(const void* y, const int32_t* inv, const float* gate, const moe_shape_t* shape,
+                void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Whole forward layer, one kernel per step on `stream` (route, layout, pull,
+ * expert FFN, combine) with every intermediate in the workspace.
+ *   x, w_router, bias : as moe_route_topk
+ *   w_* : expert weights as moe_expert_ffn (MXFP8: pre-quantised codes + scales)
+ *   out : [N][H]
+ *   idx_out, gate_out : optional [N][k] copies of the routing (NULL to skip)
+ * The MXFP8 copy of x is written once per source shard into the workspace and
+ * pulled from there through a device table of S shard pointers. */
+int moe_forward(const void* x, const void* w_router, const float* bias,
+                const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                const void* w_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                void* out, int32_t* idx_out, float* gate_out,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same layer, with gather, expert FFN and combine in ONE persistent kernel whose
+ * CTAs take the gather/combine role or the compute role ([MoK-2.37x] section 02:
+ * megakernel with an explicit SM split; GPU-local counters hand each minibatch
+ * from the gather side to the compute side and back; a fixed-size ring of token
+ * slots is refilled as soon as its slots are consumed; no host round trip and no
+ * dropped tokens).  Routing and layout run first as their own kernels.  Output is
+ * bit-identical to moe_forward for every ring size, minibatch and SM split
+ * ([Kittens], megakernel paragraph: bitwise determinism). */
+int moe_forward_fused(const void* x, const void* w_router, const float* bias,
+                      const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                      const void* w_d_scales, const moe_shape_t* shape,
+                      const moe_params_t* params, void* out, int32_t* idx_out, float* gate_out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Smallest minibatch (in slots) that gives `waves` full waves of GEMM1 tiles of
+ * tile_m x tile_n over `compute_sms` SMs when GEMM1 has 2*I output columns
+ * ([MoK-2.37x] section 02: a minibatch should form at least two full waves; the
+ * pages estimate about 2368 tokens for H=7168, I=2048).  Host-only arithmetic. */
+int moe_min_minibatch(int waves, int compute_sms, int tile_m, int tile_n, int I);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,30 @@
+"""Helpers shared by the GPU parity tests: the error metric and small builders.
+No step of the layer's arithmetic lives here."""
+import numpy as np
+import torch
+
+TOL = {"f32": 1e-5, "bf16": 2e-2, "mxfp8": 6e-2}   # max per-row relative error vs FP64
+TIE_TAU = 1e-4                                      # logit gap below which FP32 may pick differently
+
+
+def row_rel_err(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Per row: max_h |got - ref| / max_h |ref|."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    num = np.abs(got - ref).max(axis=1)
+    den = np.abs(ref).max(axis=1)
+    den[den == 0] = 1.0
+    return num / den
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.numpy()
+
+
+def need_cuda():
+    import pytest
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")

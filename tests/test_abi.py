@@ -1,0 +1,76 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function that
+include/moe.h declares, and its host-only logic (workspace sizing, argument
+checks, the minibatch wave rule) behaves as documented.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from token_dispatch_expert_top_gb300 import moe as M
+from token_dispatch_expert_top_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_entry_points():
+    decl = declared_functions()
+    assert set(decl) == set(M.ENTRY_POINTS), set(decl) ^ set(M.ENTRY_POINTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(os.path.join(ROOT, "token_dispatch_expert_top_gb300", "libmoe.so"))
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert M.status_name(0) == "MOE_OK"
+    assert M.status_name(M.MOE_ERR_TIMEOUT) == "MOE_ERR_TIMEOUT"
+    assert M.status_name(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_workspace_bytes_grows_with_shape_and_rejects_bad_shapes():
+    small = M.Shape.of(synth.WORKLOADS["tiny_f32"])
+    big = M.Shape.of(synth.WORKLOADS["dsv3_mxfp8"])
+    b_small = M.moe_workspace_bytes(small)
+    b_big = M.moe_workspace_bytes(big)
+    assert 0 < b_small < b_big
+    # config-3 staged forward: ring (T x 7392 B) + h + y (T x 14336 B) dominate
+    T = 8192 * 8
+    assert b_big > T * (7168 + 224 + 2048 + 64 + 2 * 7168)
+    for bad in [dict(k=9, E=8), dict(N=65, S=2), dict(H=100), dict(dtype=7), dict(E=0)]:
+        d = dict(N=64, H=128, I=256, E=8, k=2, S=2, dtype=0)
+        d.update(bad)
+        assert M.moe_workspace_bytes(M.Shape(**d)) == 0, bad
+    # tensor-core dtypes need H % 256 == 0 and I % 128 == 0
+    assert M.moe_workspace_bytes(M.Shape(N=64, H=128, I=256, E=8, k=2, S=2, dtype=1)) == 0
+
+
+def test_argument_errors_return_before_any_launch():
+    bad = M.Shape(N=64, H=128, I=256, E=8, k=9, S=2, dtype=0)
+    lib = M.lib()
+    assert lib.moe_layout(None, ctypes.byref(bad), None, None, None, None, None, 0, None) == M.MOE_ERR_INVALID_ARG
+    ok = M.Shape.of(synth.WORKLOADS["tiny_f32"])
+    # missing workspace
+    assert lib.moe_layout(1, ctypes.byref(ok), 1, 1, 1, 1, None, 0, None) == M.MOE_ERR_WORKSPACE
+    assert lib.moe_expert_ffn(None, None, None, None, None, None, None, ctypes.byref(ok), None, 16,
+                              1 << 40, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_mxfp8(None, 1, 4, 33, None, None, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch_pull(1, None, ctypes.byref(ok), 1, 100, 100, 1, None, 8, 16, 256,
+                                 None) == M.MOE_ERR_INVALID_ARG   # slots past T
+
+
+def test_minibatch_wave_rule_golden():
+    path = os.path.join(ROOT, "tests", "golden", "minibatch_waves.txt")
+    rows = [l.split("#")[0].split() for l in open(path)]
+    rows = [r for r in rows if r]
+    assert rows
+    for waves, sms, bm, bn, I, expect in rows:
+        assert M.moe_min_minibatch(int(waves), int(sms), int(bm), int(bn), int(I)) == int(expect)

@@ -1,0 +1,256 @@
+"""GPU parity of each step of the layer through the C ABI against the oracle:
+MXFP8 quantisation, router top-k, layout, pull dispatch, expert FFN, combine."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_common import TIE_TAU, TOL, need_cuda, row_rel_err, to_np
+from token_dispatch_expert_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    need_cuda()
+    from token_dispatch_expert_top_gb300 import moe
+    return moe
+
+
+def _ws(M, shape, params=None):
+    ws = torch.empty(M.moe_workspace_bytes(shape, params), dtype=torch.uint8, device="cuda")
+    M.moe_workspace_init(ws)
+    return ws
+
+
+# ------------------------------------------------------------------------ quantise
+def test_quantize_bit_exact_all_bf16_values(M):
+    bits = np.arange(1 << 16, dtype=np.uint32) << 16
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    rng = np.random.default_rng(0)
+    rng.shuffle(f)
+    pad = (-len(f)) % 32
+    f = np.concatenate([f, np.zeros(pad, np.float32)]).reshape(-1, 32)
+    x = torch.from_numpy(f).to(torch.bfloat16)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    scales = torch.empty((x.shape[0], 1), dtype=torch.uint8, device="cuda")
+    M.moe_quantize_mxfp8(x.cuda(), codes, scales)
+    oc, os_ = O.quantize_mxfp8(x.float().numpy().astype(np.float64))
+    np.testing.assert_array_equal(to_np(scales), os_)
+    np.testing.assert_array_equal(to_np(codes), oc)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_bit_exact_mixed_magnitudes(M, dtype):
+    rng = np.random.default_rng(1)
+    rows, K = 333, 512
+    v = rng.standard_normal((rows, K)) * np.exp2(rng.integers(-60, 60, size=(rows, K // 32)).repeat(32, 1))
+    v[3, :32] = 0.0                       # zero block
+    v[4, :32] = 1e-40                     # subnormal-only block (f32)
+    v[5, 0] = 3e38                        # near the top of the range
+    v[6, 5] = -500.0                      # saturating element
+    x = torch.from_numpy(v.astype(np.float32)).to(dtype)
+    codes = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device="cuda")
+    M.moe_quantize_mxfp8(x.cuda(), codes, scales)
+    oc, os_ = O.quantize_mxfp8(x.float().numpy().astype(np.float64))
+    np.testing.assert_array_equal(to_np(scales), os_)
+    np.testing.assert_array_equal(to_np(codes), oc)
+
+
+# -------------------------------------------------------------------------- router
+ROUTE_CASES = [
+    synth.WORKLOADS["tiny_f32"],
+    synth.WORKLOADS["small_bf16"],
+    synth.Workload("route_skew", N=1024, H=512, I=128, E=64, k=8, S=4, dtype="bf16", skew=3.0),
+    synth.Workload("route_e256", N=640, H=256, I=128, E=256, k=8, S=5, dtype="mxfp8"),
+]
+
+
+@pytest.mark.parametrize("w", ROUTE_CASES, ids=lambda w: w.name)
+def test_route_topk(M, w):
+    inp = synth.make_inputs(w, device="cpu", with_weights=False)
+    shape = M.Shape.of(w)
+    x, wr = inp["x"].cuda(), inp["w_router"].cuda()
+    bias = None if inp["bias"] is None else inp["bias"].cuda()
+    idx = torch.empty((w.N, w.k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((w.N, w.k), dtype=torch.float32, device="cuda")
+    logits = torch.empty((w.N, w.E), dtype=torch.float32, device="cuda")
+    M.moe_route_topk(x, wr, bias, shape, idx, gate, logits)
+    g_logits, g_idx, g_gate = to_np(logits).astype(np.float64), to_np(idx), to_np(gate)
+    # (i) the selection on the kernel's own FP32 logits is the oracle's, bit for bit
+    o_idx, o_gate = O.route_topk(g_logits, w.k)
+    np.testing.assert_array_equal(g_idx, o_idx)
+    np.testing.assert_allclose(g_gate, o_gate, rtol=2e-6, atol=1e-7)
+    # (ii) logits close to the FP64 oracle; indices equal away from near-ties
+    ref = O.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    assert np.abs(g_logits - ref).max() < 1e-4 * max(1.0, np.abs(ref).max())
+    r_idx, _ = O.route_topk(ref, w.k)
+    ok = O.topk_gap(ref, w.k) >= TIE_TAU
+    assert ok.mean() > 0.98
+    np.testing.assert_array_equal(g_idx[ok], r_idx[ok])
+
+
+# -------------------------------------------------------------------------- layout
+def _layout_case(M, idx_np, E, S):
+    N, k = idx_np.shape
+    w = synth.Workload("layout", N=N, H=256, I=128, E=E, k=k, S=S, dtype="bf16")
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sched = torch.empty((N * k, 2), dtype=torch.int32, device="cuda")
+    inv = torch.empty((N, k), dtype=torch.int32, device="cuda")
+    M.moe_layout(idx, shape, counts, offsets, sched, inv, ws)
+    assert M.moe_last_device_status(ws) == 0
+    oc, oo, osch, oinv = O.layout(idx_np.astype(np.int32), E, S)
+    np.testing.assert_array_equal(to_np(counts), oc)
+    np.testing.assert_array_equal(to_np(offsets), oo)
+    np.testing.assert_array_equal(to_np(sched), osch)
+    np.testing.assert_array_equal(to_np(inv), oinv)
+
+
+@pytest.mark.parametrize("N,E,k,S", [(64, 8, 2, 2), (4096, 64, 6, 8), (8192, 256, 8, 64),
+                                     (1000, 33, 5, 10), (37, 4, 4, 1), (300, 1, 1, 3)])
+def test_layout_bit_exact_random(M, N, E, k, S):
+    rng = np.random.default_rng(N + E)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)])
+    _layout_case(M, idx, E, S)
+
+
+def test_layout_bit_exact_hot_and_empty_experts(M):
+    rng = np.random.default_rng(5)
+    N, E, k = 3000, 128, 4
+    idx = np.empty((N, k), dtype=np.int64)
+    for n in range(N):
+        idx[n] = np.concatenate([[7, 100], rng.choice([1, 2, 3, 120], size=2, replace=False)])
+    _layout_case(M, idx, E, 6)
+
+
+def test_layout_reports_out_of_range_expert(M):
+    w = synth.Workload("bad", N=64, H=256, I=128, E=8, k=2, S=2, dtype="bf16")
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    idx = torch.zeros((64, 2), dtype=torch.int32, device="cuda")
+    idx[:, 1] = 1
+    idx[10, 1] = 8             # out of range: recorded, skipped, nothing written for it
+    counts = torch.empty(8, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(9, dtype=torch.int32, device="cuda")
+    sched = torch.zeros((128, 2), dtype=torch.int32, device="cuda")
+    inv = torch.zeros((64, 2), dtype=torch.int32, device="cuda")
+    M.moe_layout(idx, shape, counts, offsets, sched, inv, ws)
+    assert M.moe_last_device_status(ws) == M.MOE_ERR_DEVICE_CHECK
+    assert int(counts.sum()) == 127
+    assert M.moe_last_device_status(ws) == 0        # reading resets it
+
+
+# ------------------------------------------------------------------------ dispatch
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "mxfp8"])
+def test_dispatch_pull_rows_by_schedule(M, dtype):
+    rng = np.random.default_rng(3)
+    N, H, E, k, S = 512, 1024 if dtype != "f32" else 128, 16, 4, 8,
+    w = synth.Workload("pull", N=N, H=H, I=128, E=E, k=k, S=S, dtype=dtype)
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    rows = N // S
+    elem = {"f32": 4, "bf16": 2, "mxfp8": 1}[dtype]
+    shards = [torch.randint(0, 256, (rows, H * elem), dtype=torch.uint8, device="cuda") for _ in range(S)]
+    sc = [torch.randint(0, 256, (rows, H // 32), dtype=torch.uint8, device="cuda") for _ in range(S)]
+    tab = torch.tensor([t.data_ptr() for t in shards], dtype=torch.int64, device="cuda")
+    tab_sf = torch.tensor([t.data_ptr() for t in sc], dtype=torch.int64, device="cuda")
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    _, _, sched_np, _ = O.layout(idx, E, S)
+    sched = torch.from_numpy(sched_np).cuda()
+    T = N * k
+    R = 640                                  # ring smaller than T: slots wrap
+    ring = torch.zeros((R, H * elem), dtype=torch.uint8, device="cuda")
+    ring_sf = torch.zeros((R, H // 32), dtype=torch.uint8, device="cuda")
+    mx = dtype == "mxfp8"
+    begin, count = 1400, 600              # rows 1400..1999 wrap past R
+    M.moe_dispatch_pull(tab, tab_sf if mx else None, shape, sched, begin, count, ring,
+                        ring_sf if mx else None, R, ws)
+    assert M.moe_last_device_status(ws) == 0
+    allrows = torch.cat(shards).cpu()
+    allsf = torch.cat(sc).cpu()
+    for t in range(begin, begin + count):
+        src = sched_np[t, 0] * rows + sched_np[t, 1]
+        assert torch.equal(ring[t % R].cpu(), allrows[src])
+        if mx:
+            assert torch.equal(ring_sf[t % R].cpu(), allsf[src])
+
+
+# ------------------------------------------------------------------------- combine
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_combine_matches_oracle(M, dtype):
+    rng = np.random.default_rng(4)
+    N, H, k = 300, 512, 6
+    w = synth.Workload("comb", N=N, H=H, I=128, E=16, k=k, S=3, dtype=dtype)
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    T = N * k
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    y = torch.randn((T, H), dtype=torch.float32).to(tdt)
+    inv = torch.from_numpy(rng.permutation(T).reshape(N, k).astype(np.int32))
+    g = rng.random((N, k)).astype(np.float32)
+    g /= g.sum(1, keepdims=True)
+    gate = torch.from_numpy(g)
+    out = torch.empty((N, H), dtype=tdt, device="cuda")
+    M.moe_combine(y.cuda(), inv.cuda(), gate.cuda(), shape, out, ws)
+    ref = O.combine(to_np(y).astype(np.float64), inv.numpy(), g.astype(np.float64))
+    ref = O.round_to(ref, dtype)
+    err = row_rel_err(to_np(out), ref)
+    assert err.max() < (2e-6 if dtype == "f32" else 8e-3)
+
+
+# ---------------------------------------------------------------------- expert FFN
+FFN_CASES = [
+    ("f32", 128, 256, [0, 3, 40, 85]),
+    ("bf16", 512, 256, [0, 1, 130, 255, 300]),
+    ("mxfp8", 512, 256, [0, 1, 130, 255, 300]),
+    ("bf16", 2048, 1408, [200, 0, 383, 129, 257, 1, 640, 128]),
+    ("mxfp8", 2048, 1408, [200, 0, 383, 129, 257, 1, 640, 128]),
+    ("mxfp8", 7168, 2048, [37, 0, 256, 129]),
+]
+
+
+@pytest.mark.parametrize("dtype,H,I,counts", FFN_CASES,
+                         ids=[f"{c[0]}-H{c[1]}-I{c[2]}-E{len(c[3])}" for c in FFN_CASES])
+def test_expert_ffn_matches_oracle(M, dtype, H, I, counts):
+    E = len(counts)
+    T = sum(counts)
+    # a shape whose T = N*k equals the slot count: k = 1, N = T
+    w = synth.Workload("ffn", N=T, H=H, I=I, E=E, k=1, S=1, dtype=dtype)
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    g = torch.Generator().manual_seed(7)
+    master = torch.float32 if dtype == "f32" else torch.bfloat16
+    a = torch.randn((T, H), generator=g).to(master)
+    wgu = (torch.randn((E, 2 * I, H), generator=g) / H ** 0.5).to(master)
+    wd = (torch.randn((E, H, I), generator=g) / I ** 0.5).to(master)
+    offsets_np = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    offsets = torch.from_numpy(offsets_np).cuda()
+    y = torch.empty((T, H), dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device="cuda")
+    if dtype == "mxfp8":
+        from token_dispatch_expert_top_gb300.layer import quantize_mxfp8
+        a_c, a_s = quantize_mxfp8(a.cuda())
+        wgu_c, wgu_s = quantize_mxfp8(wgu.cuda())
+        wd_c, wd_s = quantize_mxfp8(wd.cuda())
+        M.moe_expert_ffn(a_c, a_s, offsets, wgu_c, wgu_s, wd_c, wd_s, shape, y, ws)
+    else:
+        M.moe_expert_ffn(a.cuda(), None, offsets, wgu.cuda(), None, wd.cuda(), None, shape, y, ws)
+    assert M.moe_last_device_status(ws) == 0
+    got = to_np(y)
+    a64 = O._f64(a)
+    if dtype == "mxfp8":
+        a64 = O.mxfp8_values(a64)
+    for e in range(E):
+        lo, hi = offsets_np[e], offsets_np[e + 1]
+        if lo == hi:
+            continue
+        wg, wu, wdd = O.expert_operands(wgu[e], wd[e], dtype)
+        ref = O.expert_ffn(a64[lo:hi], wg, wu, wdd, dtype)
+        err = row_rel_err(got[lo:hi], ref)
+        assert err.max() < TOL[dtype], (e, err.max())

@@ -1,0 +1,376 @@
+// api.cu -- the extern "C" entry points declared in include/moe.h: argument
+// checks, the workspace plan, and the launch sequences.  No function here
+// allocates device memory or synchronises the host (except
+// moe_last_device_status, whose job is to).
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+int num_sms_current() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+size_t act_elem(int dtype) { return dtype == MOE_F32 ? 4 : 2; }      // x, y, out
+size_t op_elem(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 1); }  // GEMM operands
+
+// Workspace regions, in order.  Every size depends only on the shape and params.
+struct Plan {
+    size_t header, cnt, base;               // layout scratch
+    size_t idx, gate, counts, offsets, sched, inv;
+    size_t xq, xq_sf, shard_tab, shard_sf_tab;
+    size_t ring, ring_sf, h, h_sf, y;
+    size_t total;
+    int ring_slots;
+};
+
+Plan make_plan(const moe_shape_t& s, const moe_params_t* p) {
+    const int64_t T = (int64_t)s.N * s.k;
+    const int nch = layout_chunks((int)T);
+    const bool mx = s.dtype == MOE_MXFP8;
+    int R = (p && p->ring_slots > 0) ? p->ring_slots : (int)T;
+    if (R < (int)T) R = (int)T;   // the staged path keeps every slot resident
+    Plan pl{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    pl.header = take(sizeof(WsHeader));
+    pl.cnt = take(sizeof(int32_t) * (size_t)nch * s.E);
+    pl.base = take(sizeof(int32_t) * (size_t)nch * s.E);
+    pl.idx = take(sizeof(int32_t) * (size_t)T);
+    pl.gate = take(sizeof(float) * (size_t)T);
+    pl.counts = take(sizeof(int32_t) * (size_t)s.E);
+    pl.offsets = take(sizeof(int32_t) * (size_t)(s.E + 1));
+    pl.sched = take(sizeof(int32_t) * 2 * (size_t)T);
+    pl.inv = take(sizeof(int32_t) * (size_t)T);
+    pl.xq = take(mx ? (size_t)s.N * s.H : 0);
+    pl.xq_sf = take(mx ? (size_t)s.N * (s.H / 32) : 0);
+    pl.shard_tab = take(sizeof(void*) * (size_t)s.S);
+    pl.shard_sf_tab = take(sizeof(void*) * (size_t)s.S);
+    pl.ring = take((size_t)R * s.H * op_elem(s.dtype));
+    pl.ring_sf = take(mx ? (size_t)R * (s.H / 32) : 0);
+    pl.h = take((size_t)R * s.I * op_elem(s.dtype));
+    pl.h_sf = take(mx ? (size_t)R * (s.I / 32) : 0);
+    pl.y = take((size_t)T * s.H * act_elem(s.dtype));
+    pl.total = off;
+    pl.ring_slots = R;
+    return pl;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int check_shape(const moe_shape_t* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->N < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 || s->S <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s->k > s->E || s->N % s->S != 0) return MOE_ERR_INVALID_ARG;
+    if (s->dtype < MOE_F32 || s->dtype > MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+    if (s->k > 32 || s->E > 1024) return MOE_ERR_UNSUPPORTED;
+    if (s->H % 32 != 0 || s->I % 32 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s->N * s->k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+    if (s->dtype != MOE_F32 && (s->H % 256 != 0 || s->I % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_ws(const moe_shape_t* s, const moe_params_t* p, void* ws, size_t bytes) {
+    if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    if (bytes < make_plan(*s, p).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+unsigned long long timeout_of(const moe_params_t* p) {
+    return (p && p->timeout_ns > 0) ? (unsigned long long)p->timeout_ns : kDefaultTimeoutNs;
+}
+
+__global__ void fill_shard_table_kernel(const uint8_t** tab, const uint8_t* base, int64_t stride, int S) {
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s < S) tab[s] = base + stride * s;
+}
+
+int expert_ffn_impl(const void* a, const void* a_scales, int a_rows, const int32_t* offsets,
+                    const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                    const void* w_d_scales, const moe_shape_t& s, void* y, void* ws,
+                    unsigned long long timeout, cudaStream_t st) {
+    const Plan pl = make_plan(s, nullptr);
+    const int T = s.N * s.k;
+    if (s.dtype == MOE_F32)
+        return cuda_status(launch_ffn_f32((const float*)a, offsets, (const float*)w_gate_up,
+                                          (const float*)w_down, T, s.H, s.I, s.E,
+                                          at<float>(ws, pl.h), (float*)y, num_sms_current(), st));
+    TcFfnCall c{};
+    c.mx = s.dtype == MOE_MXFP8;
+    c.T = T;
+    c.H = s.H;
+    c.I = s.I;
+    c.E = s.E;
+    c.a_rows = a_rows;
+    c.a = a;
+    c.a_sf = a_scales;
+    c.offsets = offsets;
+    c.w_gate_up = w_gate_up;
+    c.w_gu_sf = w_gu_scales;
+    c.w_down = w_down;
+    c.w_d_sf = w_d_scales;
+    c.h = at<void>(ws, pl.h);
+    c.h_sf = at<void>(ws, pl.h_sf);
+    c.y = y;
+    c.ws = at<WsHeader>(ws, pl.header);
+    c.timeout_ns = timeout;
+    c.grid = num_sms_current();
+    return cuda_status(launch_expert_ffn_tc(c, st));
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape_t* shape, const moe_params_t* params) {
+    if (check_shape(shape) != MOE_OK) return 0;
+    return make_plan(*shape, params).total;
+}
+
+int moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(WsHeader), (cudaStream_t)stream));
+}
+
+int moe_last_device_status(void* workspace, void* stream) {
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int status = 0;
+    if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    return status;
+}
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                       uint8_t* scales, void* stream) {
+    if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (in_dtype != MOE_F32 && in_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!in || !codes || !scales || !aligned16(in) || !aligned16(codes)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_mxfp8(in, in_dtype, rows, K, codes, scales,
+                                             num_sms_current(), (cudaStream_t)stream));
+}
+
+int moe_route_topk(const void* x, const void* w_router, const float* bias, const moe_shape_t* shape,
+                   int32_t* idx, float* gate, float* logits_out, uint8_t* xq_codes,
+                   uint8_t* xq_scales, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    if (!x || !w_router || !idx || !gate) return MOE_ERR_INVALID_ARG;
+    if ((xq_codes != nullptr) != (xq_scales != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (xq_codes && (s.dtype != MOE_MXFP8 || !aligned16(xq_codes))) return MOE_ERR_INVALID_ARG;
+    (void)workspace;
+    (void)workspace_bytes;
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = cuda_status(launch_route_topk_simt(x, w_router, bias, s.N, s.H, s.E, s.k, s.dtype, idx,
+                                            gate, logits_out, st));
+    if (rc || !xq_codes) return rc;
+    return cuda_status(launch_quantize_mxfp8(x, MOE_BF16, s.N, s.H, xq_codes, xq_scales,
+                                             num_sms_current(), st));
+}
+
+int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, int32_t* offsets,
+               int32_t* sched, int32_t* inv, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    rc = check_ws(shape, nullptr, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (!counts || !offsets || (s.N > 0 && (!idx || !sched || !inv))) return MOE_ERR_INVALID_ARG;
+    const Plan pl = make_plan(s, nullptr);
+    return cuda_status(launch_layout(idx, s.N, s.k, s.E, s.S, counts, offsets, sched, inv,
+                                     at<int32_t>(workspace, pl.cnt), at<int32_t>(workspace, pl.base),
+                                     at<WsHeader>(workspace, pl.header), (cudaStream_t)stream));
+}
+
+int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
+                      const moe_shape_t* shape, const int32_t* sched, int slot_begin,
+                      int slot_count, void* ring, void* ring_scales, int ring_slots,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    const int T = s.N * s.k;
+    if (slot_begin < 0 || slot_count < 0 || slot_begin + slot_count > T || ring_slots <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (slot_count == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!shard_rows || !sched || !ring || !aligned16(ring)) return MOE_ERR_INVALID_ARG;
+    if (mx && (!shard_scales || !ring_scales)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    const int row_bytes = s.H * (int)op_elem(s.dtype);
+    const int scale_bytes = mx ? s.H / 32 : 0;
+    return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, slot_begin, slot_count,
+                                            s.S, s.N / s.S, row_bytes, scale_bytes, ring,
+                                            ring_scales, ring_slots, num_sms_current(),
+                                            at<WsHeader>(workspace, 0), (cudaStream_t)stream));
+}
+
+int moe_expert_ffn(const void* a, const void* a_scales, const int32_t* offsets,
+                   const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                   const void* w_d_scales, const moe_shape_t* shape, void* y, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    rc = check_ws(shape, nullptr, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!a || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (mx && (!a_scales || !w_gu_scales || !w_d_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if (mx && (((uintptr_t)a_scales & 3) || ((uintptr_t)w_gu_scales & 3) || ((uintptr_t)w_d_scales & 3)))
+        return MOE_ERR_INVALID_ARG;
+    return expert_ffn_impl(a, a_scales, s.N * s.k, offsets, w_gate_up, w_gu_scales, w_down,
+                           w_d_scales, s, y, workspace, kDefaultTimeoutNs, (cudaStream_t)stream);
+}
+
+int moe_combine(const void* y, const int32_t* inv, const float* gate, const moe_shape_t* shape,
+                void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    if (!y || !inv || !gate || !out || !aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_combine(y, inv, gate, s.N, s.H, s.k, s.N * s.k, s.dtype, out,
+                                      num_sms_current(), at<WsHeader>(workspace, 0),
+                                      (cudaStream_t)stream));
+}
+
+int moe_forward(const void* x, const void* w_router, const float* bias, const void* w_gate_up,
+                const void* w_gu_scales, const void* w_down, const void* w_d_scales,
+                const moe_shape_t* shape, const moe_params_t* params, void* out, int32_t* idx_out,
+                float* gate_out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    rc = check_ws(shape, params, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!x || !w_router || !w_gate_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+    if (mx && (!w_gu_scales || !w_d_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(w_gate_up) || !aligned16(w_down))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const Plan pl = make_plan(s, params);
+    void* ws = workspace;
+    WsHeader* hdr = at<WsHeader>(ws, pl.header);
+    const int T = s.N * s.k;
+    const int rows = s.N / s.S;
+    int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, pl.idx);
+    float* gate = gate_out ? gate_out : at<float>(ws, pl.gate);
+    int32_t* counts = at<int32_t>(ws, pl.counts);
+    int32_t* offsets = at<int32_t>(ws, pl.offsets);
+    int32_t* sched = at<int32_t>(ws, pl.sched);
+    int32_t* inv = at<int32_t>(ws, pl.inv);
+
+    // 1. router + top-k (+ the MXFP8 copy of x each source shard serves)
+    uint8_t* xq = mx ? at<uint8_t>(ws, pl.xq) : nullptr;
+    uint8_t* xq_sf = mx ? at<uint8_t>(ws, pl.xq_sf) : nullptr;
+    rc = moe_route_topk(x, w_router, bias, shape, idx, gate, nullptr, xq, xq_sf, ws,
+                        workspace_bytes, stream);
+    if (rc) return rc;
+    // 2. layout
+    rc = cuda_status(launch_layout(idx, s.N, s.k, s.E, s.S, counts, offsets, sched, inv,
+                                   at<int32_t>(ws, pl.cnt), at<int32_t>(ws, pl.base), hdr, st));
+    if (rc) return rc;
+    // 3. pull dispatch through the table of S source-shard pointers
+    const uint8_t** tab = at<const uint8_t*>(ws, pl.shard_tab);
+    const uint8_t** tab_sf = at<const uint8_t*>(ws, pl.shard_sf_tab);
+    const int row_bytes = s.H * (int)op_elem(s.dtype);
+    const int tb = (s.S + 127) / 128;
+    fill_shard_table_kernel<<<tb, 128, 0, st>>>(tab, mx ? xq : (const uint8_t*)x,
+                                                (int64_t)rows * row_bytes, s.S);
+    if (mx)
+        fill_shard_table_kernel<<<tb, 128, 0, st>>>(tab_sf, xq_sf, (int64_t)rows * (s.H / 32), s.S);
+    rc = cuda_status(cudaGetLastError());
+    if (rc) return rc;
+    void* ring = at<void>(ws, pl.ring);
+    void* ring_sf = mx ? at<void>(ws, pl.ring_sf) : nullptr;
+    rc = cuda_status(launch_dispatch_pull((const void* const*)tab, (const void* const*)tab_sf, sched,
+                                          0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
+                                          ring_sf, pl.ring_slots, num_sms_current(), hdr, st));
+    if (rc) return rc;
+    // 4. grouped SwiGLU expert FFN
+    void* y = at<void>(ws, pl.y);
+    rc = expert_ffn_impl(ring, ring_sf, pl.ring_slots, offsets, w_gate_up, w_gu_scales, w_down,
+                         w_d_scales, s, y, ws, timeout_of(params), st);
+    if (rc) return rc;
+    // 5. combine + weighted merge
+    return cuda_status(launch_combine(y, inv, gate, s.N, s.H, s.k, T, s.dtype, out,
+                                      num_sms_current(), hdr, st));
+}
+
+int moe_forward_fused(const void* x, const void* w_router, const float* bias,
+                      const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                      const void* w_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                      void* out, int32_t* idx_out, float* gate_out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    (void)x; (void)w_router; (void)bias; (void)w_gate_up; (void)w_gu_scales; (void)w_down;
+    (void)w_d_scales; (void)shape; (void)params; (void)out; (void)idx_out; (void)gate_out;
+    (void)workspace; (void)workspace_bytes; (void)stream;
+    return MOE_ERR_UNSUPPORTED;
+}
+
+int moe_min_minibatch(int waves, int compute_sms, int tile_m, int tile_n, int I) {
+    if (waves <= 0 || compute_sms <= 0 || tile_m <= 0 || tile_n <= 0 || I <= 0) return 0;
+    const long long num = (long long)waves * compute_sms * tile_m * tile_n;
+    const long long den = 2LL * I;
+    return (int)((num + den - 1) / den);
+}
+
+}  // extern "C"

@@ -1,0 +1,60 @@
+// kernels.cuh -- launch functions of libmoe's kernels (host side), shared between
+// the kernel sources and the C-ABI layer in api.cu.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kLayoutChunk = 256;  // flat (token, choice) entries per layout chunk
+inline int layout_chunks(int T) { return (T + kLayoutChunk - 1) / kLayoutChunk; }
+
+cudaError_t launch_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
+                                  uint8_t* codes, uint8_t* scales, int num_sms,
+                                  cudaStream_t stream);
+
+cudaError_t launch_route_topk_simt(const void* x, const void* w, const float* bias, int N, int H,
+                                   int E, int k, int dtype, int32_t* idx, float* gate,
+                                   float* logits_out, cudaStream_t stream);
+
+cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_t* counts,
+                          int32_t* offsets, int32_t* sched, int32_t* inv, int32_t* cnt_scratch,
+                          int32_t* base_scratch, WsHeader* ws, cudaStream_t stream);
+
+cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
+                                 const int32_t* sched, int slot_begin, int slot_count, int S,
+                                 int rows_per_shard, int row_bytes, int scale_bytes, void* ring,
+                                 void* ring_scales, int ring_slots, int num_sms, WsHeader* ws,
+                                 cudaStream_t stream);
+
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* gate, int N, int H,
+                           int k, int T, int dtype, void* out, int num_sms, WsHeader* ws,
+                           cudaStream_t stream);
+
+cudaError_t launch_ffn_f32(const float* a, const int32_t* offsets, const float* wgu,
+                           const float* wd, int T, int H, int I, int E, float* h_scratch, float* y,
+                           int num_sms, cudaStream_t stream);
+
+// One call of the tensor-core expert FFN (GEMM1 + SwiGLU, then GEMM2).
+struct TcFfnCall {
+    bool mx;                  // MXFP8 operands (else BF16)
+    int T, H, I, E;
+    int a_rows;               // rows of a / h / y buffers (>= T)
+    const void* a;            // [a_rows][H]
+    const void* a_sf;         // [a_rows][H/32] (MXFP8)
+    const int32_t* offsets;   // [E+1]
+    const void* w_gate_up;    // [E][2I][H]
+    const void* w_gu_sf;      // [E][2I][H/32] (MXFP8)
+    const void* w_down;       // [E][H][I]
+    const void* w_d_sf;       // [E][H][I/32] (MXFP8)
+    void* h;                  // [a_rows][I] scratch
+    void* h_sf;               // [a_rows][I/32] scratch (MXFP8)
+    void* y;                  // [a_rows][H] BF16
+    WsHeader* ws;
+    unsigned long long timeout_ns;
+    int grid;                 // persistent CTAs (one per SM)
+};
+
+cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,154 @@
+// layout.cu -- sort-free token layout ("schedule").  The flat list of choices
+// (n, j) -> expert is placed expert-contiguously with a stable counting placement,
+// in three short kernels: per-chunk expert counts (warp match + shared-memory
+// atomics), an exclusive scan over (expert, chunk), and a warp-ballot rank that
+// writes each choice's slot, the two-column (source shard, row) pull schedule and
+// the inverse map.  ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost
+// on NVIDIA GB300 NVL72", section 01: count per expert, decide placement, keep an
+// expert's tokens together for the grouped GEMM; [Kittens] = "Смесь котят…",
+// pull paragraph: a two-column schedule built without sorting.)
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kLayoutWarps = 8;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Chunk c covers flat choices [c*kLayoutChunk, min((c+1)*kLayoutChunk, T)).
+// One warp per chunk; counts go to cnt[c][e].
+__global__ void __launch_bounds__(kLayoutWarps * 32) layout_count_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int nchunks, int32_t* __restrict__ cnt,
+    WsHeader* ws) {
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int32_t* hist = sh + warp * E;
+    const int c = blockIdx.x * kLayoutWarps + warp;
+    if (c >= nchunks) return;
+    for (int e = lane; e < E; e += 32) hist[e] = 0;
+    __syncwarp();
+    const int begin = c * kLayoutChunk;
+    const int end = min(begin + kLayoutChunk, T);
+    for (int base = begin; base < end; base += 32) {
+        const int t = base + lane;
+        int e = (t < end) ? idx[t] : -1;
+        if (t < end && (e < 0 || e >= E)) {
+            set_status(ws, MOE_ERR_DEVICE_CHECK);
+            e = -1;
+        }
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && (same & lanemask_lt()) == 0) atomicAdd(&hist[e], __popc(same));
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) cnt[(int64_t)c * E + e] = hist[e];
+}
+
+// One block.  base[c][e] = offsets[e] + sum_{c' < c} cnt[c'][e];
+// counts[e] = sum_c cnt[c][e]; offsets = exclusive scan of counts.
+__global__ void __launch_bounds__(1024) layout_scan_kernel(const int32_t* __restrict__ cnt,
+                                                           int nchunks, int E,
+                                                           int32_t* __restrict__ base,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets) {
+    extern __shared__ int32_t tot[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            base[(int64_t)c * E + e] = run;
+            run += cnt[(int64_t)c * E + e];
+        }
+        tot[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan of tot[0..E) by warp 0: each lane owns a contiguous run
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (E + 31) / 32;
+        const int lo = min(lane * per, E), hi = min(lo + per, E);
+        int s = 0;
+        for (int e = lo; e < hi; ++e) s += tot[e];
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - s;
+        for (int e = lo; e < hi; ++e) {
+            const int c = tot[e];
+            tot[e] = run;
+            offsets[e] = run;
+            run += c;
+        }
+        if (lane == 31) offsets[E] = incl;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int off = tot[e];
+        for (int c = 0; c < nchunks; ++c) base[(int64_t)c * E + e] += off;
+    }
+}
+
+// One warp per chunk, walking its choices in flat order 32 at a time: the lanes
+// holding the same expert find each other with a match, rank themselves by lane
+// order, and the group's first lane advances the expert's cursor.
+__global__ void __launch_bounds__(kLayoutWarps * 32) layout_place_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int nchunks,
+    const int32_t* __restrict__ base, int rows_per_shard, int32_t* __restrict__ sched,
+    int32_t* __restrict__ inv) {
+    extern __shared__ int32_t sh[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int32_t* cursor = sh + warp * E;
+    const int c = blockIdx.x * kLayoutWarps + warp;
+    if (c >= nchunks) return;
+    for (int e = lane; e < E; e += 32) cursor[e] = base[(int64_t)c * E + e];
+    __syncwarp();
+    const int begin = c * kLayoutChunk;
+    const int end = min(begin + kLayoutChunk, T);
+    for (int b = begin; b < end; b += 32) {
+        const int t = b + lane;
+        int e = (t < end) ? idx[t] : -1;
+        if (e >= E) e = -1;
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & lanemask_lt());
+        const int cur = (e >= 0) ? cursor[e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+            const int slot = cur + rank;
+            const int n = t / k;
+            sched[2 * (int64_t)slot] = n / rows_per_shard;
+            sched[2 * (int64_t)slot + 1] = n % rows_per_shard;
+            inv[t] = slot;
+            if (rank == 0) cursor[e] = cur + __popc(same);
+        }
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_t* counts,
+                          int32_t* offsets, int32_t* sched, int32_t* inv, int32_t* cnt_scratch,
+                          int32_t* base_scratch, WsHeader* ws, cudaStream_t stream) {
+    const int T = N * k;
+    const int nchunks = layout_chunks(T);
+    const int blocks = (nchunks + kLayoutWarps - 1) / kLayoutWarps;
+    const size_t smem_w = sizeof(int32_t) * kLayoutWarps * E;
+    if (nchunks > 0) {
+        layout_count_kernel<<<blocks, kLayoutWarps * 32, smem_w, stream>>>(idx, T, E, nchunks,
+                                                                          cnt_scratch, ws);
+    }
+    layout_scan_kernel<<<1, 1024, sizeof(int32_t) * E, stream>>>(cnt_scratch, nchunks, E,
+                                                                base_scratch, counts, offsets);
+    if (nchunks > 0) {
+        layout_place_kernel<<<blocks, kLayoutWarps * 32, smem_w, stream>>>(
+            idx, T, k, E, nchunks, base_scratch, N / S, sched, inv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,62 @@
+"""Device-side plumbing around the C ABI: holds a layer's device tensors (weights
+quantised once by libmoe for the MXFP8 dtype), its workspace, and calls
+moe_forward / moe_forward_fused.  PyTorch only allocates memory and supplies the
+stream here; every step of the layer runs in libmoe's kernels."""
+from __future__ import annotations
+
+import torch
+
+from . import moe as M
+from .synth import Workload, master_dtype
+
+
+def quantize_mxfp8(t: torch.Tensor):
+    """MXFP8 codes and scales of t along its last axis, made by libmoe."""
+    K = t.shape[-1]
+    codes = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+    scales = torch.empty(t.shape[:-1] + (K // 32,), dtype=torch.uint8, device=t.device)
+    M.moe_quantize_mxfp8(t.contiguous(), codes, scales)
+    return codes, scales
+
+
+class MoeLayer:
+    def __init__(self, w: Workload, inputs: dict, params: M.Params | None = None,
+                 device: str = "cuda", keep_master: bool = False):
+        self.w = w
+        self.shape = M.Shape.of(w)
+        self.params = params
+        dev = torch.device(device)
+        self.x = inputs["x"].to(dev).contiguous()
+        self.w_router = inputs["w_router"].to(dev).contiguous()
+        self.bias = None if inputs.get("bias") is None else inputs["bias"].to(dev).float().contiguous()
+        wgu = inputs["w_gate_up"].to(dev).contiguous()
+        wd = inputs["w_down"].to(dev).contiguous()
+        if w.dtype == "mxfp8":
+            self.wgu, self.wgu_sf = quantize_mxfp8(wgu)
+            self.wd, self.wd_sf = quantize_mxfp8(wd)
+        else:
+            self.wgu, self.wgu_sf, self.wd, self.wd_sf = wgu, None, wd, None
+        if keep_master:
+            self.master = (wgu, wd)
+        else:
+            del wgu, wd
+        nbytes = M.moe_workspace_bytes(self.shape, params)
+        if nbytes == 0:
+            raise M.MoeError("moe_workspace_bytes", M.MOE_ERR_INVALID_ARG)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        M.moe_workspace_init(self.ws)
+        out_dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.out = torch.empty((w.N, w.H), dtype=out_dt, device=dev)
+        self.idx = torch.empty((w.N, w.k), dtype=torch.int32, device=dev)
+        self.gate = torch.empty((w.N, w.k), dtype=torch.float32, device=dev)
+
+    def forward(self, x: torch.Tensor | None = None, fused: bool = False, params=None,
+                out: torch.Tensor | None = None):
+        fn = M.moe_forward_fused if fused else M.moe_forward
+        fn(self.x if x is None else x, self.w_router, self.bias, self.wgu, self.wgu_sf, self.wd,
+           self.wd_sf, self.shape, params if params is not None else self.params,
+           self.out if out is None else out, self.idx, self.gate, self.ws)
+        return self.out if out is None else out
+
+    def device_status(self) -> int:
+        return M.moe_last_device_status(self.ws)
