@@ -1,0 +1,424 @@
+"""Benchmark of the forward MoE layer on one GB300 (replicas on N GPUs).
+
+Workload: the DeepSeek-V3-shaped MXFP8 layer (N=8192 tokens, H=7168, I=2048,
+E=256 experts, top-8, 64 virtual source shards of 128 tokens), seeded synthetic
+inputs drawn on the device.  One step = one whole forward layer (route + quantise
+x, layout, pull dispatch, grouped SwiGLU expert FFN, combine).
+
+Prints one JSON line (rank 0).  `value` is device-timed tokens/s of moe_forward
+with inputs resident in HBM; `e2e` is the same call from pinned host buffers with
+the host<->device copies inside the timed region; `stages` breaks one step down by
+entry point; `roofline` is for the dominant kernel (the expert FFN's two grouped
+GEMM launches); `cpu_baseline` times the oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+                  [--fused]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from token_dispatch_expert_top_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s & TFLOP/s (% MXFP8 peak); dispatch/combine HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0      # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the GPU arm
+class StagedStep:
+    """The same kernels as moe_forward, issued entry point by entry point so that
+    CUDA events can bracket each stage on the launching stream."""
+
+    def __init__(self, layer):
+        from token_dispatch_expert_top_gb300 import moe as M
+        self.M = M
+        self.L = layer
+        w = layer.w
+        dev = layer.x.device
+        T = w.T
+        mx = w.dtype == "mxfp8"
+        self.mx = mx
+        opb = {"f32": 4, "bf16": 2, "mxfp8": 1}[w.dtype]
+        self.idx = torch.empty((w.N, w.k), dtype=torch.int32, device=dev)
+        self.gate = torch.empty((w.N, w.k), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+        self.sched = torch.empty((T, 2), dtype=torch.int32, device=dev)
+        self.inv = torch.empty((w.N, w.k), dtype=torch.int32, device=dev)
+        if mx:
+            self.xq = torch.empty((w.N, w.H), dtype=torch.uint8, device=dev)
+            self.xq_sf = torch.empty((w.N, w.H // 32), dtype=torch.uint8, device=dev)
+            src, src_sf = self.xq, self.xq_sf
+        else:
+            self.xq = self.xq_sf = None
+            src, src_sf = layer.x, None
+        rows = w.rows_per_shard
+        self.tab = torch.tensor([src.data_ptr() + s * rows * w.H * opb for s in range(w.S)],
+                                dtype=torch.int64, device=dev)
+        self.tab_sf = None if not mx else torch.tensor(
+            [src_sf.data_ptr() + s * rows * (w.H // 32) for s in range(w.S)], dtype=torch.int64, device=dev)
+        self.ring = torch.empty((T, w.H * opb), dtype=torch.uint8, device=dev)
+        self.ring_sf = torch.empty((T, w.H // 32), dtype=torch.uint8, device=dev) if mx else None
+        self.y = torch.empty((T, w.H), dtype=layer.out.dtype, device=dev)
+        self.names = ["route", "layout", "dispatch", "expert_ffn", "combine"]
+
+    def run(self, events=None):
+        M, L, w = self.M, self.L, self.L.w
+        ev = events or [None] * 6
+        if ev[0]:
+            ev[0].record()
+        M.moe_route_topk(L.x, L.w_router, L.bias, L.shape, self.idx, self.gate, None, self.xq,
+                         self.xq_sf, L.ws)
+        if ev[1]:
+            ev[1].record()
+        M.moe_layout(self.idx, L.shape, self.counts, self.offsets, self.sched, self.inv, L.ws)
+        if ev[2]:
+            ev[2].record()
+        M.moe_dispatch_pull(self.tab, self.tab_sf, L.shape, self.sched, 0, w.T, self.ring,
+                            self.ring_sf, w.T, L.ws)
+        if ev[3]:
+            ev[3].record()
+        M.moe_expert_ffn(self.ring, self.ring_sf, self.offsets, L.wgu, L.wgu_sf, L.wd, L.wd_sf,
+                         L.shape, self.y, L.ws)
+        if ev[4]:
+            ev[4].record()
+        M.moe_combine(self.y, self.inv, self.gate, L.shape, L.out, L.ws)
+        if ev[5]:
+            ev[5].record()
+
+
+def kernel_launches_per_step(w, fused: bool) -> int:
+    # route (1) + quantise x (1, MXFP8) + layout (3) + shard tables (1-2) + dispatch (1)
+    # + expert FFN (2: GEMM1+SwiGLU, GEMM2) + combine (1)
+    n = 1 + 3 + 1 + 2 + 1
+    if w.dtype == "mxfp8":
+        n += 1 + 2
+    else:
+        n += 1
+    if w.dtype == "f32":
+        n += 0
+    return n
+
+
+def gpu_arm(args, rank, world):
+    from token_dispatch_expert_top_gb300 import moe as M
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w, device=dev)
+    layer = MoeLayer(w, inp, device=str(dev))
+    del inp
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- value: moe_forward, device-resident inputs
+    for _ in range(args.warmup):
+        layer.forward(fused=args.fused)
+    status = layer.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {M.status_name(status)} after warm-up")
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            layer.forward(fused=args.fused)
+        ev1.record(stream)
+        barrier()
+    t_ms = ev0.elapsed_time(ev1)
+    status = layer.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {M.status_name(status)} in timed region")
+    if world > 1:
+        t = torch.tensor([t_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_ms = float(t.item())
+    ms_per_step = t_ms / args.steps
+    tokens_per_s = world * w.N * args.steps / (t_ms / 1e3)
+
+    # ---- stage breakdown through the individual entry points (same kernels)
+    st = StagedStep(layer)
+    for _ in range(2):
+        st.run()
+    torch.cuda.synchronize()
+    sums = [0.0] * 5
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        st.run(evs)
+        torch.cuda.synchronize()
+        for i in range(5):
+            sums[i] += evs[i].elapsed_time(evs[i + 1])
+    stage_ms = {n: s / args.steps for n, s in zip(st.names, sums)}
+    assert layer.device_status() == 0
+
+    # ---- e2e: the public call from pinned host buffers, copies inside the timed region
+    x_host = layer.x.cpu().pin_memory()
+    out_host = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
+    x_dev = torch.empty_like(layer.x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x=x_dev, fused=args.fused)
+        out_host.copy_(layer.out, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x=x_dev, fused=args.fused)
+        out_host.copy_(layer.out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * w.N * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    # ---- derived figures
+    peaks, peak_src = load_peaks()
+    ffn_flops = w.ffn_flops
+    opb = {"f32": 4, "bf16": 2, "mxfp8": 1}[w.dtype]
+    row_bytes = w.H * opb + (w.H // 32 if w.dtype == "mxfp8" else 0)
+    act = 4 if w.dtype == "f32" else 2
+    dispatch_bytes = w.N * row_bytes + w.T * row_bytes
+    combine_bytes = w.T * w.H * act + w.N * w.H * act + w.T * 8
+    ffn_s = stage_ms["expert_ffn"] / 1e3
+    ffn_tflops = ffn_flops / ffn_s / 1e12
+    if w.dtype == "mxfp8":
+        tensor_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+        peak_note = f"MXFP8 = {peak_src} sustained BF16 x {FP8_PER_BF16:g} (nominal FP8/BF16)"
+    elif w.dtype == "bf16":
+        tensor_peak = peaks["bf16_tflops_sustained"]
+        peak_note = f"{peak_src} sustained BF16"
+    else:
+        tensor_peak = None
+        peak_note = "FP32 SIMT"
+    roofline = {
+        "kernel": "expert FFN grouped GEMMs (GEMM1+SwiGLU and GEMM2 launches of moe_expert_ffn)",
+        "bound": "tensor", "achieved": round(ffn_tflops, 2),
+        "peak": round(tensor_peak, 1) if tensor_peak else None, "unit": "TFLOP/s",
+        "frac": round(ffn_tflops / tensor_peak, 4) if tensor_peak else None,
+        "traffic": None, "peak_source": peak_note,
+        "algorithmic": f"{ffn_flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
+    }
+    hbm = peaks["hbm_gbs"]
+    disp_gbs = dispatch_bytes / (stage_ms["dispatch"] / 1e3) / 1e9
+    comb_gbs = combine_bytes / (stage_ms["combine"] / 1e3) / 1e9
+    layer_tflops = world * ffn_flops * args.steps / (t_ms / 1e3) / 1e12
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), drawn on the device)",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                   "S": w.S, "skew": w.skew, "path": "fused" if args.fused else "staged",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: ~11.6 GB of MXFP8 expert weights streamed per step"},
+        "layer_tflops": round(layer_tflops, 2),
+        "pct_mxfp8_peak_layer": round(layer_tflops / tensor_peak, 4) if tensor_peak else None,
+        "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "dispatch_gbs": round(disp_gbs, 1), "dispatch_frac_hbm": round(disp_gbs / hbm, 4),
+        "combine_gbs": round(comb_gbs, 1), "combine_frac_hbm": round(comb_gbs / hbm, 4),
+        "hbm_peak_gbs": hbm, "hbm_peak_source": peak_src,
+        "roofline": roofline,
+        "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    return res, layer
+
+
+# ------------------------------------------------------------- the oracle (CPU)
+def oracle_sample(w, inp, n_tokens: int, seed: int):
+    """One bounded sample of the layer on the oracle: routing and layout of all N
+    tokens, expert FFN and combine for n_tokens sampled tokens.  Returns seconds."""
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import numpy as np
+    import oracle as O
+
+    toks = np.random.default_rng(seed).choice(w.N, size=n_tokens, replace=False)
+
+    def weights(e):
+        return O.expert_operands(inp["w_gate_up"][e].cpu(), inp["w_down"][e].cpu(), w.dtype)
+
+    t0 = time.perf_counter()
+    O.forward({"x": inp["x"], "w_router": inp["w_router"], "bias": inp["bias"]}, w.E, w.k, w.S,
+              w.dtype, tokens=toks, weights=weights)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    dev = "cuda" if (w.name in synth.DEVICE_DRAWN and torch.cuda.is_available()) else "cpu"
+    inp = synth.make_inputs(w, device=dev)
+    n_tok = args.sample_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_sample(w, inp, n_tok, seed=i)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = n_tok * args.steps / total
+    sample = (f"per step: routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
+              f"random tokens (FP64 oracle)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                   "S": w.S, "skew": w.skew},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dsv3_mxfp8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--fused", action="store_true", help="time moe_forward_fused")
+    ap.add_argument("--sample-tokens", type=int, default=2,
+                    help="tokens per oracle sample (CPU baseline / reference arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl" if args.impl == "gb300" else "gloo")
+
+    if args.impl == "reference":
+        res = reference_arm(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    res, layer = gpu_arm(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            w = layer.w
+            del layer
+            torch.cuda.empty_cache()
+            inp = synth.make_inputs(w, device="cuda" if w.name in synth.DEVICE_DRAWN else "cpu")
+            n_tok = args.sample_tokens
+            dt = oracle_sample(w, inp, n_tok, seed=12345)
+            res["cpu_baseline"] = {
+                "value": round(n_tok / dt, 4), "unit": "tokens/s", "cores": cpu_cores(),
+                "kind": "oracle",
+                "sample": f"routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
+                          f"random tokens, FP64 oracle, {dt:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -68,10 +68,14 @@ WORKLOADS = {
     # Same shapes with a Zipf-like router bias b_e = 3*log(1/rank_e).
     "dsv3_mxfp8_skew": Workload("dsv3_mxfp8_skew", N=8192, H=7168, I=2048, E=256, k=8, S=64,
                                 dtype="mxfp8", skew=3.0),
+    # Profiling stand-in: DeepSeek-V3 shapes and per-expert load (T/E = 256 rows),
+    # 32 experts, so a capture holds ~1.4 GB of weights instead of 11.6 GB.
+    "dsv3_mxfp8_e32": Workload("dsv3_mxfp8_e32", N=1024, H=7168, I=2048, E=32, k=8, S=8,
+                               dtype="mxfp8"),
 }
 
 # Workloads whose tensors are drawn on the device generator (too large for the host).
-DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew"}
+DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_e32"}
 
 
 def master_dtype(w: Workload) -> torch.dtype:
