@@ -226,6 +226,27 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
                       const moe_params_t* params, void* out, int32_t* idx_out, float* gate_out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* moe_layout without a workspace, for callers that cannot allocate device memory:
+ * code running inside a stream capture (an allocation there breaks the capture), a
+ * serving process that reserves all its device memory at start-up and allocates
+ * nothing afterwards, or a plug-in whose host owns the allocator.  The pages
+ * describe no such entry point; it exists for those callers only.
+ *   Same arguments and results as moe_layout, minus the workspace.  Its scratch
+ *   (per-chunk expert counts and their scan) is a fixed 1 MiB __device__ array
+ *   compiled into the library, resident on every GPU that loads it until the
+ *   process exits.  Shapes with ceil(N*k/256) * E > 131072 are rejected with
+ *   MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress (that device must be current); make that first call
+ *   before any stream capture begins.
+ *   Every call on a device uses that device's one copy of the array and leaves
+ *   its contents behind: calls that overlap on the same GPU (for example on two
+ *   streams) race.  Calls on different GPUs use different copies.
+ *   Expert indices out of range are skipped but not reported (there is no status
+ *   word without a workspace). */
+int moe_layout_noalloc(const int32_t* idx, const moe_shape_t* shape, int32_t* counts,
+                       int32_t* offsets, int32_t* sched, int32_t* inv, void* stream);
+
 /* Smallest minibatch (in slots) that gives `waves` full waves of GEMM1 tiles of
  * tile_m x tile_n over `compute_sms` SMs when GEMM1 has 2*I output columns
  * ([MoK-2.37x] section 02: a minibatch should form at least two full waves; the

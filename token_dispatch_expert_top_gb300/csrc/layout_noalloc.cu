@@ -1,0 +1,79 @@
+// layout_noalloc.cu -- moe_layout_noalloc: the sort-free layout for callers that
+// cannot allocate device memory, with its scratch in a fixed device array.
+//
+// Who needs it: code that runs where cudaMalloc is not an option -- inside a
+// region being captured into a CUDA graph (an allocation there breaks the
+// capture), in a serving process that reserves all of its device memory up front
+// and forbids allocation afterwards, or in a plug-in whose host owns the allocator
+// and hands out no scratch.  moe_layout needs a caller-supplied workspace for its
+// per-chunk counts; this variant needs none, because that scratch lives in a
+// file-scope __device__ array that is part of the library's image.
+//
+// The array is LAYOUT_NOALLOC_SCRATCH_BYTES (1 MiB) on every GPU that loads the
+// library and stays allocated until the process exits.  It holds the per-chunk
+// expert counts and their scan, 2 * ceil(N*k/256) * E int32 values, which caps the
+// shape at ceil(N*k/256) * E <= 131072 (for example N*k = 131072 with E = 256).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+
+// The scratch.  In host code this name is only a stand-in for the device symbol:
+// its device address must be fetched with cudaGetSymbolAddress before a kernel
+// may be given it.
+static __device__ __align__(256) unsigned char g_layout_scratch[kNoAllocScratchBytes];
+
+// Device address of g_layout_scratch on the current device, looked up once per
+// device (with that device current) and cached.  Returns nullptr on failure.
+void* scratch_on_current_device(cudaError_t* err) {
+    static std::mutex mu;
+    static void* addr[256] = {};
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= 256) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        *err = cudaGetSymbolAddress(&p, g_layout_scratch);
+        if (*err != cudaSuccess || p == nullptr) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_layout_noalloc(const int32_t* idx, const moe_shape_t* shape, int32_t* counts,
+                                  int32_t* offsets, int32_t* sched, int32_t* inv, void* stream) {
+    using namespace moe;
+    if (!shape) return MOE_ERR_INVALID_ARG;
+    const moe_shape_t& s = *shape;
+    if (s.N < 0 || s.E <= 0 || s.k <= 0 || s.S <= 0 || s.k > s.E || s.N % s.S != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s.k > 32 || s.E > 1024 || (int64_t)s.N * s.k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+    if (!counts || !offsets || (s.N > 0 && (!idx || !sched || !inv))) return MOE_ERR_INVALID_ARG;
+    const int T = s.N * s.k;
+    const size_t per_array = sizeof(int32_t) * (size_t)layout_chunks(T) * (size_t)s.E;
+    const size_t per_array_padded = (per_array + 255) & ~(size_t)255;
+    if (2 * per_array_padded > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;  // shape too large
+    cudaError_t err = cudaSuccess;
+    uint8_t* scratch = static_cast<uint8_t*>(scratch_on_current_device(&err));
+    if (!scratch) return MOE_ERR_CUDA;
+    // Both arrays are written in full before they are read, so stale contents
+    // from an earlier call need no clearing.
+    int32_t* cnt = reinterpret_cast<int32_t*>(scratch);
+    int32_t* base = reinterpret_cast<int32_t*>(scratch + per_array_padded);
+    err = launch_layout(idx, s.N, s.k, s.E, s.S, counts, offsets, sched, inv, cnt, base,
+                        /*ws=*/nullptr, (cudaStream_t)stream);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -26,7 +26,7 @@ DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8}
 ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_last_device_status", "moe_status_string",
     "moe_quantize_mxfp8", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
-    "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch",
+    "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
 )
 
 
@@ -76,6 +76,7 @@ _SIGS = {
     "moe_forward_fused": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _prm, _vp, _vp, _vp, _vp,
                                _sz, _vp]),
     "moe_min_minibatch": (_i, [_i, _i, _i, _i, _i]),
+    "moe_layout_noalloc": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -189,3 +190,10 @@ def moe_forward_fused(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_sca
 
 def moe_min_minibatch(waves: int, compute_sms: int, tile_m: int, tile_n: int, I: int) -> int:
     return _lib.moe_min_minibatch(waves, compute_sms, tile_m, tile_n, I)
+
+
+def moe_layout_noalloc(idx, shape: Shape, counts, offsets, sched, inv, stream=None) -> None:
+    """moe_layout for callers that cannot allocate: no workspace argument; the
+    library's fixed device scratch array is used instead (see include/moe.h)."""
+    _check("moe_layout_noalloc", _lib.moe_layout_noalloc(
+        _p(idx), ctypes.byref(shape), _p(counts), _p(offsets), _p(sched), _p(inv), _stream(stream)))
