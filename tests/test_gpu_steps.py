@@ -93,6 +93,23 @@ def test_route_topk(M, w):
     np.testing.assert_array_equal(g_idx[ok], r_idx[ok])
 
 
+@pytest.mark.parametrize("N,H,E,k", [(640, 512, 256, 8), (200, 1024, 32, 4), (8192, 7168, 256, 8)])
+def test_route_topk_fused_x_quantisation_bit_exact(M, N, H, E, k):
+    """The MXFP8 copy of x written by the router pass equals the oracle's quantiser."""
+    w = synth.Workload("route_xq", N=N, H=H, I=128, E=E, k=k, S=N // 8 if N % 8 == 0 else 1,
+                       dtype="mxfp8")
+    inp = synth.make_inputs(w, device="cpu", with_weights=False)
+    shape = M.Shape.of(w)
+    idx = torch.empty((N, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((N, k), dtype=torch.float32, device="cuda")
+    xq = torch.empty((N, H), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((N, H // 32), dtype=torch.uint8, device="cuda")
+    M.moe_route_topk(inp["x"].cuda(), inp["w_router"].cuda(), None, shape, idx, gate, None, xq, xs)
+    oc, os_ = O.quantize_mxfp8(O._f64(inp["x"]))
+    np.testing.assert_array_equal(to_np(xs), os_)
+    np.testing.assert_array_equal(to_np(xq), oc)
+
+
 # -------------------------------------------------------------------------- layout
 def _layout_case(M, idx_np, E, S):
     N, k = idx_np.shape

@@ -209,9 +209,13 @@ int moe_route_topk(const void* x, const void* w_router, const float* bias, const
     if (!x || !w_router || !idx || !gate) return MOE_ERR_INVALID_ARG;
     if ((xq_codes != nullptr) != (xq_scales != nullptr)) return MOE_ERR_INVALID_ARG;
     if (xq_codes && (s.dtype != MOE_MXFP8 || !aligned16(xq_codes))) return MOE_ERR_INVALID_ARG;
-    (void)workspace;
-    (void)workspace_bytes;
     cudaStream_t st = (cudaStream_t)stream;
+    WsHeader* hdr = (workspace && workspace_bytes >= sizeof(WsHeader)) ? at<WsHeader>(workspace, 0)
+                                                                         : nullptr;
+    if (route_tc_supported(s.dtype, s.H, s.E, s.k))
+        return cuda_status(launch_route_topk_tc(x, w_router, bias, s.N, s.H, s.E, s.k, idx, gate,
+                                                logits_out, xq_codes, xq_scales, hdr,
+                                                kDefaultTimeoutNs, st));
     rc = cuda_status(launch_route_topk_simt(x, w_router, bias, s.N, s.H, s.E, s.k, s.dtype, idx,
                                             gate, logits_out, st));
     if (rc || !xq_codes) return rc;

@@ -10,32 +10,35 @@ namespace moe {
 
 constexpr int kGatherWarps = 8;
 
-// Copy n16 16-byte units, lanes interleaved, U loads in flight per lane.
-template <int U>
-__device__ __forceinline__ void copy_v4(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
-                                        int n16, int lane) {
-    int j = lane;
-    for (; j + 32 * (U - 1) < n16; j += 32 * U) {
-        uint4 v[U];
+// Copy a row of n16 16-byte units (plus an optional second row of m16 units, the
+// scales) with every load of a batch issued before any store: up to 16 + 1
+// 16-byte loads in flight per lane.
+__device__ __forceinline__ void copy_rows_v4(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
+                                             int n16, uint8_t* __restrict__ dst2,
+                                             const uint8_t* __restrict__ src2, int m16, int lane) {
+    constexpr int U = 16;
+    for (int b = 0; b < n16 || b < m16; b += 32 * U) {
+        uint4 v[U], w;
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = ld_nc_v4(src + 16 * (int64_t)(j + 32 * u));
+        for (int u = 0; u < U; ++u) {
+            const int j = b + lane + 32 * u;
+            if (j < n16) v[u] = ld_nc_v4(src + 16 * (int64_t)j);
+        }
+        const int j2 = b + lane;
+        if (j2 < m16) w = ld_nc_v4(src2 + 16 * (int64_t)j2);
 #pragma unroll
-        for (int u = 0; u < U; ++u) st_v4(dst + 16 * (int64_t)(j + 32 * u), v[u]);
+        for (int u = 0; u < U; ++u) {
+            const int j = b + lane + 32 * u;
+            if (j < n16) st_v4(dst + 16 * (int64_t)j, v[u]);
+        }
+        if (j2 < m16) st_v4(dst2 + 16 * (int64_t)j2, w);
     }
-    for (; j < n16; j += 32) st_v4(dst + 16 * (int64_t)j, ld_nc_v4(src + 16 * (int64_t)j));
 }
 
 // Bytes not a multiple of 16 (small rows): 4-byte units.
 __device__ __forceinline__ void copy_u32(uint8_t* dst, const uint8_t* src, int n4, int lane) {
     for (int j = lane; j < n4; j += 32)
         reinterpret_cast<uint32_t*>(dst)[j] = reinterpret_cast<const uint32_t*>(src)[j];
-}
-
-__device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int bytes, int lane) {
-    if ((bytes & 15) == 0)
-        copy_v4<8>(dst, src, bytes >> 4, lane);
-    else
-        copy_u32(dst, src, bytes >> 2, lane);
 }
 
 // One warp per slot, grid-stride.  Slot t goes to ring row t % ring_slots.
@@ -56,11 +59,19 @@ __global__ void __launch_bounds__(kGatherWarps * 32) dispatch_pull_kernel(
             continue;
         }
         const int64_t dst_row = t % ring_slots;
-        copy_row(ring + dst_row * row_bytes, shard_rows[s] + (int64_t)r * row_bytes, row_bytes,
-                 lane);
-        if (scale_bytes)
-            copy_row(ring_scales + dst_row * scale_bytes,
-                     shard_scales[s] + (int64_t)r * scale_bytes, scale_bytes, lane);
+        uint8_t* drow = ring + dst_row * row_bytes;
+        const uint8_t* srow = shard_rows[s] + (int64_t)r * row_bytes;
+        uint8_t* dsc = scale_bytes ? ring_scales + dst_row * scale_bytes : nullptr;
+        const uint8_t* ssc = scale_bytes ? shard_scales[s] + (int64_t)r * scale_bytes : nullptr;
+        if ((row_bytes & 15) == 0 && (scale_bytes & 15) == 0) {
+            copy_rows_v4(drow, srow, row_bytes >> 4, dsc, ssc, scale_bytes >> 4, lane);
+        } else {
+            if ((row_bytes & 15) == 0)
+                copy_rows_v4(drow, srow, row_bytes >> 4, nullptr, nullptr, 0, lane);
+            else
+                copy_u32(drow, srow, row_bytes >> 2, lane);
+            if (scale_bytes) copy_u32(dsc, ssc, scale_bytes >> 2, lane);
+        }
     }
 }
 

@@ -28,6 +28,7 @@
 // clock); when one runs out the CTA records MOE_ERR_TIMEOUT and winds down.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 
@@ -35,22 +36,28 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int STAGES = 4;
+constexpr int SFG = 2;                                     // scale staging groups (4 K-stages each)
 constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
-constexpr int SFA_BYTES = 512;
-constexpr int SFB_BYTES = 1024;
+constexpr int SFA_BYTES = 512;                             // [32 lanes][4 words]: 128 rows x 4 K-steps
+constexpr int SFB_BYTES = 1024;                            // two such blocks (256 rows)
+constexpr int SFSA_BYTES = BM * 16;                        // staged scales: 128 rows x 16 B (4 stages)
+constexpr int SFSB_BYTES = BN * 16;
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;      // full[S], empty[S], tfull, tempty, drain
-constexpr int NUM_BARS = 2 * STAGES + 3;
+constexpr int OFF_SFSA = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int OFF_SFSB = OFF_SFSA + SFG * SFSA_BYTES;
+constexpr int OFF_BAR = OFF_SFSB + SFG * SFSB_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * SFG;        // full, empty, tfull, tempty, drain, sfull, sempty
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;           // tmem base, abort flag
 constexpr int OFF_MPRE = OFF_MISC + 16;                    // int32 mpre[E+1]
 constexpr int TMEM_COLS = 512;
 constexpr int TCOL_SFA = 256;                              // + stage*4
 constexpr int TCOL_SFB = 256 + 4 * STAGES;                 // + stage*8
-constexpr int THREADS = 256;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = (4 + EPI_WARPS) * 32;
 inline size_t smem_bytes(int E) { return 1024 + OFF_MPRE + sizeof(int32_t) * (E + 1); }
 }  // namespace tc
 
@@ -62,6 +69,7 @@ struct TcArgs {
     int I;                    // GEMM1: offset of the up rows inside w_gate_up
     int a_rows;               // rows of the A tensor (scale loads stay inside)
     int b_rows;               // rows of one expert's weight matrix (2I or H)
+    int sf_tma;               // MXFP8 with K % 512 == 0: scales staged by TMA
     const uint8_t* a_sf;      // MXFP8: [a_rows][K/32]
     const uint8_t* b_sf;      // MXFP8: [E][b_rows][K/32]
     uint8_t* out;             // GEMM1: h codes/BF16 [a_rows][I]; GEMM2: y BF16 [a_rows][H]
@@ -95,10 +103,16 @@ __device__ __forceinline__ Tile tile_at(int t, const int32_t* mpre, const int32_
     return tl;
 }
 
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
+    return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
+}
+
 template <bool MX, bool SWIGLU>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, TcArgs args) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmSFA,
+                           const __grid_constant__ CUtensorMap tmSFB, TcArgs args) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -109,6 +123,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 1;
     uint64_t* drain = tfull + 2;
+    uint64_t* sfull = tfull + 3;
+    uint64_t* sempty = sfull + SFG;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     int32_t* mpre = reinterpret_cast<int32_t*>(smem + OFF_MPRE);
@@ -116,6 +132,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int E = args.E;
     const int KB = args.K / (MX ? 128 : 64);   // K stages (128 bytes each)
+    const bool sf_tma = MX && args.sf_tma;
 
     // ---------------------------------------------------------------- prologue
     if (warp == 0 && lane == 0) {
@@ -124,12 +141,20 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
-        mbar_init(tempty, 4);
+        mbar_init(tempty, EPI_WARPS);
         mbar_init(drain, 1);
+        for (int g = 0; g < SFG; ++g) {
+            mbar_init(&sfull[g], 1);
+            mbar_init(&sempty[g], 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (sf_tma) {
+            prefetch_tmap(&tmSFA);
+            prefetch_tmap(&tmSFB);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -164,12 +189,30 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, g = 0;
+            uint32_t phase = 0, gphase = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
                 const Tile tl = tile_at(t, mpre, args.offsets, E, args.n_tiles);
+                const int brow0 = SWIGLU ? tl.n * 128 : tl.n * BN;
+                const int brow1 = SWIGLU ? args.I + tl.n * 128 : tl.n * BN + 128;
                 for (int kb = 0; kb < KB; ++kb) {
+                    if (sf_tma && (kb & 3) == 0) {
+                        if (!mbar_wait_bounded(&sempty[g], gphase ^ 1, abort_flag, args.ws, deadline)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* sa = smem + OFF_SFSA + g * SFSA_BYTES;
+                        uint8_t* sb = smem + OFF_SFSB + g * SFSB_BYTES;
+                        mbar_arrive_expect_tx(&sfull[g], SFSA_BYTES + SFSB_BYTES);
+                        tma_load_2d(sa, &tmSFA, &sfull[g], kb * 4, tl.row0);
+                        tma_load_3d(sb, &tmSFB, &sfull[g], kb * 4, brow0, tl.e);
+                        tma_load_3d(sb + SFSB_BYTES / 2, &tmSFB, &sfull[g], kb * 4, brow1, tl.e);
+                        if (++g == SFG) {
+                            g = 0;
+                            gphase ^= 1;
+                        }
+                    }
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) {
                         ok = false;
                         break;
@@ -180,11 +223,10 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                     const int kx = kb * (MX ? 128 : 64);
                     tma_load_2d(sa, &tmA, &full[stage], kx, tl.row0);
                     if (SWIGLU) {
-                        tma_load_3d(sb, &tmB, &full[stage], kx, tl.n * 128, tl.e);
-                        tma_load_3d(sb + B_BYTES / 2, &tmB, &full[stage], kx, args.I + tl.n * 128,
-                                    tl.e);
+                        tma_load_3d(sb, &tmB, &full[stage], kx, brow0, tl.e);
+                        tma_load_3d(sb + B_BYTES / 2, &tmB, &full[stage], kx, brow1, tl.e);
                     } else {
-                        tma_load_3d(sb, &tmB, &full[stage], kx, tl.n * BN, tl.e);
+                        tma_load_3d(sb, &tmB, &full[stage], kx, brow0, tl.e);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -243,38 +285,71 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             }
         }
     } else if (warp == 2) {
-        // -------------------------------------------- scale-factor loader (MXFP8)
+        // ------------------------------------------ scale factors (MXFP8 only)
+        // Each K-stage needs, for the A rows and for both 128-row halves of B, a
+        // [32 lanes][4 words] block: word j of lane r holds the four K-step scales of
+        // row 32j + r.  tcgen05.cp moves that block into tensor memory.
         if constexpr (MX) {
-            const int ksf = args.K / 32;                // scale bytes per row
-            const bool vec16 = (ksf % 16) == 0;         // 4 stages per 16-byte load
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, g = 0;
+            uint32_t phase = 0, gphase = 0;
             bool ok = true;
+            const int ksf = args.K / 32;                // scale bytes per row
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
                 const Tile tl = tile_at(t, mpre, args.offsets, E, args.n_tiles);
-                const uint8_t* bsf = args.b_sf + (int64_t)tl.e * args.b_rows * ksf;
-                int brow[8];
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        brow[c * 4 + j] = SWIGLU ? (c * args.I + tl.n * 128 + 32 * j + lane)
-                                                 : (tl.n * BN + c * 128 + 32 * j + lane);
-                for (int kb4 = 0; ok && kb4 < KB; kb4 += 4) {
-                    uint4 va[4], vb[8];
-                    const int nq = min(4, KB - kb4);
-                    if (vec16) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int row = tl.row0 + 32 * j + lane;
-                            va[j] = row < args.a_rows
-                                        ? *reinterpret_cast<const uint4*>(args.a_sf + (int64_t)row * ksf + kb4 * 4)
-                                        : make_uint4(0, 0, 0, 0);
+                if (sf_tma) {
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if ((kb & 3) == 0 &&
+                            !mbar_wait_bounded(&sfull[g], gphase, abort_flag, args.ws, deadline)) {
+                            ok = false;
+                            break;
                         }
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) {
+                            ok = false;
+                            break;
+                        }
+                        const int q = kb & 3;
+                        const uint8_t* sa = smem + OFF_SFSA + g * SFSA_BYTES + 4 * q;
+                        const uint8_t* sb = smem + OFF_SFSB + g * SFSB_BYTES + 4 * q;
+                        uint32_t a[4], b[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            a[j] = *reinterpret_cast<const uint32_t*>(sa + (32 * j + lane) * 16);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            vb[i] = *reinterpret_cast<const uint4*>(bsf + (int64_t)brow[i] * ksf + kb4 * 4);
-                    } else {
+                            b[i] = *reinterpret_cast<const uint32_t*>(sb + (32 * i + lane) * 16);
+                        uint4* sfa = reinterpret_cast<uint4*>(smem + OFF_SFA + stage * SFA_BYTES);
+                        uint4* sfb = reinterpret_cast<uint4*>(smem + OFF_SFB + stage * SFB_BYTES);
+                        sfa[lane] = make_uint4(a[0], a[1], a[2], a[3]);
+                        sfb[lane] = make_uint4(b[0], b[1], b[2], b[3]);
+                        sfb[32 + lane] = make_uint4(b[4], b[5], b[6], b[7]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&full[stage]);
+                            if (q == 3) mbar_arrive(&sempty[g]);
+                        }
+                        if (q == 3 && ++g == SFG) {
+                            g = 0;
+                            gphase ^= 1;
+                        }
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                } else {
+                    // scales whose rows are not 16-byte multiples: direct loads
+                    const uint8_t* bsf = args.b_sf + (int64_t)tl.e * args.b_rows * ksf;
+                    int brow[8];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            brow[c * 4 + j] = SWIGLU ? (c * args.I + tl.n * 128 + 32 * j + lane)
+                                                     : (tl.n * BN + c * 128 + 32 * j + lane);
+                    for (int kb4 = 0; ok && kb4 < KB; kb4 += 4) {
+                        uint4 va[4], vb[8];
+                        const int nq = min(4, KB - kb4);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int row = tl.row0 + 32 * j + lane;
@@ -291,26 +366,23 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
                                 w[q] = *reinterpret_cast<const uint32_t*>(bsf + (int64_t)brow[i] * ksf + (kb4 + q) * 4);
                             vb[i] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                    }
-                    for (int q = 0; q < nq; ++q) {
-                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) {
-                            ok = false;
-                            break;
-                        }
-                        auto pick = [q](const uint4& v) {
-                            return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
-                        };
-                        uint4* sfa = reinterpret_cast<uint4*>(smem + OFF_SFA + stage * SFA_BYTES);
-                        uint4* sfb = reinterpret_cast<uint4*>(smem + OFF_SFB + stage * SFB_BYTES);
-                        sfa[lane] = make_uint4(pick(va[0]), pick(va[1]), pick(va[2]), pick(va[3]));
-                        sfb[lane] = make_uint4(pick(vb[0]), pick(vb[1]), pick(vb[2]), pick(vb[3]));
-                        sfb[32 + lane] = make_uint4(pick(vb[4]), pick(vb[5]), pick(vb[6]), pick(vb[7]));
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&full[stage]);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1;
+                        for (int q = 0; q < nq; ++q) {
+                            if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) {
+                                ok = false;
+                                break;
+                            }
+                            uint4* sfa = reinterpret_cast<uint4*>(smem + OFF_SFA + stage * SFA_BYTES);
+                            uint4* sfb = reinterpret_cast<uint4*>(smem + OFF_SFB + stage * SFB_BYTES);
+                            sfa[lane] = make_uint4(word_of(va[0], q), word_of(va[1], q), word_of(va[2], q), word_of(va[3], q));
+                            sfb[lane] = make_uint4(word_of(vb[0], q), word_of(vb[1], q), word_of(vb[2], q), word_of(vb[3], q));
+                            sfb[32 + lane] = make_uint4(word_of(vb[4], q), word_of(vb[5], q), word_of(vb[6], q), word_of(vb[7], q));
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&full[stage]);
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1;
+                            }
                         }
                     }
                 }
@@ -318,7 +390,12 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------------ epilogue
-        const int q = warp & 3;                   // tensor-memory lane quarter
+        // Two warps per tensor-memory lane quarter, each taking half of the tile's
+        // columns.  A warp first moves its whole share of the accumulator into
+        // registers (converted), releases the accumulator to the MMA issuer, and
+        // only then writes to global memory, so the next tile's MMAs overlap it.
+        const int q = warp & 3;
+        const int half = (warp - 4) >> 2;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
             const Tile tl = tile_at(t, mpre, args.offsets, E, args.n_tiles);
@@ -328,8 +405,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
             const bool valid = row < tl.row_end;
             const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
             if constexpr (SWIGLU) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                uint32_t pk[2][16];
+                uint8_t sc[2];
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int c = half * 2 + c2;
                     uint32_t g[32], u[32];
                     tmem_ld_32x32b_x32(tq + 32 * c, g);
                     tmem_ld_32x32b_x32(tq + 128 + 32 * c, u);
@@ -338,48 +418,60 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         hv[i] = silu_f32(__uint_as_float(g[i])) * __uint_as_float(u[i]);
-                    const int col = tl.n * 128 + 32 * c;
-                    if (valid) {
+                    if constexpr (MX) {
+                        sc[c2] = mx_quantize32(hv, pk[c2]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[c2][i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+                if (valid) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int col = tl.n * 128 + 32 * (half * 2 + c2);
                         if constexpr (MX) {
-                            uint32_t codes[8];
-                            const uint8_t sc = mx_quantize32(hv, codes);
                             uint8_t* dst = args.out + (int64_t)row * args.out_ld + col;
-                            st_v4(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-                            st_v4(dst + 16, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-                            args.out_sf[(int64_t)row * (args.out_ld / 32) + col / 32] = sc;
+                            st_v4(dst, make_uint4(pk[c2][0], pk[c2][1], pk[c2][2], pk[c2][3]));
+                            st_v4(dst + 16, make_uint4(pk[c2][4], pk[c2][5], pk[c2][6], pk[c2][7]));
+                            args.out_sf[(int64_t)row * (args.out_ld / 32) + col / 32] = sc[c2];
                         } else {
                             uint8_t* dst = args.out + ((int64_t)row * args.out_ld + col) * 2;
 #pragma unroll
                             for (int p = 0; p < 4; ++p)
-                                st_v4(dst + 16 * p,
-                                      make_uint4(pack_bf16x2(hv[8 * p + 0], hv[8 * p + 1]),
-                                                 pack_bf16x2(hv[8 * p + 2], hv[8 * p + 3]),
-                                                 pack_bf16x2(hv[8 * p + 4], hv[8 * p + 5]),
-                                                 pack_bf16x2(hv[8 * p + 6], hv[8 * p + 7])));
+                                st_v4(dst + 16 * p, make_uint4(pk[c2][4 * p], pk[c2][4 * p + 1],
+                                                               pk[c2][4 * p + 2], pk[c2][4 * p + 3]));
                         }
                     }
                 }
             } else {
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[4][16];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
                     uint32_t v[32];
-                    tmem_ld_32x32b_x32(tq + 32 * c, v);
+                    tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v);
                     tmem_ld_wait();
-                    if (valid) {
-                        uint8_t* dst = args.out + ((int64_t)row * args.out_ld + tl.n * BN + 32 * c) * 2;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[c4][i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+                if (valid) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint8_t* dst = args.out +
+                                       ((int64_t)row * args.out_ld + tl.n * BN + 32 * (half * 4 + c4)) * 2;
 #pragma unroll
                         for (int p = 0; p < 4; ++p)
-                            st_v4(dst + 16 * p,
-                                  make_uint4(pack_bf16x2(__uint_as_float(v[8 * p + 0]), __uint_as_float(v[8 * p + 1])),
-                                             pack_bf16x2(__uint_as_float(v[8 * p + 2]), __uint_as_float(v[8 * p + 3])),
-                                             pack_bf16x2(__uint_as_float(v[8 * p + 4]), __uint_as_float(v[8 * p + 5])),
-                                             pack_bf16x2(__uint_as_float(v[8 * p + 6]), __uint_as_float(v[8 * p + 7]))));
+                            st_v4(dst + 16 * p, make_uint4(pk[c4][4 * p], pk[c4][4 * p + 1],
+                                                           pk[c4][4 * p + 2], pk[c4][4 * p + 3]));
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
             acc_phase ^= 1;
         }
     }
@@ -398,36 +490,31 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-static bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
-                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
-    using EncodeFn = decltype(&cuTensorMapEncodeTiled);
-    static EncodeFn fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess || !p)
-            return false;
-        fn = reinterpret_cast<EncodeFn>(p);
-    }
-    uint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), (const cuuint64_t*)dims,
-                    (const cuuint64_t*)strides_bytes, (const cuuint32_t*)box, (const cuuint32_t*)estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <bool MX, bool SWIGLU>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const TcArgs& args,
-                              int grid, cudaStream_t stream) {
+static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                              const CUtensorMap& tsb, const TcArgs& args, int grid,
+                              cudaStream_t stream) {
     auto kern = tc_grouped_gemm_kernel<MX, SWIGLU>;
     const size_t smem = tc::smem_bytes(args.E);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tb, args);
+    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tb, tsa, tsb, args);
     return cudaGetLastError();
+}
+
+// Scale tensors as 16-byte-wide TMA boxes of 128 rows (four K-stages of scales).
+static bool encode_sf_maps(CUtensorMap* tsa, CUtensorMap* tsb, const void* a_sf, int a_rows,
+                           const void* b_sf, int b_rows, int E, int K) {
+    const uint64_t ksf = (uint64_t)K / 32;
+    uint64_t da[2] = {ksf, (uint64_t)a_rows};
+    uint64_t sa[1] = {ksf};
+    uint32_t ba[2] = {16, 128};
+    if (!encode_tmap(tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a_sf, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    uint64_t db[3] = {ksf, (uint64_t)b_rows, (uint64_t)E};
+    uint64_t sb[2] = {ksf, (uint64_t)b_rows * ksf};
+    uint32_t bb[3] = {16, 128, 1};
+    return encode_tmap(tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b_sf, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // a: [a_rows][K] (codes or BF16); weights as documented in moe.h.
@@ -484,15 +571,24 @@ cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream) {
     a2.out = (uint8_t*)c.y;
     a2.out_sf = nullptr;
     a2.out_ld = c.H;
+    CUtensorMap ts1a{}, ts1b{}, ts2a{}, ts2b{};
+    if (mx) {
+        a1.sf_tma = (c.H % 512) == 0;
+        a2.sf_tma = (c.I % 512) == 0;
+        if (a1.sf_tma && !encode_sf_maps(&ts1a, &ts1b, c.a_sf, c.a_rows, c.w_gu_sf, 2 * c.I, c.E, c.H))
+            return cudaErrorInvalidValue;
+        if (a2.sf_tma && !encode_sf_maps(&ts2a, &ts2b, c.h_sf, c.a_rows, c.w_d_sf, c.H, c.E, c.I))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t err;
     if (mx) {
-        err = launch_one<true, true>(ta1, tb1, a1, c.grid, stream);
+        err = launch_one<true, true>(ta1, tb1, ts1a, ts1b, a1, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<true, false>(ta2, tb2, a2, c.grid, stream);
+        err = launch_one<true, false>(ta2, tb2, ts2a, ts2b, a2, c.grid, stream);
     } else {
-        err = launch_one<false, true>(ta1, tb1, a1, c.grid, stream);
+        err = launch_one<false, true>(ta1, tb1, ts1a, ts1b, a1, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<false, false>(ta2, tb2, a2, c.grid, stream);
+        err = launch_one<false, false>(ta2, tb2, ts2a, ts2b, a2, c.grid, stream);
     }
     return err;
 }

@@ -17,6 +17,13 @@ cudaError_t launch_route_topk_simt(const void* x, const void* w, const float* bi
                                    int E, int k, int dtype, int32_t* idx, float* gate,
                                    float* logits_out, cudaStream_t stream);
 
+bool route_tc_supported(int dtype, int H, int E, int k);
+
+cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias, int N, int H,
+                                 int E, int k, int32_t* idx, float* gate, float* logits_out,
+                                 uint8_t* xq, uint8_t* xq_sf, WsHeader* ws,
+                                 unsigned long long timeout_ns, cudaStream_t stream);
+
 cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_t* counts,
                           int32_t* offsets, int32_t* sched, int32_t* inv, int32_t* cnt_scratch,
                           int32_t* base_scratch, WsHeader* ws, cudaStream_t stream);

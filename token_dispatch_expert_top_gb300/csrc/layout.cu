@@ -1,7 +1,7 @@
 // layout.cu -- sort-free token layout ("schedule").  The flat list of choices
 // (n, j) -> expert is placed expert-contiguously with a stable counting placement,
 // in three short kernels: per-chunk expert counts (warp match + shared-memory
-// atomics), an exclusive scan over (expert, chunk), and a warp-ballot rank that
+// atomics), a per-expert exclusive scan over chunks (one warp per expert), and a warp-ballot rank that
 // writes each choice's slot, the two-column (source shard, row) pull schedule and
 // the inverse map.  ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost
 // on NVIDIA GB300 NVL72", section 01: count per expert, decide placement, keep an
@@ -21,7 +21,8 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 // Chunk c covers flat choices [c*kLayoutChunk, min((c+1)*kLayoutChunk, T)).
-// One warp per chunk; counts go to cnt[c][e].
+// One warp per chunk; counts go to cnt[e][c] (expert-major, so that each
+// expert's per-chunk counts are contiguous for the scan).
 __global__ void __launch_bounds__(kLayoutWarps * 32) layout_count_kernel(
     const int32_t* __restrict__ idx, int T, int E, int nchunks, int32_t* __restrict__ cnt,
     WsHeader* ws) {
@@ -45,69 +46,67 @@ __global__ void __launch_bounds__(kLayoutWarps * 32) layout_count_kernel(
         if (e >= 0 && (same & lanemask_lt()) == 0) atomicAdd(&hist[e], __popc(same));
     }
     __syncwarp();
-    for (int e = lane; e < E; e += 32) cnt[(int64_t)c * E + e] = hist[e];
+    for (int e = lane; e < E; e += 32) cnt[(int64_t)e * nchunks + c] = hist[e];
 }
 
-// One block.  base[c][e] = offsets[e] + sum_{c' < c} cnt[c'][e];
-// counts[e] = sum_c cnt[c][e]; offsets = exclusive scan of counts.
-__global__ void __launch_bounds__(1024) layout_scan_kernel(const int32_t* __restrict__ cnt,
-                                                           int nchunks, int E,
-                                                           int32_t* __restrict__ base,
-                                                           int32_t* __restrict__ counts,
-                                                           int32_t* __restrict__ offsets) {
-    extern __shared__ int32_t tot[];  // [E]
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            base[(int64_t)c * E + e] = run;
-            run += cnt[(int64_t)c * E + e];
-        }
-        tot[e] = run;
-        counts[e] = run;
-    }
-    __syncthreads();
-    // exclusive scan of tot[0..E) by warp 0: each lane owns a contiguous run
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const int per = (E + 31) / 32;
-        const int lo = min(lane * per, E), hi = min(lo + per, E);
-        int s = 0;
-        for (int e = lo; e < hi; ++e) s += tot[e];
-        int incl = s;
+// Exclusive scan over an int array of length n by one warp: each lane takes a
+// contiguous run, the run totals are scanned with shuffles.  Writes out[i] =
+// base + sum_{i' < i} in[i'] and returns the total (in every lane).
+__device__ __forceinline__ int warp_exclusive_scan(const int32_t* in, int32_t* out, int n, int base,
+                                                   int lane) {
+    const int per = (n + 31) / 32;
+    const int lo = min(lane * per, n), hi = min(lo + per, n);
+    int s = 0;
+    for (int i = lo; i < hi; ++i) s += in[i];
+    int incl = s;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - s;
-        for (int e = lo; e < hi; ++e) {
-            const int c = tot[e];
-            tot[e] = run;
-            offsets[e] = run;
-            run += c;
-        }
-        if (lane == 31) offsets[E] = incl;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int off = tot[e];
-        for (int c = 0; c < nchunks; ++c) base[(int64_t)c * E + e] += off;
+    int run = base + incl - s;
+    for (int i = lo; i < hi; ++i) {
+        const int c = in[i];
+        out[i] = run;
+        run += c;
     }
+    return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-// One warp per chunk, walking its choices in flat order 32 at a time: the lanes
-// holding the same expert find each other with a match, rank themselves by lane
-// order, and the group's first lane advances the expert's cursor.
+// One warp per expert: base[e][c] = sum_{c' < c} cnt[e][c'];  counts[e] = total.
+__global__ void __launch_bounds__(kLayoutWarps * 32) layout_scan_kernel(
+    const int32_t* __restrict__ cnt, int nchunks, int E, int32_t* __restrict__ base,
+    int32_t* __restrict__ counts) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int e = blockIdx.x * kLayoutWarps + warp;
+    if (e >= E) return;
+    const int total = warp_exclusive_scan(cnt + (int64_t)e * nchunks, base + (int64_t)e * nchunks,
+                                          nchunks, 0, lane);
+    if (lane == 0) counts[e] = total;
+}
+
+// Every block first scans counts into the expert offsets (block 0 also writes
+// them out); then one warp per chunk walks its choices in flat order 32 at a
+// time: lanes holding the same expert find each other with a match, rank
+// themselves by lane order, and the group's first lane advances the cursor.
 __global__ void __launch_bounds__(kLayoutWarps * 32) layout_place_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, int nchunks,
-    const int32_t* __restrict__ base, int rows_per_shard, int32_t* __restrict__ sched,
-    int32_t* __restrict__ inv) {
+    const int32_t* __restrict__ base, const int32_t* __restrict__ counts, int rows_per_shard,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sched, int32_t* __restrict__ inv) {
     extern __shared__ int32_t sh[];
+    int32_t* off = sh;                         // [E+1]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    int32_t* cursor = sh + warp * E;
+    int32_t* cursor = sh + (E + 1) + warp * E;
+    if (warp == 0) {
+        const int total = warp_exclusive_scan(counts, off, E, 0, lane);
+        if (lane == 0) off[E] = total;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
     const int c = blockIdx.x * kLayoutWarps + warp;
     if (c >= nchunks) return;
-    for (int e = lane; e < E; e += 32) cursor[e] = base[(int64_t)c * E + e];
+    for (int e = lane; e < E; e += 32) cursor[e] = off[e] + base[(int64_t)e * nchunks + c];
     __syncwarp();
     const int begin = c * kLayoutChunk;
     const int end = min(begin + kLayoutChunk, T);
@@ -137,17 +136,14 @@ cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_
     const int T = N * k;
     const int nchunks = layout_chunks(T);
     const int blocks = (nchunks + kLayoutWarps - 1) / kLayoutWarps;
-    const size_t smem_w = sizeof(int32_t) * kLayoutWarps * E;
-    if (nchunks > 0) {
-        layout_count_kernel<<<blocks, kLayoutWarps * 32, smem_w, stream>>>(idx, T, E, nchunks,
-                                                                          cnt_scratch, ws);
-    }
-    layout_scan_kernel<<<1, 1024, sizeof(int32_t) * E, stream>>>(cnt_scratch, nchunks, E,
-                                                                base_scratch, counts, offsets);
-    if (nchunks > 0) {
-        layout_place_kernel<<<blocks, kLayoutWarps * 32, smem_w, stream>>>(
-            idx, T, k, E, nchunks, base_scratch, N / S, sched, inv);
-    }
+    if (nchunks > 0)
+        layout_count_kernel<<<blocks, kLayoutWarps * 32, sizeof(int32_t) * kLayoutWarps * E,
+                              stream>>>(idx, T, E, nchunks, cnt_scratch, ws);
+    layout_scan_kernel<<<(E + kLayoutWarps - 1) / kLayoutWarps, kLayoutWarps * 32, 0, stream>>>(
+        cnt_scratch, nchunks, E, base_scratch, counts);
+    layout_place_kernel<<<blocks > 0 ? blocks : 1, kLayoutWarps * 32,
+                          sizeof(int32_t) * ((E + 1) + kLayoutWarps * E), stream>>>(
+        idx, T, k, E, nchunks, base_scratch, counts, N / S, offsets, sched, inv);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,315 @@
+// route_tc.cu -- router on the tensor cores: logits = x . W_r (BF16 products,
+// FP32 accumulation in tensor memory) for a 128-token tile per CTA, then softmax
+// top-k and renormalised gates in the epilogue, one token per thread.  When the
+// layer is MXFP8 the same pass quantises x for the dispatch: eight warps read each
+// K-stage of x from shared memory (where TMA put it for the MMA) and write its E4M3
+// codes and UE8M0 scales, so x is read from HBM once.
+// ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72": section 01, each token picks a few experts per step; section 02, MXFP8
+// activation quantisation folded into the data path.)
+//
+// CTA = 16 warps:  w0 TMA producer, w1 MMA issuer + TMEM owner, w2-3 idle,
+//                  w4-11 x quantisers (MXFP8 only; two threads per token row, one MX
+//                  block each), w12-15 top-k epilogue.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tmap.cuh"
+
+namespace moe {
+
+namespace rt {
+constexpr int BM = 128;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * 128;            // 128 tokens x 64 BF16
+constexpr int B_MAX = 256 * 128;             // up to 256 experts x 64 BF16
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_BAR = OFF_B + STAGES * B_MAX;
+constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 1) * 8;
+constexpr int OFF_BIAS = OFF_MISC + 16;
+constexpr int THREADS = 512;
+constexpr int QUANT_WARPS = 8;
+inline size_t smem_bytes() { return 1024 + OFF_BIAS + 256 * sizeof(float); }
+}  // namespace rt
+
+struct RouteArgs {
+    int N, H, E, k;
+    const float* bias;
+    int32_t* idx;
+    float* gate;
+    float* logits_out;
+    uint8_t* xq;          // [N][H] codes, or null
+    uint8_t* xq_sf;       // [N][H/32]
+    WsHeader* ws;
+    unsigned long long timeout_ns;
+    uint32_t tmem_cols;
+};
+
+// Keep the KMAX largest (value, index) pairs, sorted by descending value; equal
+// values keep the earlier (lower) index first because a newcomer only moves up
+// past strictly smaller values.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float v, int e) {
+    if (!(v > tv[KMAX - 1])) return;
+    tv[KMAX - 1] = v;
+    ti[KMAX - 1] = e;
+#pragma unroll
+    for (int i = KMAX - 1; i > 0; --i) {
+        if (tv[i] > tv[i - 1]) {
+            const float fv = tv[i];
+            tv[i] = tv[i - 1];
+            tv[i - 1] = fv;
+            const int fi = ti[i];
+            ti[i] = ti[i - 1];
+            ti[i - 1] = fi;
+        }
+    }
+}
+
+template <int KMAX, bool QUANT>
+__global__ void __launch_bounds__(rt::THREADS, 1)
+    route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    RouteArgs args) {
+    using namespace rt;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = full + 2 * STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    float* sbias = reinterpret_cast<float*>(smem + OFF_BIAS);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int row0 = blockIdx.x * BM;
+    const int KB = args.H / 64;
+    const int E = args.E;
+    const uint32_t b_bytes = (uint32_t)E * 128;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS : 1);
+        }
+        mbar_init(tfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, args.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp >= 12)
+        for (int e = threadIdx.x - 384; e < E; e += 128) sbias[e] = args.bias ? args.bias[e] : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) break;
+                mbar_arrive_expect_tx(&full[stage], A_BYTES + b_bytes);
+                tma_load_2d(smem + OFF_A + stage * A_BYTES, &tmX, &full[stage], kb * 64, row0);
+                tma_load_2d(smem + OFF_B + stage * B_MAX, &tmW, &full[stage], kb * 64, 0);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16(BM, E);
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + OFF_A + stage * A_BYTES);
+                const uint32_t sb = smem_u32(smem + OFF_B + stage * B_MAX);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(tmem_base, sdesc_kmajor_sw128(sa + 32 * k), sdesc_kmajor_sw128(sb + 32 * k),
+                             idesc, (kb | k) != 0);
+                mma_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (ok) mma_commit(tfull);
+        }
+    } else if (warp >= 4 && warp < 12) {
+        if constexpr (QUANT) {
+            // thread = (token row r, MX block b of the stage's 64 columns)
+            const int tq = (warp - 4) * 32 + lane;
+            const int r = tq & (BM - 1);
+            const int b = tq >> 7;
+            const int row = row0 + r;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
+                const uint8_t* tile = smem + OFF_A + stage * A_BYTES + r * 128;
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    // 128-byte swizzle: 16-byte chunk cc of row r sits at chunk cc ^ (r % 8)
+                    const int cc = 4 * b + c;
+                    const uint4 q = *reinterpret_cast<const uint4*>(tile + ((cc ^ (r & 7)) << 4));
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        v[8 * c + 2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
+                        v[8 * c + 2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
+                    }
+                }
+                uint32_t codes[8];
+                const uint8_t sc = mx_quantize32(v, codes);
+                if (row < args.N) {
+                    uint8_t* dst = args.xq + (int64_t)row * args.H + kb * 64 + 32 * b;
+                    st_v4(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+                    st_v4(dst + 16, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+                    args.xq_sf[(int64_t)row * (args.H / 32) + kb * 2 + b] = sc;
+                }
+                // Release the stage only after every lane has consumed what it read
+                // (its codes are computed from all of them), so the next TMA refill
+                // of this stage cannot overtake a lane's shared-memory reads.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    } else if (warp >= 12) {
+        const int q = warp & 3;
+        const int row = row0 + 32 * q + lane;
+        if (mbar_wait_bounded(tfull, 0, abort_flag, args.ws, deadline)) {
+            tc_fence_after();
+            float tv[KMAX];
+            int ti[KMAX];
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+                tv[i] = -INFINITY;
+                ti[i] = -1;
+            }
+            const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+            for (int c = 0; c < E / 16; ++c) {
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tq + 16 * c, r);
+                tmem_ld_wait();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + sbias[16 * c + i];
+                if (args.logits_out && row < args.N) {
+                    float* dst = args.logits_out + (int64_t)row * E + 16 * c;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_v4(dst + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                                      __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) topk_insert<KMAX>(tv, ti, v[i], 16 * c + i);
+            }
+            if (row < args.N) {
+                float z = 0.f;
+                float p[KMAX];
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    p[j] = (j < args.k) ? expf(tv[j] - tv[0]) : 0.f;
+                    z += p[j];
+                }
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < args.k) {
+                        args.idx[(int64_t)row * args.k + j] = ti[j];
+                        args.gate[(int64_t)row * args.k + j] = p[j] / z;
+                    }
+                }
+            }
+        }
+    }
+
+    if (*abort_flag) {
+        const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+        while (globaltimer_ns() < d2) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
+}
+
+bool route_tc_supported(int dtype, int H, int E, int k) {
+    return dtype != MOE_F32 && E % 16 == 0 && E <= 256 && H % 64 == 0 && k <= 32;
+}
+
+template <int KMAX, bool QUANT>
+static cudaError_t launch_route(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
+                                int grid, cudaStream_t st) {
+    auto kern = route_tc_kernel<KMAX, QUANT>;
+    const size_t smem = rt::smem_bytes();
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    kern<<<grid, rt::THREADS, smem, st>>>(tx, tw, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias, int N, int H,
+                                 int E, int k, int32_t* idx, float* gate, float* logits_out,
+                                 uint8_t* xq, uint8_t* xq_sf, WsHeader* ws,
+                                 unsigned long long timeout_ns, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    CUtensorMap tx, tw;
+    {
+        uint64_t dims[2] = {(uint64_t)H, (uint64_t)N};
+        uint64_t str[1] = {(uint64_t)H * 2};
+        uint32_t box[2] = {64, (uint32_t)rt::BM};
+        if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box))
+            return cudaErrorInvalidValue;
+        uint64_t dw[2] = {(uint64_t)H, (uint64_t)E};
+        uint32_t bw[2] = {64, (uint32_t)E};
+        if (!encode_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dw, str, bw))
+            return cudaErrorInvalidValue;
+    }
+    RouteArgs a{};
+    a.N = N;
+    a.H = H;
+    a.E = E;
+    a.k = k;
+    a.bias = bias;
+    a.idx = idx;
+    a.gate = gate;
+    a.logits_out = logits_out;
+    a.xq = xq;
+    a.xq_sf = xq_sf;
+    a.ws = ws;
+    a.timeout_ns = timeout_ns;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)E) cols <<= 1;
+    a.tmem_cols = cols;
+    const int grid = (N + rt::BM - 1) / rt::BM;
+    const bool quant = xq != nullptr;
+    if (k <= 8)
+        return quant ? launch_route<8, true>(tx, tw, a, grid, stream) : launch_route<8, false>(tx, tw, a, grid, stream);
+    if (k <= 16)
+        return quant ? launch_route<16, true>(tx, tw, a, grid, stream) : launch_route<16, false>(tx, tw, a, grid, stream);
+    return quant ? launch_route<32, true>(tx, tw, a, grid, stream) : launch_route<32, false>(tx, tw, a, grid, stream);
+}
+
+}  // namespace moe
