@@ -33,23 +33,63 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 size_t act_elem(int dtype) { return dtype == MOE_F32 ? 4 : 2; }      // x, y, out
 size_t op_elem(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 1); }  // GEMM operands
 
-// Workspace regions, in order.  Every size depends only on the shape and params.
+// Ring and minibatch geometry of the fused forward (moe_params_t resolved).
+struct FusedGeom {
+    int G, C;       // gather CTAs, compute CTAs
+    int MB, R;      // slots per minibatch, ring slots (a multiple of MB)
+    int nmb;        // minibatches
+    int status;     // MOE_OK, or why these params cannot run
+};
+
+int num_sms_current();
+
+FusedGeom resolve_fused(const moe_shape_t& s, const moe_params_t* p, int max_ctas) {
+    FusedGeom g{};
+    const int T = s.N * s.k;
+    const int sms = num_sms_current();
+    if (max_ctas <= 0) max_ctas = sms;
+    g.G = (p && p->gather_ctas > 0) ? p->gather_ctas : (sms >= 64 ? sms / 16 : 1);
+    g.C = (p && p->compute_ctas > 0) ? p->compute_ctas : max_ctas - g.G;
+    if (g.G < 1 || g.C < 1 || g.G + g.C > max_ctas) g.status = MOE_ERR_INVALID_ARG;
+    const int Tp = T > 0 ? T : 1;
+    if (p && p->minibatch > 0) {
+        g.MB = p->minibatch;
+    } else if (p && p->ring_slots > 0) {
+        g.MB = p->ring_slots >= 64 ? p->ring_slots / 2 : p->ring_slots;
+    } else {
+        // two full waves of GEMM1 tiles over the compute SMs, in whole 32-slot units
+        const int waves = moe_min_minibatch(2, g.C > 0 ? g.C : 1, 128, 256, s.I);
+        g.MB = ((waves + 31) / 32) * 32;
+    }
+    if (g.MB > Tp) g.MB = Tp;
+    if (g.MB < 1) g.MB = 1;
+    g.R = (p && p->ring_slots > 0) ? p->ring_slots : (4 * g.MB < Tp ? 4 * g.MB : ((Tp + g.MB - 1) / g.MB) * g.MB);
+    if (g.R < g.MB || g.R % g.MB != 0) g.status = MOE_ERR_INVALID_ARG;
+    g.nmb = (T + g.MB - 1) / g.MB;
+    return g;
+}
+
+// Workspace regions, in order.  Every size depends only on the shape and params;
+// one workspace serves both moe_forward and moe_forward_fused.
 struct Plan {
     size_t header, cnt, base;               // layout scratch
     size_t idx, gate, counts, offsets, sched, inv;
     size_t xq, xq_sf, shard_tab, shard_sf_tab;
-    size_t ring, ring_sf, h, h_sf, y;
+    size_t ring, ring_sf, h, h_sf, y, fused_ints;
     size_t total;
-    int ring_slots;
+    int ring_slots;                         // rows of ring / h (>= T and >= the fused ring)
+    FusedGeom fg;
 };
 
 Plan make_plan(const moe_shape_t& s, const moe_params_t* p) {
     const int64_t T = (int64_t)s.N * s.k;
     const int nch = layout_chunks((int)T);
     const bool mx = s.dtype == MOE_MXFP8;
-    int R = (p && p->ring_slots > 0) ? p->ring_slots : (int)T;
-    if (R < (int)T) R = (int)T;   // the staged path keeps every slot resident
+    const FusedGeom fg = resolve_fused(s, p, 0);
+    int R = (int)T > fg.R ? (int)T : fg.R;
+    if (R < 1) R = 1;
     Plan pl{};
+    pl.fg = fg;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -74,6 +114,7 @@ Plan make_plan(const moe_shape_t& s, const moe_params_t* p) {
     pl.h = take((size_t)R * s.I * op_elem(s.dtype));
     pl.h_sf = take(mx ? (size_t)R * (s.I / 32) : 0);
     pl.y = take((size_t)T * s.H * act_elem(s.dtype));
+    pl.fused_ints = take(sizeof(int32_t) * fused_plan_ints((int)T, s.E, fg.nmb > 0 ? fg.nmb : 1));
     pl.total = off;
     pl.ring_slots = R;
     return pl;
@@ -364,10 +405,96 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
                       const void* w_d_scales, const moe_shape_t* shape, const moe_params_t* params,
                       void* out, int32_t* idx_out, float* gate_out, void* workspace,
                       size_t workspace_bytes, void* stream) {
-    (void)x; (void)w_router; (void)bias; (void)w_gate_up; (void)w_gu_scales; (void)w_down;
-    (void)w_d_scales; (void)shape; (void)params; (void)out; (void)idx_out; (void)gate_out;
-    (void)workspace; (void)workspace_bytes; (void)stream;
-    return MOE_ERR_UNSUPPORTED;
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;   // no tensor-core pipeline for FP32
+    rc = check_ws(shape, params, workspace, workspace_bytes);
+    if (rc) return rc;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!x || !w_router || !w_gate_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+    if (mx && (!w_gu_scales || !w_d_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(w_gate_up) || !aligned16(w_down))
+        return MOE_ERR_INVALID_ARG;
+    const Plan pl = make_plan(s, params);
+    const FusedGeom fg = resolve_fused(s, params, fused_max_ctas());
+    if (fg.status) return fg.status;
+    if (fg.R > pl.ring_slots || fg.nmb > pl.fg.nmb) return MOE_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    void* ws = workspace;
+    WsHeader* hdr = at<WsHeader>(ws, pl.header);
+    const int T = s.N * s.k;
+    const int rows = s.N / s.S;
+    int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, pl.idx);
+    float* gate = gate_out ? gate_out : at<float>(ws, pl.gate);
+    int32_t* counts = at<int32_t>(ws, pl.counts);
+    int32_t* offsets = at<int32_t>(ws, pl.offsets);
+    int32_t* sched = at<int32_t>(ws, pl.sched);
+    int32_t* inv = at<int32_t>(ws, pl.inv);
+    uint8_t* xq = mx ? at<uint8_t>(ws, pl.xq) : nullptr;
+    uint8_t* xq_sf = mx ? at<uint8_t>(ws, pl.xq_sf) : nullptr;
+
+    // routing and layout run first as their own kernels
+    rc = moe_route_topk(x, w_router, bias, shape, idx, gate, nullptr, xq, xq_sf, ws, workspace_bytes,
+                        stream);
+    if (rc) return rc;
+    rc = cuda_status(launch_layout(idx, s.N, s.k, s.E, s.S, counts, offsets, sched, inv,
+                                   at<int32_t>(ws, pl.cnt), at<int32_t>(ws, pl.base), hdr, st));
+    if (rc) return rc;
+    const uint8_t** tab = at<const uint8_t*>(ws, pl.shard_tab);
+    const uint8_t** tab_sf = at<const uint8_t*>(ws, pl.shard_sf_tab);
+    const int row_bytes = s.H * (int)op_elem(s.dtype);
+    const int tb = (s.S + 127) / 128;
+    fill_shard_table_kernel<<<tb, 128, 0, st>>>(tab, mx ? xq : (const uint8_t*)x,
+                                                (int64_t)rows * row_bytes, s.S);
+    if (mx)
+        fill_shard_table_kernel<<<tb, 128, 0, st>>>(tab_sf, xq_sf, (int64_t)rows * (s.H / 32), s.S);
+    rc = cuda_status(cudaGetLastError());
+    if (rc) return rc;
+
+    FusedCall c{};
+    c.ffn.mx = mx;
+    c.ffn.T = T;
+    c.ffn.H = s.H;
+    c.ffn.I = s.I;
+    c.ffn.E = s.E;
+    c.ffn.a_rows = fg.R;
+    c.ffn.a = at<void>(ws, pl.ring);
+    c.ffn.a_sf = mx ? at<void>(ws, pl.ring_sf) : nullptr;
+    c.ffn.offsets = offsets;
+    c.ffn.w_gate_up = w_gate_up;
+    c.ffn.w_gu_sf = w_gu_scales;
+    c.ffn.w_down = w_down;
+    c.ffn.w_d_sf = w_d_scales;
+    c.ffn.h = at<void>(ws, pl.h);
+    c.ffn.h_sf = mx ? at<void>(ws, pl.h_sf) : nullptr;
+    c.ffn.y = at<void>(ws, pl.y);
+    c.ffn.ws = hdr;
+    c.ffn.timeout_ns = timeout_of(params);
+    c.ffn.grid = fg.G + fg.C;
+    c.N = s.N;
+    c.H = s.H;
+    c.E = s.E;
+    c.k = s.k;
+    c.S = s.S;
+    c.T = T;
+    c.MB = fg.MB;
+    c.R = fg.R;
+    c.nmb = fg.nmb;
+    c.G = fg.G;
+    c.C = fg.C;
+    c.row_bytes = row_bytes;
+    c.sf_bytes = mx ? s.H / 32 : 0;
+    c.skip_ready = (params && params->test_skip_ready > 0) ? params->test_skip_ready - 1 : -1;
+    c.sched = sched;
+    c.inv = inv;
+    c.gate = gate;
+    c.shard_rows = (const void* const*)tab;
+    c.shard_sf = (const void* const*)tab_sf;
+    c.out = out;
+    c.plan_ints = at<int>(ws, pl.fused_ints);
+    return cuda_status(launch_fused_forward(c, st));
 }
 
 int moe_min_minibatch(int waves, int compute_sms, int tile_m, int tile_n, int I) {

@@ -1,0 +1,473 @@
+// fused.cu -- the persistent forward kernel: gather, expert FFN and combine as
+// roles of ONE launch, handing minibatches of token slots between SM groups
+// through GPU-local counters, with a fixed-size ring of slots that is refilled
+// as soon as the slots it holds have been consumed.
+// ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72", section 02: one megakernel; some SMs do dispatch/combine/state, the
+// rest only the expert FFN; a GPU-local counter tells the compute side when a
+// full batch of tokens has arrived and the comm side when results are ready; the
+// minibatch should give at least two full waves of GEMM tiles; a fixed-size ring
+// token buffer absorbs the rate difference, no worst-case buffer, no CPU in the
+// loop, no dropped tokens.  [Kittens], megakernel paragraph: bitwise determinism.)
+//
+// Slots [0, T) in expert-sorted order are cut into minibatches of MB slots.
+// Minibatch b lives in ring buffer b mod NR (NR = R / MB buffers of MB slots).
+//   gather CTAs   copy the rows of minibatch b into its ring buffer once the
+//                 GEMM2 tiles of minibatch b - NR (the buffer's previous tenant)
+//                 are done, then bump gather_done[b];
+//   compute CTAs  run the tcgen05 pipeline over the tile sequence
+//                 [GEMM1 tiles of 0][GEMM2 tiles of 0][GEMM1 tiles of 1]...
+//                 (round-robin over compute CTAs); a GEMM1 tile waits for
+//                 gather_done[b], a GEMM2 tile for its m-tile's GEMM1 counter;
+//                 h lives in a ring too, y in a [T][H] buffer;
+//   every CTA     combines tokens once all GEMM2 tiles are done.
+// Every dependency points backwards in that order, so the schedule cannot
+// deadlock; every wait is bounded by timeout_ns from kernel start, after which
+// the kernel records MOE_ERR_TIMEOUT, raises a global abort flag and returns.
+#include "common.cuh"
+#include "gemm_roles.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+// ------------------------------------------------------------ global counters
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// Spin until *ctr >= target.  Gives up (false) when the global abort flag is
+// raised or the deadline passes (then it raises the flag and records a timeout).
+__device__ bool wait_counter(const int* ctr, int target, int* abort_g, WsHeader* ws,
+                             unsigned long long deadline) {
+    uint32_t n = 0;
+    while (ld_acquire(ctr) < target) {
+        if (ld_acquire(abort_g)) return false;
+        if ((++n & 63u) == 0) {
+            if (globaltimer_ns() > deadline) {
+                atomicExch(abort_g, 1);
+                set_status(ws, MOE_ERR_TIMEOUT);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Make this thread's global stores visible to other CTAs and to the TMA (async
+// proxy) of other CTAs before a counter is bumped.
+__device__ __forceinline__ void publish_fence() {
+    fence_proxy_async_all();
+    __threadfence();
+}
+
+}  // namespace
+
+// Counters and plan arrays in the workspace (int32 unless noted).
+struct FusedPlan {
+    int* tbase;        // [nmb+1] tile prefix over minibatches (P_b * (NT1 + NT2) each)
+    int* pbase;        // [nmb+1] m-tile prefix over minibatches (P_b each)
+    int* elo;          // [nmb] first expert overlapping minibatch b
+    int* gather_done;  // [nmb] gather CTAs done with minibatch b
+    int* g1_done;      // [pbase[nmb]] epilogue-warp reports of GEMM1 tiles per m-tile
+    int* g2_done;      // [nmb] epilogue-warp reports of GEMM2 tiles per minibatch
+    int* g2_all;       // [1]  epilogue-warp reports of all GEMM2 tiles
+    int* abort_g;      // [1]  set when any wait gave up
+};
+
+struct FusedArgs {
+    FusedPlan plan;
+    const int32_t* offsets;   // [E+1]
+    const int32_t* sched;     // [T][2]
+    const int32_t* inv;       // [N][k]
+    const float* gate;        // [N][k]
+    const uint8_t* const* shard_rows;
+    const uint8_t* const* shard_sf;
+    uint8_t* ring;            // [R][H] (codes or BF16)
+    uint8_t* ring_sf;         // [R][H/32]
+    uint8_t* y;               // [T][H] BF16
+    uint8_t* out;             // [N][H] BF16
+    int N, H, E, k, S, T;
+    int MB, NR, nmb;          // minibatch, ring buffers, minibatches
+    int G;                    // gather CTAs (blockIdx.x < G)
+    int row_bytes, sf_bytes;  // gathered row and its scales
+    int skip_ready;           // test hook: minibatch whose gather_done is never bumped (-1: none)
+    WsHeader* ws;
+    unsigned long long timeout_ns;
+};
+
+// One block: per-minibatch m-tile counts, prefixes, first experts; zero counters.
+__global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restrict__ offsets, int E,
+                                                          int T, int MB, int nmb, int nt_sum,
+                                                          FusedPlan plan, int counters_len,
+                                                          int* counters) {
+    extern __shared__ int32_t off[];
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = offsets[e];
+    for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < nmb; b += blockDim.x) {
+        const int lo = b * MB, hi = min(lo + MB, T);
+        int a = 0, z = E;  // first e with off[e+1] > lo
+        while (a < z) {
+            const int mid = (a + z) >> 1;
+            if (off[mid + 1] > lo) z = mid; else a = mid + 1;
+        }
+        plan.elo[b] = a;
+        int P = 0;
+        for (int e = a; e < E && off[e] < hi; ++e) {
+            const int len = min(off[e + 1], hi) - max(off[e], lo);
+            if (len > 0) P += (len + tc::BM - 1) / tc::BM;
+        }
+        plan.tbase[b] = P;   // the count for now; the scan below turns it into prefixes
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int per = (nmb + 31) / 32;
+        const int lo = min(lane * per, nmb), hi = min(lo + per, nmb);
+        int s = 0;
+        for (int b = lo; b < hi; ++b) s += plan.tbase[b];
+        int incl = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - s;
+        for (int b = lo; b < hi; ++b) {       // each lane touches only its own b's
+            const int P = plan.tbase[b];
+            plan.pbase[b] = run;
+            plan.tbase[b] = run * nt_sum;
+            run += P;
+        }
+        if (lane == 31) {
+            plan.pbase[nmb] = incl;
+            plan.tbase[nmb] = incl * nt_sum;
+        }
+    }
+}
+
+// Tiles of the fused schedule: per minibatch, its GEMM1 tiles then its GEMM2
+// tiles, each ordered N tile major, m-tile minor (as in the staged kernel), so
+// compute CTAs working at the same time share weight tiles in L2.
+struct MinibatchTiles {
+    const FusedArgs* a;
+    const int32_t* off;       // offsets in shared memory
+    int nt1, nt2, c0, C;      // N tiles of GEMM1 / GEMM2, this CTA's index among C
+    __device__ int first() const { return c0; }
+    __device__ int next(int t) const { return t + C; }
+    __device__ int count() const { return a->plan.tbase[a->nmb]; }
+    __device__ TileInfo tile(int t) const {
+        const FusedPlan& pl = a->plan;
+        int lo = 0, hi = a->nmb;   // last b with tbase[b] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pl.tbase[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int b = lo;
+        const int P = pl.pbase[b + 1] - pl.pbase[b];
+        int local = t - pl.tbase[b];
+        TileInfo tl;
+        if (local < P * nt1) {
+            tl.kind = 0;
+        } else {
+            tl.kind = 1;
+            local -= P * nt1;
+        }
+        tl.n = local / P;
+        const int mi = local % P;
+        const int s_lo = b * a->MB, s_hi = min(s_lo + a->MB, a->T);
+        int e = pl.elo[b], m = mi;
+        for (; e < a->E; ++e) {
+            const int len = min(off[e + 1], s_hi) - max(off[e], s_lo);
+            const int mt = len > 0 ? (len + tc::BM - 1) / tc::BM : 0;
+            if (m < mt) break;
+            m -= mt;
+        }
+        int piece0, piece_end;
+        if (e < a->E) {
+            piece0 = max(off[e], s_lo) + m * tc::BM;   // first slot of the m-tile
+            piece_end = min(off[e + 1], s_hi);
+        } else {                                       // plan and decode disagree: store nothing
+            set_status(a->ws, MOE_ERR_DEVICE_CHECK);
+            e = a->E - 1;
+            piece0 = piece_end = s_lo;
+        }
+        const int ring_row = (b % a->NR) * a->MB + (piece0 - s_lo);
+        tl.e = e;
+        tl.a_row0 = ring_row;
+        tl.out_row0 = tl.kind == 0 ? ring_row : piece0;
+        tl.nrows = min(piece_end - piece0, tc::BM);
+        tl.mb = b;
+        tl.midx = pl.pbase[b] + mi;
+        return tl;
+    }
+    __device__ bool wait_inputs(const TileInfo& tl, const Pipe& p) const {
+        const FusedPlan& pl = a->plan;
+        const unsigned long long dl = p.deadline;
+        bool ok = tl.kind == 0
+                      ? wait_counter(pl.gather_done + tl.mb, a->G, pl.abort_g, a->ws, dl)
+                      : wait_counter(pl.g1_done + tl.midx, nt1 * tc::EPI_WARPS, pl.abort_g, a->ws, dl);
+        if (!ok) {
+            *p.abort_flag = 1;
+            return false;
+        }
+        fence_proxy_async_all();   // the rows another CTA stored may now be read by TMA
+        return true;
+    }
+    __device__ void tile_stored(const TileInfo& tl, const Pipe&) const {
+        publish_fence();
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            if (tl.kind == 0) {
+                atomicAdd(a->plan.g1_done + tl.midx, 1);
+            } else {
+                atomicAdd(a->plan.g2_done + tl.mb, 1);
+                atomicAdd(a->plan.g2_all, 1);
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ void copy_slot_row(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
+                                              int n16, uint8_t* __restrict__ dst2,
+                                              const uint8_t* __restrict__ src2, int m16, int lane) {
+    constexpr int U = 16;
+    for (int b = 0; b < n16 || b < m16; b += 32 * U) {
+        uint4 v[U], w;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = b + lane + 32 * u;
+            if (j < n16) v[u] = ld_nc_v4(src + 16 * (int64_t)j);
+        }
+        const int j2 = b + lane;
+        if (j2 < m16) w = ld_nc_v4(src2 + 16 * (int64_t)j2);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = b + lane + 32 * u;
+            if (j < n16) st_v4(dst + 16 * (int64_t)j, v[u]);
+        }
+        if (j2 < m16) st_v4(dst2 + 16 * (int64_t)j2, w);
+    }
+}
+
+// Gather role: minibatch by minibatch, wait for the ring buffer, copy, publish.
+__device__ void gather_role(const FusedArgs& a, unsigned long long deadline, int nt2) {
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int nw = a.G * (blockDim.x / 32);
+    const FusedPlan& pl = a.plan;
+    __shared__ int s_ok;
+    for (int b = 0; b < a.nmb; ++b) {
+        if (threadIdx.x == 0) {
+            bool ok = true;
+            if (b >= a.NR) {
+                const int prev = b - a.NR;
+                const int target = (pl.pbase[prev + 1] - pl.pbase[prev]) * nt2 * tc::EPI_WARPS;
+                ok = wait_counter(pl.g2_done + prev, target, pl.abort_g, a.ws, deadline);
+            }
+            s_ok = ok && !ld_acquire(pl.abort_g);
+        }
+        __syncthreads();
+        if (!s_ok) return;
+        const int lo = b * a.MB, hi = min(lo + a.MB, a.T);
+        const int base = (b % a.NR) * a.MB;
+        for (int t = lo + gw; t < hi; t += nw) {
+            const int s = a.sched[2 * (int64_t)t];
+            const int r = a.sched[2 * (int64_t)t + 1];
+            if (s < 0 || s >= a.S || r < 0 || r >= a.N / a.S) {
+                if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
+                continue;
+            }
+            const int64_t dr = base + (t - lo);
+            const bool has_sf = a.sf_bytes > 0;
+            copy_slot_row(a.ring + dr * a.row_bytes, a.shard_rows[s] + (int64_t)r * a.row_bytes,
+                          a.row_bytes >> 4, has_sf ? a.ring_sf + dr * a.sf_bytes : nullptr,
+                          has_sf ? a.shard_sf[s] + (int64_t)r * a.sf_bytes : nullptr,
+                          has_sf ? a.sf_bytes >> 4 : 0, lane);
+        }
+        publish_fence();
+        __syncthreads();
+        if (threadIdx.x == 0 && b != a.skip_ready) atomicAdd(pl.gather_done + b, 1);
+    }
+}
+
+// Combine role (every CTA, after all GEMM2 tiles): out[n] = sum_j g[n][j] y[inv[n][j]]
+// in FP32, fixed j order, one warp per (token, 256-column chunk).
+__device__ void combine_role(const FusedArgs& a) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = (a.H + 255) / 256;
+    const int64_t items = (int64_t)a.N * chunks;
+    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t it = gw; it < items; it += nw) {
+        const int n = (int)(it / chunks);
+        const int col = (int)(it % chunks) * 256 + lane * 8;
+        const int my_slot = lane < a.k ? a.inv[(int64_t)n * a.k + lane] : 0;
+        const float my_g = lane < a.k ? a.gate[(int64_t)n * a.k + lane] : 0.f;
+        float acc[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+        for (int j = 0; j < a.k; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            const float g = __shfl_sync(0xffffffffu, my_g, j);
+            if (slot < 0 || slot >= a.T) {
+                if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
+                continue;
+            }
+            if (col < a.H) {
+                // y was stored by other CTAs of this launch: read it through L2
+                const uint4 q = ld_cg_v4(a.y + ((int64_t)slot * a.H + col) * 2);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    acc[2 * p] = fmaf(g, bf16_to_f32((uint16_t)(w[p] & 0xFFFF)), acc[2 * p]);
+                    acc[2 * p + 1] = fmaf(g, bf16_to_f32((uint16_t)(w[p] >> 16)), acc[2 * p + 1]);
+                }
+            }
+        }
+        if (col < a.H)
+            st_v4(a.out + ((int64_t)n * a.H + col) * 2,
+                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+    }
+}
+
+template <bool MX>
+__global__ void __launch_bounds__(tc::THREADS, 1)
+    fused_forward_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                         const __grid_constant__ CUtensorMap tmS1a, const __grid_constant__ CUtensorMap tmS1b,
+                         const __grid_constant__ CUtensorMap tmS2a, const __grid_constant__ CUtensorMap tmS2b,
+                         const GemmSide s1, const GemmSide s2, const FusedArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const unsigned long long deadline = globaltimer_ns() + a.timeout_ns;
+    const FusedPlan& pl = a.plan;
+
+    if ((int)blockIdx.x < a.G) {
+        gather_role(a, deadline, s2.n_tiles);
+    } else {
+        int32_t* off = reinterpret_cast<int32_t*>(smem + tc::OFF_TAIL);
+        for (int e = threadIdx.x; e <= a.E; e += blockDim.x) off[e] = a.offsets[e];
+        __syncthreads();
+        MinibatchTiles src{&a, off, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G, (int)gridDim.x - a.G};
+        GemmMaps maps;
+        maps.a[0] = &tmA1;
+        maps.b[0] = &tmB1;
+        maps.a[1] = &tmA2;
+        maps.b[1] = &tmB2;
+        maps.sfa[0] = &tmS1a;
+        maps.sfb[0] = &tmS1b;
+        maps.sfa[1] = &tmS2a;
+        maps.sfb[1] = &tmS2b;
+        GemmSide sides[2] = {s1, s2};
+        run_gemm_pipeline<MX>(smem, maps, sides, src, a.ws, a.timeout_ns);
+    }
+
+    // combine once every GEMM2 tile has been stored
+    __shared__ int s_go;
+    if (threadIdx.x == 0) {
+        const int target = pl.pbase[a.nmb] * s2.n_tiles * tc::EPI_WARPS;
+        s_go = wait_counter(pl.g2_all, target, pl.abort_g, a.ws, deadline) ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_go) combine_role(a);
+}
+
+// ------------------------------------------------------------------ host side
+cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
+    if (c.T == 0) return cudaSuccess;
+    // plan arrays and counters live in one int region of the workspace
+    int* w = c.plan_ints;
+    FusedPlan pl;
+    pl.tbase = w;
+    pl.pbase = w + (c.nmb + 1);
+    pl.elo = w + 2 * (c.nmb + 1);
+    int* counters = w + 3 * (c.nmb + 1);
+    const int max_m = fused_max_mtiles(c.T, c.E, c.nmb);
+    pl.gather_done = counters;
+    pl.g2_done = counters + c.nmb;
+    pl.g2_all = counters + 2 * c.nmb;
+    pl.abort_g = counters + 2 * c.nmb + 1;
+    pl.g1_done = counters + 2 * c.nmb + 8;
+    const int counters_len = 2 * c.nmb + 8 + max_m;
+
+    FfnMaps m;
+    GemmSide s1, s2;
+    if (!encode_ffn_maps(c.ffn, &m, &s1, &s2)) return cudaErrorInvalidValue;
+    fused_plan_kernel<<<1, 1024, sizeof(int32_t) * (c.E + 1), stream>>>(
+        c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles + s2.n_tiles, pl, counters_len, counters);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    FusedArgs a{};
+    a.plan = pl;
+    a.offsets = c.ffn.offsets;
+    a.sched = c.sched;
+    a.inv = c.inv;
+    a.gate = c.gate;
+    a.shard_rows = (const uint8_t* const*)c.shard_rows;
+    a.shard_sf = (const uint8_t* const*)c.shard_sf;
+    a.ring = (uint8_t*)c.ffn.a;
+    a.ring_sf = (uint8_t*)c.ffn.a_sf;
+    a.y = (uint8_t*)c.ffn.y;
+    a.out = (uint8_t*)c.out;
+    a.N = c.N;
+    a.H = c.H;
+    a.E = c.E;
+    a.k = c.k;
+    a.S = c.S;
+    a.T = c.T;
+    a.MB = c.MB;
+    a.NR = c.R / c.MB;
+    a.nmb = c.nmb;
+    a.G = c.G;
+    a.row_bytes = c.row_bytes;
+    a.sf_bytes = c.sf_bytes;
+    a.skip_ready = c.skip_ready;
+    a.ws = c.ffn.ws;
+    a.timeout_ns = c.ffn.timeout_ns;
+
+    const size_t smem = 1024 + tc::OFF_TAIL + sizeof(int32_t) * (c.E + 1);
+    void* kern = c.ffn.mx ? (void*)fused_forward_kernel<true> : (void*)fused_forward_kernel<false>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    void* args[] = {&m.a1, &m.b1, &m.a2, &m.b2, &m.s1a, &m.s1b, &m.s2a, &m.s2b, &s1, &s2, &a};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c.G + c.C);
+    cfg.blockDim = dim3(tc::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on each other
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+int fused_max_ctas() {
+    int dev = 0, sms = 0, per = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    const size_t smem = 1024 + tc::OFF_TAIL + sizeof(int32_t) * 1025;
+    if (cudaFuncSetAttribute(fused_forward_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, fused_forward_kernel<true>, tc::THREADS,
+                                                      smem) != cudaSuccess)
+        return 0;
+    return per * sms;
+}
+
+}  // namespace moe

@@ -64,4 +64,37 @@ struct TcFfnCall {
 
 cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream);
 
+// Fused persistent forward (gather, expert FFN, combine in one launch).
+// Upper bound on the m-tiles of all minibatches: each piece (expert x minibatch)
+// of L slots takes ceil(L/128) <= L/128 + 1 tiles and there are at most E + nmb
+// pieces.
+inline int fused_max_mtiles(int T, int E, int nmb) { return T / 128 + E + 2 * nmb + 8; }
+// int32 entries of the plan + counter region: tbase, pbase, elo, then counters
+inline size_t fused_plan_ints(int T, int E, int nmb) {
+    return (size_t)3 * (nmb + 1) + 2 * nmb + 8 + fused_max_mtiles(T, E, nmb);
+}
+struct FusedCall {
+    TcFfnCall ffn;            // a = ring [R][H], h = ring [R][I], y = [T][H]
+    int N, H, E, k, S, T;
+    int MB, R, nmb, G, C;
+    int row_bytes, sf_bytes;
+    int skip_ready;           // -1: none
+    const int32_t* sched;
+    const int32_t* inv;
+    const float* gate;
+    const void* const* shard_rows;
+    const void* const* shard_sf;
+    void* out;
+    int* plan_ints;
+};
+cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream);
+int fused_max_ctas();
+
+// TMA maps of both expert GEMMs (operands and, for MXFP8, staged scales).
+struct FfnMaps {
+    CUtensorMap a1, b1, a2, b2, s1a, s1b, s2a, s2b;
+};
+struct GemmSide;
+bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2);
+
 }  // namespace moe
