@@ -166,15 +166,15 @@ class StagedStep:
 
 
 def kernel_launches_per_step(w, fused: bool) -> int:
-    # route (1) + quantise x (1, MXFP8) + layout (3) + shard tables (1-2) + dispatch (1)
-    # + expert FFN (2: GEMM1+SwiGLU, GEMM2) + combine (1)
-    n = 1 + 3 + 1 + 2 + 1
-    if w.dtype == "mxfp8":
-        n += 1 + 2
+    """libmoe kernels one forward launches (counted from the launch sequence)."""
+    tc_router = w.dtype != "f32" and w.E % 16 == 0 and w.E <= 256 and w.H % 64 == 0
+    n = 1 if tc_router else (2 if w.dtype == "mxfp8" else 1)    # router (+ separate x quantiser)
+    n += 3                                                      # layout: count, scan, place
+    n += 2 if w.dtype == "mxfp8" else 1                         # shard pointer tables
+    if fused:
+        n += 2                                                  # plan + persistent kernel
     else:
-        n += 1
-    if w.dtype == "f32":
-        n += 0
+        n += 1 + 2 + 1                                          # dispatch, GEMM1, GEMM2, combine
     return n
 
 
@@ -281,8 +281,17 @@ def gpu_arm(args, rank, world):
     else:
         tensor_peak = None
         peak_note = "FP32 SIMT"
+    if args.fused:
+        # the persistent kernel runs gather + FFN + combine; its time is the step minus
+        # the router and layout launches that precede it (same kernels, timed above)
+        t_kernel = ms_per_step - stage_ms["route"] - stage_ms["layout"]
+        ffn_tflops = ffn_flops / (t_kernel / 1e3) / 1e12
+        kname = ("fused persistent kernel (gather + GEMM1/SwiGLU + GEMM2 + combine; time = "
+                 "step minus the router and layout launches)")
+    else:
+        kname = "expert FFN grouped GEMMs (GEMM1+SwiGLU and GEMM2 launches of moe_expert_ffn)"
     roofline = {
-        "kernel": "expert FFN grouped GEMMs (GEMM1+SwiGLU and GEMM2 launches of moe_expert_ffn)",
+        "kernel": kname,
         "bound": "tensor", "achieved": round(ffn_tflops, 2),
         "peak": round(tensor_peak, 1) if tensor_peak else None, "unit": "TFLOP/s",
         "frac": round(ffn_tflops / tensor_peak, 4) if tensor_peak else None,

@@ -31,8 +31,9 @@
  *     status word at the start of the workspace (first error wins) and read with
  *     moe_last_device_status().  Kernels that detect one skip the offending work
  *     and return; they never trap.
- *   - Row-major layouts throughout.  Weights are K-major per expert: each output
- *     column's K values are contiguous (the GEMMs' B operands).
+ *   - Row-major layouts throughout.  Expert weights are quantised (MXFP8) and
+ *     repacked into GEMM tile images once, by moe_quantize_mxfp8 and
+ *     moe_pack_expert_weights, before any forward call.
  *
  * Number formats (moe_shape_t.dtype)
  *   MOE_F32   : x, router weight, expert weights, y and out are FP32.
@@ -118,6 +119,27 @@ const char* moe_status_string(int status);
 int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
                        uint8_t* codes, uint8_t* scales, void* stream);
 
+/* One-time repacking of the expert weights into the layout the grouped GEMMs
+ * read (pull dispatch lets the receiver choose its own placement, [MoK-2.37x]
+ * section 02; the same holds for the static weights).  Input is the natural
+ * K-major layout; output has the same size and is what moe_expert_ffn,
+ * moe_forward and moe_forward_fused take:
+ *   w_gate_up [E][2I][H] (rows 0..I-1 W_gate^T, rows I..2I-1 W_up^T),
+ *   w_down [E][H][I] (W_down^T); MXFP8: E4M3 codes plus [rows][K/32] scales.
+ *   packed_gate_up : [E][I/128][K-stages][32 KB]: per N tile of 128 h columns and
+ *                    K-stage of 128 bytes (128 E4M3 or 64 BF16 values), the 128
+ *                    gate rows then the 128 up rows, 128 bytes each, 16-byte chunk
+ *                    c of row r stored at chunk c ^ (r % 8) of that row
+ *   packed_down    : [E][H/256][K-stages][32 KB], 256 down rows per tile, same form
+ *   packed_*_scales: [..][K-stages][1 KB]: two 128-row halves of [32][4] words,
+ *                    word j of entry r holding the 4 K-step scales of row 32j + r
+ * FP32 weights are copied unchanged (the FP32 path reads them as they are). */
+int moe_pack_expert_weights(const moe_shape_t* shape, const void* w_gate_up,
+                            const uint8_t* w_gu_scales, const void* w_down,
+                            const uint8_t* w_d_scales, void* packed_gate_up,
+                            uint8_t* packed_gu_scales, void* packed_down, uint8_t* packed_d_scales,
+                            void* stream);
+
 /* Router + top-k ([MoK-2.37x] section 01: every token picks a few experts each
  * step; configuration: softmax over the router logits, top-k, gates renormalised
  * to sum 1).
@@ -178,13 +200,13 @@ int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_sc
  *   a, a_scales : [T][H] slot rows in slot order (+ [T][H/32] scales, MXFP8)
  *   offsets     : [E+1] DEVICE exclusive scan of expert counts (read on device;
  *                 the host never learns the counts)
- *   w_gate_up   : [E][2I][H]: rows 0..I-1 are W_gate^T, rows I..2I-1 W_up^T
- *   w_gu_scales : [E][2I][H/32] (MXFP8) or NULL
- *   w_down      : [E][H][I] (W_down^T);  w_d_scales: [E][H][I/32] or NULL
+ *   w_gate_up, w_gu_scales, w_down, w_d_scales : the expert weights in the
+ *                 tile-packed layout written by moe_pack_expert_weights (W_gate /
+ *                 W_up / W_down; scales NULL unless MXFP8)
  *   y           : [T][H] FP32 (MOE_F32) or BF16                        (out)
- * BF16 / MXFP8 run on tcgen05 tensor cores (128x256 tiles, TMA-fed, accumulators
- * in tensor memory) and need H % 256 == 0 and I % 128 == 0; MOE_F32 runs a SIMT
- * kernel. */
+ * BF16 / MXFP8 run on tcgen05 tensor cores (128x256 tiles, A by TMA, B by bulk
+ * copies of packed tiles, accumulators in tensor memory) and need H % 256 == 0 and
+ * I % 128 == 0; MOE_F32 runs a SIMT kernel. */
 int moe_expert_ffn(const void* a, const void* a_scales, const int32_t* offsets,
                    const void* w_gate_up, const void* w_gu_scales, const void* w_down,
                    const void* w_d_scales, const moe_shape_t* shape, void* y,
@@ -201,7 +223,7 @@ int moe_combine(const void* y, const int32_t* inv, const float* gate, const moe_
 /* Whole forward layer, one kernel per step on `stream` (route, layout, pull,
  * expert FFN, combine) with every intermediate in the workspace.
  *   x, w_router, bias : as moe_route_topk
- *   w_* : expert weights as moe_expert_ffn (MXFP8: pre-quantised codes + scales)
+ *   w_* : tile-packed expert weights as moe_expert_ffn (moe_pack_expert_weights)
  *   out : [N][H]
  *   idx_out, gate_out : optional [N][k] copies of the routing (NULL to skip)
  * The MXFP8 copy of x is written once per source shard into the workspace and

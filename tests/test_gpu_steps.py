@@ -222,6 +222,60 @@ def test_combine_matches_oracle(M, dtype):
     assert err.max() < (2e-6 if dtype == "f32" else 8e-3)
 
 
+# -------------------------------------------------------------------- weight packing
+def _expected_pack(w, rows_fn, NT, KB):
+    """Tile images by definition: tile (e, n, kb) row r = weight row rows_fn(n, r),
+    K bytes [128 kb, 128 kb + 128); chunk c of row r stored at chunk c ^ (r % 8)."""
+    E = w.shape[0]
+    out = np.empty((E, NT, KB, 256, 8, 16), dtype=np.uint8)
+    for n in range(NT):
+        src_rows = np.array([rows_fn(n, r) for r in range(256)])
+        blk = w[:, src_rows, :].reshape(E, 256, KB, 8, 16)          # [E][r][kb][c][16]
+        for r in range(256):
+            perm = np.arange(8) ^ (r & 7)                               # position p holds chunk p ^ (r%8)
+            out[:, n, :, r, :, :] = blk[:, r][:, :, perm, :]
+    return out.reshape(-1)
+
+
+def _expected_pack_sf(sf, rows_fn, NT, KB):
+    E = sf.shape[0]
+    out = np.empty((E, NT, KB, 2, 32, 4, 4), dtype=np.uint8)         # [..][half][lane][j][q]
+    for n in range(NT):
+        for half in range(2):
+            for j in range(4):
+                src_rows = np.array([rows_fn(n, 128 * half + 32 * j + lane) for lane in range(32)])
+                v = sf[:, src_rows, :].reshape(E, 32, KB, 4)             # [E][lane][kb][q]
+                out[:, n, :, half, :, j, :] = v.transpose(0, 2, 1, 3)
+    return out.reshape(-1)
+
+
+@pytest.mark.parametrize("dtype", ["mxfp8", "bf16"])
+def test_pack_expert_weights_layout(M, dtype):
+    from token_dispatch_expert_top_gb300.layer import pack_expert_weights
+    E, H, I = 2, 512, 256
+    w = synth.Workload("pack", N=8, H=H, I=I, E=E, k=1, S=1, dtype=dtype)
+    shape = M.Shape.of(w)
+    esz = 1 if dtype == "mxfp8" else 2
+    g = torch.Generator().manual_seed(3)
+    wgu = torch.randint(0, 256, (E, 2 * I, H * esz), generator=g, dtype=torch.uint8)
+    wd = torch.randint(0, 256, (E, H, I * esz), generator=g, dtype=torch.uint8)
+    sgu = torch.randint(0, 256, (E, 2 * I, H // 32), generator=g, dtype=torch.uint8) if esz == 1 else None
+    sd = torch.randint(0, 256, (E, H, I // 32), generator=g, dtype=torch.uint8) if esz == 1 else None
+    dev = lambda t: None if t is None else t.cuda()
+    p_gu, p_gu_sf, p_d, p_d_sf = pack_expert_weights(shape, dev(wgu), dev(sgu), dev(wd), dev(sd))
+    rows1 = lambda n, r: n * 128 + r if r < 128 else I + n * 128 + (r - 128)
+    rows2 = lambda n, r: n * 256 + r
+    np.testing.assert_array_equal(to_np(p_gu).reshape(-1),
+                                  _expected_pack(wgu.numpy(), rows1, I // 128, H * esz // 128))
+    np.testing.assert_array_equal(to_np(p_d).reshape(-1),
+                                  _expected_pack(wd.numpy(), rows2, H // 256, I * esz // 128))
+    if esz == 1:
+        np.testing.assert_array_equal(to_np(p_gu_sf).reshape(-1),
+                                      _expected_pack_sf(sgu.numpy(), rows1, I // 128, H // 128))
+        np.testing.assert_array_equal(to_np(p_d_sf).reshape(-1),
+                                      _expected_pack_sf(sd.numpy(), rows2, H // 256, I // 128))
+
+
 # ---------------------------------------------------------------------- expert FFN
 FFN_CASES = [
     ("f32", 128, 256, [0, 3, 40, 85]),
@@ -250,14 +304,14 @@ def test_expert_ffn_matches_oracle(M, dtype, H, I, counts):
     offsets_np = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     offsets = torch.from_numpy(offsets_np).cuda()
     y = torch.empty((T, H), dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device="cuda")
+    from token_dispatch_expert_top_gb300.layer import pack_expert_weights, quantize_mxfp8
     if dtype == "mxfp8":
-        from token_dispatch_expert_top_gb300.layer import quantize_mxfp8
         a_c, a_s = quantize_mxfp8(a.cuda())
-        wgu_c, wgu_s = quantize_mxfp8(wgu.cuda())
-        wd_c, wd_s = quantize_mxfp8(wd.cuda())
-        M.moe_expert_ffn(a_c, a_s, offsets, wgu_c, wgu_s, wd_c, wd_s, shape, y, ws)
+        packed = pack_expert_weights(shape, *quantize_mxfp8(wgu.cuda()), *quantize_mxfp8(wd.cuda()))
+        M.moe_expert_ffn(a_c, a_s, offsets, *packed[:2], *packed[2:], shape, y, ws)
     else:
-        M.moe_expert_ffn(a.cuda(), None, offsets, wgu.cuda(), None, wd.cuda(), None, shape, y, ws)
+        packed = pack_expert_weights(shape, wgu.cuda(), None, wd.cuda(), None)
+        M.moe_expert_ffn(a.cuda(), None, offsets, packed[0], None, packed[2], None, shape, y, ws)
     assert M.moe_last_device_status(ws) == 0
     got = to_np(y)
     a64 = O._f64(a)

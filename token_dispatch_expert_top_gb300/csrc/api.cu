@@ -240,6 +240,50 @@ int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K, ui
                                              num_sms_current(), (cudaStream_t)stream));
 }
 
+int moe_pack_expert_weights(const moe_shape_t* shape, const void* w_gate_up,
+                            const uint8_t* w_gu_scales, const void* w_down,
+                            const uint8_t* w_d_scales, void* packed_gate_up,
+                            uint8_t* packed_gu_scales, void* packed_down, uint8_t* packed_d_scales,
+                            void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!w_gate_up || !w_down || !packed_gate_up || !packed_down) return MOE_ERR_INVALID_ARG;
+    if (mx && (!w_gu_scales || !w_d_scales || !packed_gu_scales || !packed_d_scales))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(packed_gate_up) ||
+        !aligned16(packed_down))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t esz = op_elem(s.dtype);
+    if (s.dtype == MOE_F32) {   // the SIMT path reads the natural layout
+        const size_t b1 = (size_t)s.E * 2 * s.I * s.H * esz, b2 = (size_t)s.E * s.H * s.I * esz;
+        if (cudaMemcpyAsync(packed_gate_up, w_gate_up, b1, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(packed_down, w_down, b2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (mx && (((uintptr_t)w_gu_scales & 3) || ((uintptr_t)w_d_scales & 3) ||
+               ((uintptr_t)packed_gu_scales & 3) || ((uintptr_t)packed_d_scales & 3)))
+        return MOE_ERR_INVALID_ARG;
+    PackCall c{};
+    c.mx = mx;
+    c.E = s.E;
+    c.H = s.H;
+    c.I = s.I;
+    c.w_gate_up = w_gate_up;
+    c.w_gu_sf = w_gu_scales;
+    c.w_down = w_down;
+    c.w_d_sf = w_d_scales;
+    c.p_gate_up = packed_gate_up;
+    c.p_gu_sf = packed_gu_scales;
+    c.p_down = packed_down;
+    c.p_d_sf = packed_d_scales;
+    c.num_sms = num_sms_current();
+    return cuda_status(launch_pack_weights(c, st));
+}
+
 int moe_route_topk(const void* x, const void* w_router, const float* bias, const moe_shape_t* shape,
                    int32_t* idx, float* gate, float* logits_out, uint8_t* xq_codes,
                    uint8_t* xq_scales, void* workspace, size_t workspace_bytes, void* stream) {

@@ -71,9 +71,25 @@ __device__ __forceinline__ void publish_fence() {
 
 }  // namespace
 
+// The compute schedule is a list of 2*nmb segments, each all GEMM1 or all GEMM2
+// tiles of one minibatch.  With two or more ring buffers it is software-pipelined,
+//   G1(0) G1(1) G2(0) G1(2) G2(1) ... G1(nmb-1) G2(nmb-2) G2(nmb-1),
+// so a GEMM2 tile's inputs were finished a whole minibatch earlier; with a single
+// ring buffer it is G1(0) G2(0) G1(1) G2(1) ... (the gather of b needs G2(b-1)).
+struct Segment {
+    int kind, b;
+};
+
+__host__ __device__ __forceinline__ Segment segment_of(int j, int nmb, bool interleave) {
+    if (!interleave) return Segment{j & 1, j >> 1};
+    if (j == 0) return Segment{0, 0};
+    if (j == 2 * nmb - 1) return Segment{1, nmb - 1};
+    return (j & 1) ? Segment{0, (j + 1) >> 1} : Segment{1, (j >> 1) - 1};
+}
+
 // Counters and plan arrays in the workspace (int32 unless noted).
 struct FusedPlan {
-    int* tbase;        // [nmb+1] tile prefix over minibatches (P_b * (NT1 + NT2) each)
+    int* tbase;        // [2*nmb+1] tile prefix over the segments of the schedule
     int* pbase;        // [nmb+1] m-tile prefix over minibatches (P_b each)
     int* elo;          // [nmb] first expert overlapping minibatch b
     int* gather_done;  // [nmb] gather CTAs done with minibatch b
@@ -106,9 +122,9 @@ struct FusedArgs {
 
 // One block: per-minibatch m-tile counts, prefixes, first experts; zero counters.
 __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restrict__ offsets, int E,
-                                                          int T, int MB, int nmb, int nt_sum,
-                                                          FusedPlan plan, int counters_len,
-                                                          int* counters) {
+                                                          int T, int MB, int nmb, int nt1, int nt2,
+                                                          int interleave, FusedPlan plan,
+                                                          int counters_len, int* counters) {
     extern __shared__ int32_t off[];
     for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = offsets[e];
     for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
@@ -126,15 +142,16 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
             const int len = min(off[e + 1], hi) - max(off[e], lo);
             if (len > 0) P += (len + tc::BM - 1) / tc::BM;
         }
-        plan.tbase[b] = P;   // the count for now; the scan below turns it into prefixes
+        plan.pbase[b] = P;   // the count for now; the scan below turns it into prefixes
     }
     __syncthreads();
     if (threadIdx.x < 32) {
+        // m-tile prefix over minibatches (each lane touches only its own b's)
         const int lane = threadIdx.x;
         const int per = (nmb + 31) / 32;
         const int lo = min(lane * per, nmb), hi = min(lo + per, nmb);
         int s = 0;
-        for (int b = lo; b < hi; ++b) s += plan.tbase[b];
+        for (int b = lo; b < hi; ++b) s += plan.pbase[b];
         int incl = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -142,16 +159,36 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
             if (lane >= o) incl += v;
         }
         int run = incl - s;
-        for (int b = lo; b < hi; ++b) {       // each lane touches only its own b's
-            const int P = plan.tbase[b];
+        for (int b = lo; b < hi; ++b) {
+            const int P = plan.pbase[b];
             plan.pbase[b] = run;
-            plan.tbase[b] = run * nt_sum;
             run += P;
         }
-        if (lane == 31) {
-            plan.pbase[nmb] = incl;
-            plan.tbase[nmb] = incl * nt_sum;
+        __syncwarp();
+        if (lane == 31) plan.pbase[nmb] = incl;
+        __syncwarp();
+        // tile prefix over the 2*nmb segments of the schedule
+        const int nseg = 2 * nmb;
+        const int pers = (nseg + 31) / 32;
+        const int slo = min(lane * pers, nseg), shi = min(slo + pers, nseg);
+        auto seg_tiles = [&](int j) {
+            const Segment sg = segment_of(j, nmb, interleave != 0);
+            return (plan.pbase[sg.b + 1] - plan.pbase[sg.b]) * (sg.kind == 0 ? nt1 : nt2);
+        };
+        int ss = 0;
+        for (int j = slo; j < shi; ++j) ss += seg_tiles(j);
+        int sincl = ss;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, sincl, o);
+            if (lane >= o) sincl += v;
         }
+        int srun = sincl - ss;
+        for (int j = slo; j < shi; ++j) {
+            plan.tbase[j] = srun;
+            srun += seg_tiles(j);
+        }
+        if (lane == 31) plan.tbase[nseg] = sincl;
     }
 }
 
@@ -164,24 +201,20 @@ struct MinibatchTiles {
     int nt1, nt2, c0, C;      // N tiles of GEMM1 / GEMM2, this CTA's index among C
     __device__ int first() const { return c0; }
     __device__ int next(int t) const { return t + C; }
-    __device__ int count() const { return a->plan.tbase[a->nmb]; }
+    __device__ int count() const { return a->plan.tbase[2 * a->nmb]; }
     __device__ TileInfo tile(int t) const {
         const FusedPlan& pl = a->plan;
-        int lo = 0, hi = a->nmb;   // last b with tbase[b] <= t
+        int lo = 0, hi = 2 * a->nmb;   // last segment j with tbase[j] <= t
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (pl.tbase[mid] <= t) lo = mid; else hi = mid;
         }
-        const int b = lo;
+        const Segment sg = segment_of(lo, a->nmb, a->NR >= 2);
+        const int b = sg.b;
         const int P = pl.pbase[b + 1] - pl.pbase[b];
-        int local = t - pl.tbase[b];
+        const int local = t - pl.tbase[lo];
         TileInfo tl;
-        if (local < P * nt1) {
-            tl.kind = 0;
-        } else {
-            tl.kind = 1;
-            local -= P * nt1;
-        }
+        tl.kind = sg.kind;
         tl.n = local / P;
         const int mi = local % P;
         const int s_lo = b * a->MB, s_hi = min(s_lo + a->MB, a->T);
@@ -343,10 +376,8 @@ __device__ void combine_role(const FusedArgs& a) {
 
 template <bool MX>
 __global__ void __launch_bounds__(tc::THREADS, 1)
-    fused_forward_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                         const __grid_constant__ CUtensorMap tmS1a, const __grid_constant__ CUtensorMap tmS1b,
-                         const __grid_constant__ CUtensorMap tmS2a, const __grid_constant__ CUtensorMap tmS2b,
+    fused_forward_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
+                         const __grid_constant__ CUtensorMap tmS1a, const __grid_constant__ CUtensorMap tmS2a,
                          const GemmSide s1, const GemmSide s2, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -363,13 +394,9 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         MinibatchTiles src{&a, off, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G, (int)gridDim.x - a.G};
         GemmMaps maps;
         maps.a[0] = &tmA1;
-        maps.b[0] = &tmB1;
         maps.a[1] = &tmA2;
-        maps.b[1] = &tmB2;
         maps.sfa[0] = &tmS1a;
-        maps.sfb[0] = &tmS1b;
         maps.sfa[1] = &tmS2a;
-        maps.sfb[1] = &tmS2b;
         GemmSide sides[2] = {s1, s2};
         run_gemm_pipeline<MX>(smem, maps, sides, src, a.ws, a.timeout_ns);
     }
@@ -391,9 +418,9 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     int* w = c.plan_ints;
     FusedPlan pl;
     pl.tbase = w;
-    pl.pbase = w + (c.nmb + 1);
-    pl.elo = w + 2 * (c.nmb + 1);
-    int* counters = w + 3 * (c.nmb + 1);
+    pl.pbase = w + (2 * c.nmb + 2);
+    pl.elo = pl.pbase + (c.nmb + 1);
+    int* counters = pl.elo + (c.nmb + 1);
     const int max_m = fused_max_mtiles(c.T, c.E, c.nmb);
     pl.gather_done = counters;
     pl.g2_done = counters + c.nmb;
@@ -406,7 +433,8 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     GemmSide s1, s2;
     if (!encode_ffn_maps(c.ffn, &m, &s1, &s2)) return cudaErrorInvalidValue;
     fused_plan_kernel<<<1, 1024, sizeof(int32_t) * (c.E + 1), stream>>>(
-        c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles + s2.n_tiles, pl, counters_len, counters);
+        c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles, s2.n_tiles, (c.R / c.MB) >= 2 ? 1 : 0, pl,
+        counters_len, counters);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
@@ -442,7 +470,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     void* kern = c.ffn.mx ? (void*)fused_forward_kernel<true> : (void*)fused_forward_kernel<false>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    void* args[] = {&m.a1, &m.b1, &m.a2, &m.b2, &m.s1a, &m.s1b, &m.s2a, &m.s2b, &s1, &s2, &a};
+    void* args[] = {&m.a1, &m.a2, &m.s1a, &m.s2a, &s1, &s2, &a};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.G + c.C);
     cfg.blockDim = dim3(tc::THREADS);

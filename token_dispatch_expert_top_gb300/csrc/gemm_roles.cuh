@@ -4,13 +4,16 @@
 //
 // One CTA of 12 warps per SM runs a software pipeline over a sequence of output
 // tiles handed out by a tile source:
-//   warp 0      TMA producer: A tile (128 rows x 128 B) and B tile (256 rows x
-//               128 B) per K-stage into a 4-stage shared-memory ring; for MXFP8
-//               with K % 512 == 0 also the scale bytes of four K-stages at a time
+//   warp 0      producer: per K-stage, the A tile (128 rows x 128 B) by a TMA
+//               tensor load and the B tile (256 rows x 128 B) plus, for MXFP8,
+//               its 1 KB scale image by two bulk copies from the tile-packed
+//               weights, into a 4-stage shared-memory ring; for MXFP8 with
+//               K % 512 == 0 also the A scale bytes of four K-stages at a time
 //   warp 1      TMEM owner and MMA issuer (one thread): tcgen05.mma 128x256,
 //               kind::f16 (BF16) or kind::mxf8f6f4 with UE8M0 block scales
-//   warp 2      scale-factor transposer (MXFP8): builds the [32 lanes][4 words]
-//               blocks that tcgen05.cp moves into tensor memory
+//   warp 2      A scale-factor transposer (MXFP8): builds the [32 lanes][4 words]
+//               block of the A rows that tcgen05.cp moves into tensor memory (the
+//               B scales arrive already in that form)
 //   warp 3      idle after the prologue
 //   warps 4-11  epilogue: two warps per tensor-memory lane quarter, each taking
 //               half the columns, drain the FP32 accumulator into registers,
@@ -37,15 +40,15 @@ constexpr int A_BYTES = BM * 128;
 constexpr int B_BYTES = BN * 128;
 constexpr int SFA_BYTES = 512;                             // [32 lanes][4 words]: 128 rows x 4 K-steps
 constexpr int SFB_BYTES = 1024;                            // two such blocks (256 rows)
-constexpr int SFSA_BYTES = BM * 16;                        // staged scales: 128 rows x 16 B (4 stages)
-constexpr int SFSB_BYTES = BN * 16;
+constexpr int SFSA_BYTES = BM * 16;                        // staged A scales: 128 rows x 16 B (4 stages)
+constexpr int B_TILE = B_BYTES;                            // packed B tile image
+constexpr int SFB_TILE = SFB_BYTES;                        // packed B scale image
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr int OFF_SFSA = OFF_SFB + STAGES * SFB_BYTES;
-constexpr int OFF_SFSB = OFF_SFSA + SFG * SFSA_BYTES;
-constexpr int OFF_BAR = OFF_SFSB + SFG * SFSB_BYTES;
+constexpr int OFF_BAR = OFF_SFSA + SFG * SFSA_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * SFG;        // full, empty, tfull, tempty, drain, sfull, sempty
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;           // tmem base, abort flag
 constexpr int OFF_TAIL = OFF_MISC + 16;                    // kernel-specific tail
@@ -62,10 +65,11 @@ struct GemmSide {
     int n_tiles;              // N tiles per expert
     int up_off;               // GEMM1: first up row inside w_gate_up (= I)
     int b_rows;               // rows of one expert's weight matrix (2I or H)
-    int sf_tma;               // MXFP8 scales staged by TMA (K % 512 == 0)
+    int sf_tma;               // MXFP8 A scales staged by TMA (K % 512 == 0)
     int a_rows;               // rows of the A tensor (scale loads stay inside)
     const uint8_t* a_sf;      // MXFP8: [a_rows][K/32]
-    const uint8_t* b_sf;      // MXFP8: [E][b_rows][K/32]
+    const uint8_t* b_pk;      // tile-packed weights [E][n_tiles][K-stages][32 KB]
+    const uint8_t* sfb_pk;    // MXFP8: tile-packed scales [E][n_tiles][K-stages][1 KB]
     uint8_t* out;             // GEMM1: h [rows][I] (codes or BF16); GEMM2: y BF16 [rows][H]
     uint8_t* out_sf;          // GEMM1 MXFP8: h scales [rows][I/32]
     int out_ld;               // row length of out in elements
@@ -73,9 +77,7 @@ struct GemmSide {
 
 struct GemmMaps {
     const CUtensorMap* a[2];
-    const CUtensorMap* b[2];
     const CUtensorMap* sfa[2];
-    const CUtensorMap* sfb[2];
 };
 
 struct TileInfo {
@@ -149,17 +151,13 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
         if (!src.wait_inputs(tl, p)) return;
         const bool sf_tma = MX && sd.sf_tma;
         const int KB = sd.K / (MX ? 128 : 64);
-        const int brow0 = tl.kind == 0 ? tl.n * 128 : tl.n * BN;
-        const int brow1 = tl.kind == 0 ? sd.up_off + tl.n * 128 : tl.n * BN + 128;
+        const int64_t tile0 = ((int64_t)tl.e * sd.n_tiles + tl.n) * KB;   // first packed K-stage
         for (int kb = 0; kb < KB; ++kb) {
             if (sf_tma && (kb & 3) == 0) {
                 if (!mbar_wait_bounded(&p.sempty[g], gphase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
-                uint8_t* sa = p.smem + OFF_SFSA + g * SFSA_BYTES;
-                uint8_t* sb = p.smem + OFF_SFSB + g * SFSB_BYTES;
-                mbar_arrive_expect_tx(&p.sfull[g], SFSA_BYTES + SFSB_BYTES);
-                tma_load_2d(sa, maps.sfa[tl.kind], &p.sfull[g], kb * 4, tl.a_row0);
-                tma_load_3d(sb, maps.sfb[tl.kind], &p.sfull[g], kb * 4, brow0, tl.e);
-                tma_load_3d(sb + SFSB_BYTES / 2, maps.sfb[tl.kind], &p.sfull[g], kb * 4, brow1, tl.e);
+                mbar_arrive_expect_tx(&p.sfull[g], SFSA_BYTES);
+                tma_load_2d(p.smem + OFF_SFSA + g * SFSA_BYTES, maps.sfa[tl.kind], &p.sfull[g], kb * 4,
+                            tl.a_row0);
                 if (++g == SFG) {
                     g = 0;
                     gphase ^= 1;
@@ -168,15 +166,12 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
             if (!mbar_wait_bounded(&p.empty[stage], phase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
             uint8_t* sa = p.smem + OFF_A + stage * A_BYTES;
             uint8_t* sb = p.smem + OFF_B + stage * B_BYTES;
-            mbar_arrive_expect_tx(&p.full[stage], A_BYTES + B_BYTES);
-            const int kx = kb * (MX ? 128 : 64);
-            tma_load_2d(sa, maps.a[tl.kind], &p.full[stage], kx, tl.a_row0);
-            if (tl.kind == 0) {
-                tma_load_3d(sb, maps.b[0], &p.full[stage], kx, brow0, tl.e);
-                tma_load_3d(sb + B_BYTES / 2, maps.b[0], &p.full[stage], kx, brow1, tl.e);
-            } else {
-                tma_load_3d(sb, maps.b[1], &p.full[stage], kx, brow0, tl.e);
-            }
+            mbar_arrive_expect_tx(&p.full[stage], A_BYTES + B_BYTES + (MX ? SFB_BYTES : 0));
+            tma_load_2d(sa, maps.a[tl.kind], &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
+            bulk_load(sb, sd.b_pk + (tile0 + kb) * B_TILE, B_TILE, &p.full[stage]);
+            if (MX)
+                bulk_load(p.smem + OFF_SFB + stage * SFB_BYTES, sd.sfb_pk + (tile0 + kb) * SFB_TILE,
+                          SFB_TILE, &p.full[stage]);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
@@ -238,10 +233,10 @@ __device__ void mma_role(const Pipe& p, const GemmSide* sides, Src& src) {
     }
 }
 
-// ------------------------------------------- scale factors (MXFP8, whole warp 2)
-// Each K-stage needs, for the A rows and for both 128-row halves of B, a
-// [32 lanes][4 words] block: word j of lane r holds the four K-step scales of
-// row 32j + r.  tcgen05.cp moves that block into tensor memory.
+// ----------------------------------------- A scale factors (MXFP8, whole warp 2)
+// Each K-stage needs a [32 lanes][4 words] block for the A rows: word j of lane r
+// holds the four K-step scales of row 32j + r.  tcgen05.cp moves that block into
+// tensor memory; the B scales arrive already packed this way.
 template <class Src>
 __device__ void sf_role(const Pipe& p, const GemmSide* sides, Src& src) {
     using namespace tc;
@@ -260,19 +255,13 @@ __device__ void sf_role(const Pipe& p, const GemmSide* sides, Src& src) {
                 if (!mbar_wait_bounded(&p.empty[stage], phase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
                 const int q = kb & 3;
                 const uint8_t* sa = p.smem + OFF_SFSA + g * SFSA_BYTES + 4 * q;
-                const uint8_t* sb = p.smem + OFF_SFSB + g * SFSB_BYTES + 4 * q;
-                uint32_t a[4], b[8];
+                uint32_t a[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) a[j] = *reinterpret_cast<const uint32_t*>(sa + (32 * j + lane) * 16);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) b[i] = *reinterpret_cast<const uint32_t*>(sb + (32 * i + lane) * 16);
-                uint4* sfa = reinterpret_cast<uint4*>(p.smem + OFF_SFA + stage * SFA_BYTES);
-                uint4* sfb = reinterpret_cast<uint4*>(p.smem + OFF_SFB + stage * SFB_BYTES);
-                sfa[lane] = make_uint4(a[0], a[1], a[2], a[3]);
-                sfb[lane] = make_uint4(b[0], b[1], b[2], b[3]);
-                sfb[32 + lane] = make_uint4(b[4], b[5], b[6], b[7]);
-                // every lane's reads are consumed by its own stores before the
-                // fence, so the releases below cannot overtake them
+                reinterpret_cast<uint4*>(p.smem + OFF_SFA + stage * SFA_BYTES)[lane] =
+                    make_uint4(a[0], a[1], a[2], a[3]);
+                // every lane's reads are consumed by its own store before the fence,
+                // so the releases below cannot overtake them
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -294,40 +283,21 @@ __device__ void sf_role(const Pipe& p, const GemmSide* sides, Src& src) {
             // (fused kernel), so every lane first waits for the tile's inputs
             // itself (its own acquire) and the loads bypass L1.
             if (!src.wait_inputs(tl, p)) return;
-            const uint8_t* bsf = sd.b_sf + (int64_t)tl.e * sd.b_rows * ksf;
-            int brow[8];
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    brow[c * 4 + j] = tl.kind == 0 ? (c * sd.up_off + tl.n * 128 + 32 * j + lane)
-                                                   : (tl.n * BN + c * 128 + 32 * j + lane);
             for (int kb4 = 0; kb4 < KB; kb4 += 4) {
-                uint4 va[4], vb[8];
+                uint4 va[4];
                 const int nq = min(4, KB - kb4);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int row = tl.a_row0 + 32 * j + lane;
                     uint32_t w[4] = {0, 0, 0, 0};
                     for (int q = 0; q < nq; ++q)
-                        if (row < sd.a_rows)
-                            w[q] = ld_cg_u32(sd.a_sf + (int64_t)row * ksf + (kb4 + q) * 4);
+                        if (row < sd.a_rows) w[q] = ld_cg_u32(sd.a_sf + (int64_t)row * ksf + (kb4 + q) * 4);
                     va[j] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t w[4] = {0, 0, 0, 0};
-                    for (int q = 0; q < nq; ++q)
-                        w[q] = *reinterpret_cast<const uint32_t*>(bsf + (int64_t)brow[i] * ksf + (kb4 + q) * 4);
-                    vb[i] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 for (int q = 0; q < nq; ++q) {
                     if (!mbar_wait_bounded(&p.empty[stage], phase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
-                    uint4* sfa = reinterpret_cast<uint4*>(p.smem + OFF_SFA + stage * SFA_BYTES);
-                    uint4* sfb = reinterpret_cast<uint4*>(p.smem + OFF_SFB + stage * SFB_BYTES);
-                    sfa[lane] = make_uint4(word_of(va[0], q), word_of(va[1], q), word_of(va[2], q), word_of(va[3], q));
-                    sfb[lane] = make_uint4(word_of(vb[0], q), word_of(vb[1], q), word_of(vb[2], q), word_of(vb[3], q));
-                    sfb[32 + lane] = make_uint4(word_of(vb[4], q), word_of(vb[5], q), word_of(vb[6], q), word_of(vb[7], q));
+                    reinterpret_cast<uint4*>(p.smem + OFF_SFA + stage * SFA_BYTES)[lane] =
+                        make_uint4(word_of(va[0], q), word_of(va[1], q), word_of(va[2], q), word_of(va[3], q));
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p.full[stage]);
@@ -444,9 +414,7 @@ __device__ void run_gemm_pipeline(uint8_t* smem, const GemmMaps& maps, const Gem
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         prefetch_tmap(maps.a[0]);
-        prefetch_tmap(maps.b[0]);
         prefetch_tmap(maps.a[1]);
-        prefetch_tmap(maps.b[1]);
     }
     tc_fence_before();
     __syncthreads();

@@ -10,6 +10,7 @@
 // Expert segments of rows are [offsets[e], offsets[e+1]) of the A operand; the
 // kernel reads the offsets on device and enumerates (expert, m-tile, n-tile)
 // tiles itself, m-tiles innermost so consecutive CTAs share weight tiles in L2.
+// The weights come tile-packed (pack.cu): one bulk copy per 32 KB B tile.
 // ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
 // NVL72": section 01, the grouped GEMM fed expert-contiguous input on Blackwell
 // tensor cores; section 02, SwiGLU and MXFP8 activation quantisation inside the
@@ -70,9 +71,7 @@ struct ExpertTiles {
 template <bool MX, int KIND>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmSFA,
-                           const __grid_constant__ CUtensorMap tmSFB, const GemmSide side,
+                           const __grid_constant__ CUtensorMap tmSFA, const GemmSide side,
                            const int32_t* offsets, int E, WsHeader* ws,
                            unsigned long long timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -103,9 +102,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     ExpertTiles src{offsets, mpre, E, side.n_tiles, KIND, mpre[E] * side.n_tiles};
     GemmMaps maps;
     maps.a[0] = maps.a[1] = &tmA;
-    maps.b[0] = maps.b[1] = &tmB;
     maps.sfa[0] = maps.sfa[1] = &tmSFA;
-    maps.sfb[0] = maps.sfb[1] = &tmSFB;
     GemmSide sides[2] = {side, side};
     run_gemm_pipeline<MX>(smem, maps, sides, src, ws, timeout_ns);
 }
@@ -114,36 +111,29 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 inline size_t gemm_smem_bytes(int E) { return 1024 + tc::OFF_TAIL + sizeof(int32_t) * (E + 1); }
 
 template <bool MX, int KIND>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                              const CUtensorMap& tsb, const GemmSide& side, const int32_t* offsets,
-                              int E, WsHeader* ws, unsigned long long timeout_ns, int grid,
-                              cudaStream_t stream) {
+static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tsa, const GemmSide& side,
+                              const int32_t* offsets, int E, WsHeader* ws,
+                              unsigned long long timeout_ns, int grid, cudaStream_t stream) {
     auto kern = tc_grouped_gemm_kernel<MX, KIND>;
     const size_t smem = gemm_smem_bytes(E);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tb, tsa, tsb, side, offsets, E, ws, timeout_ns);
+    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tsa, side, offsets, E, ws, timeout_ns);
     return cudaGetLastError();
 }
 
-// Scale tensors as 16-byte-wide TMA boxes of 128 rows (four K-stages of scales).
-bool encode_sf_maps(CUtensorMap* tsa, CUtensorMap* tsb, const void* a_sf, int a_rows,
-                    const void* b_sf, int b_rows, int E, int K) {
+// A scales as 16-byte-wide TMA boxes of 128 rows (four K-stages of scales).
+static bool encode_sfa_map(CUtensorMap* tsa, const void* a_sf, int a_rows, int K) {
     const uint64_t ksf = (uint64_t)K / 32;
     uint64_t da[2] = {ksf, (uint64_t)a_rows};
     uint64_t sa[1] = {ksf};
     uint32_t ba[2] = {16, 128};
-    if (!encode_tmap(tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a_sf, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return false;
-    uint64_t db[3] = {ksf, (uint64_t)b_rows, (uint64_t)E};
-    uint64_t sb[2] = {ksf, (uint64_t)b_rows * ksf};
-    uint32_t bb[3] = {16, 128, 1};
-    return encode_tmap(tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b_sf, db, sb, bb, CU_TENSOR_MAP_SWIZZLE_NONE);
+    return encode_tmap(tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a_sf, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Operand maps of both GEMMs: A1 = a [a_rows][H], B1 = w_gate_up [E][2I][H] (two
-// 128-row boxes per stage), A2 = h [a_rows][I], B2 = w_down [E][H][I] (one
-// 256-row box), plus the scale maps when the scales are TMA-staged.
+// A operand maps of both GEMMs (a [a_rows][H] and h [a_rows][I], 128-row boxes of
+// 128 bytes, 128-byte swizzle), the A scale maps when TMA-staged, and the two
+// GemmSides over the tile-packed weights.
 bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2) {
     const bool mx = c.mx;
     const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -154,20 +144,12 @@ bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2)
         uint64_t str[1] = {(uint64_t)c.H * esz};
         uint32_t box[2] = {bk, 128};
         if (!encode_tmap(&m->a1, dt, 2, c.a, dims, str, box)) return false;
-        uint64_t dimsb[3] = {(uint64_t)c.H, (uint64_t)2 * c.I, (uint64_t)c.E};
-        uint64_t strb[2] = {(uint64_t)c.H * esz, (uint64_t)2 * c.I * c.H * esz};
-        uint32_t boxb[3] = {bk, 128, 1};
-        if (!encode_tmap(&m->b1, dt, 3, c.w_gate_up, dimsb, strb, boxb)) return false;
     }
     {
         uint64_t dims[2] = {(uint64_t)c.I, (uint64_t)c.a_rows};
         uint64_t str[1] = {(uint64_t)c.I * esz};
         uint32_t box[2] = {bk, 128};
         if (!encode_tmap(&m->a2, dt, 2, c.h, dims, str, box)) return false;
-        uint64_t dimsb[3] = {(uint64_t)c.I, (uint64_t)c.H, (uint64_t)c.E};
-        uint64_t strb[2] = {(uint64_t)c.I * esz, (uint64_t)c.H * c.I * esz};
-        uint32_t boxb[3] = {bk, 256, 1};
-        if (!encode_tmap(&m->b2, dt, 3, c.w_down, dimsb, strb, boxb)) return false;
     }
     *s1 = GemmSide{};
     s1->K = c.H;
@@ -176,7 +158,8 @@ bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2)
     s1->b_rows = 2 * c.I;
     s1->a_rows = c.a_rows;
     s1->a_sf = (const uint8_t*)c.a_sf;
-    s1->b_sf = (const uint8_t*)c.w_gu_sf;
+    s1->b_pk = (const uint8_t*)c.w_gate_up;
+    s1->sfb_pk = (const uint8_t*)c.w_gu_sf;
     s1->out = (uint8_t*)c.h;
     s1->out_sf = (uint8_t*)c.h_sf;
     s1->out_ld = c.I;
@@ -186,21 +169,18 @@ bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2)
     s2->up_off = 0;
     s2->b_rows = c.H;
     s2->a_sf = (const uint8_t*)c.h_sf;
-    s2->b_sf = (const uint8_t*)c.w_d_sf;
+    s2->b_pk = (const uint8_t*)c.w_down;
+    s2->sfb_pk = (const uint8_t*)c.w_d_sf;
     s2->out = (uint8_t*)c.y;
     s2->out_sf = nullptr;
     s2->out_ld = c.H;
     m->s1a = CUtensorMap{};
-    m->s1b = CUtensorMap{};
     m->s2a = CUtensorMap{};
-    m->s2b = CUtensorMap{};
     if (mx) {
         s1->sf_tma = (c.H % 512) == 0;
         s2->sf_tma = (c.I % 512) == 0;
-        if (s1->sf_tma && !encode_sf_maps(&m->s1a, &m->s1b, c.a_sf, c.a_rows, c.w_gu_sf, 2 * c.I, c.E, c.H))
-            return false;
-        if (s2->sf_tma && !encode_sf_maps(&m->s2a, &m->s2b, c.h_sf, c.a_rows, c.w_d_sf, c.H, c.E, c.I))
-            return false;
+        if (s1->sf_tma && !encode_sfa_map(&m->s1a, c.a_sf, c.a_rows, c.H)) return false;
+        if (s2->sf_tma && !encode_sfa_map(&m->s2a, c.h_sf, c.a_rows, c.I)) return false;
     }
     return true;
 }
@@ -212,13 +192,13 @@ cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream) {
     if (!encode_ffn_maps(c, &m, &s1, &s2)) return cudaErrorInvalidValue;
     cudaError_t err;
     if (c.mx) {
-        err = launch_one<true, 0>(m.a1, m.b1, m.s1a, m.s1b, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<true, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<true, 1>(m.a2, m.b2, m.s2a, m.s2b, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<true, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     } else {
-        err = launch_one<false, 0>(m.a1, m.b1, m.s1a, m.s1b, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<false, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<false, 1>(m.a2, m.b2, m.s2a, m.s2b, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<false, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     }
     return err;
 }

@@ -50,10 +50,10 @@ struct TcFfnCall {
     const void* a;            // [a_rows][H]
     const void* a_sf;         // [a_rows][H/32] (MXFP8)
     const int32_t* offsets;   // [E+1]
-    const void* w_gate_up;    // [E][2I][H]
-    const void* w_gu_sf;      // [E][2I][H/32] (MXFP8)
-    const void* w_down;       // [E][H][I]
-    const void* w_d_sf;       // [E][H][I/32] (MXFP8)
+    const void* w_gate_up;    // tile-packed GEMM1 weights (pack.cu)
+    const void* w_gu_sf;      // tile-packed GEMM1 scales (MXFP8)
+    const void* w_down;       // tile-packed GEMM2 weights
+    const void* w_d_sf;       // tile-packed GEMM2 scales (MXFP8)
     void* h;                  // [a_rows][I] scratch
     void* h_sf;               // [a_rows][I/32] scratch (MXFP8)
     void* y;                  // [a_rows][H] BF16
@@ -64,14 +64,31 @@ struct TcFfnCall {
 
 cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream);
 
+// One-time repacking of natural K-major expert weights into tile images.
+struct PackCall {
+    bool mx;
+    int E, H, I;
+    const void* w_gate_up;    // [E][2I][H] codes or BF16
+    const uint8_t* w_gu_sf;   // [E][2I][H/32]
+    const void* w_down;       // [E][H][I]
+    const uint8_t* w_d_sf;    // [E][H][I/32]
+    void* p_gate_up;
+    uint8_t* p_gu_sf;
+    void* p_down;
+    uint8_t* p_d_sf;
+    int num_sms;
+};
+cudaError_t launch_pack_weights(const PackCall& c, cudaStream_t stream);
+
 // Fused persistent forward (gather, expert FFN, combine in one launch).
 // Upper bound on the m-tiles of all minibatches: each piece (expert x minibatch)
 // of L slots takes ceil(L/128) <= L/128 + 1 tiles and there are at most E + nmb
 // pieces.
 inline int fused_max_mtiles(int T, int E, int nmb) { return T / 128 + E + 2 * nmb + 8; }
-// int32 entries of the plan + counter region: tbase, pbase, elo, then counters
+// int32 entries of the plan + counter region: tbase [2nmb+2], pbase [nmb+1],
+// elo [nmb+1], then the counters
 inline size_t fused_plan_ints(int T, int E, int nmb) {
-    return (size_t)3 * (nmb + 1) + 2 * nmb + 8 + fused_max_mtiles(T, E, nmb);
+    return (size_t)(2 * nmb + 2) + 2 * (nmb + 1) + 2 * nmb + 8 + fused_max_mtiles(T, E, nmb);
 }
 struct FusedCall {
     TcFfnCall ffn;            // a = ring [R][H], h = ring [R][I], y = [T][H]
@@ -92,7 +109,7 @@ int fused_max_ctas();
 
 // TMA maps of both expert GEMMs (operands and, for MXFP8, staged scales).
 struct FfnMaps {
-    CUtensorMap a1, b1, a2, b2, s1a, s1b, s2a, s2b;
+    CUtensorMap a1, a2, s1a, s2a;
 };
 struct GemmSide;
 bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2);

@@ -10,6 +10,16 @@ from . import moe as M
 from .synth import Workload, master_dtype
 
 
+def pack_expert_weights(shape, wgu, wgu_sf, wd, wd_sf):
+    """Tile-packed copies of the expert weights (and scales), made by libmoe."""
+    p_gu = torch.empty_like(wgu)
+    p_d = torch.empty_like(wd)
+    p_gu_sf = None if wgu_sf is None else torch.empty_like(wgu_sf)
+    p_d_sf = None if wd_sf is None else torch.empty_like(wd_sf)
+    M.moe_pack_expert_weights(shape, wgu, wgu_sf, wd, wd_sf, p_gu, p_gu_sf, p_d, p_d_sf)
+    return p_gu, p_gu_sf, p_d, p_d_sf
+
+
 def quantize_mxfp8(t: torch.Tensor):
     """MXFP8 codes and scales of t along its last axis, made by libmoe."""
     K = t.shape[-1]
@@ -32,10 +42,13 @@ class MoeLayer:
         wgu = inputs["w_gate_up"].to(dev).contiguous()
         wd = inputs["w_down"].to(dev).contiguous()
         if w.dtype == "mxfp8":
-            self.wgu, self.wgu_sf = quantize_mxfp8(wgu)
-            self.wd, self.wd_sf = quantize_mxfp8(wd)
+            q_gu, q_gu_sf = quantize_mxfp8(wgu)
+            q_d, q_d_sf = quantize_mxfp8(wd)
         else:
-            self.wgu, self.wgu_sf, self.wd, self.wd_sf = wgu, None, wd, None
+            q_gu, q_gu_sf, q_d, q_d_sf = wgu, None, wd, None
+        self.wgu, self.wgu_sf, self.wd, self.wd_sf = pack_expert_weights(
+            self.shape, q_gu, q_gu_sf, q_d, q_d_sf)
+        del q_gu, q_gu_sf, q_d, q_d_sf
         if keep_master:
             self.master = (wgu, wd)
         else:

@@ -27,6 +27,7 @@ ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_last_device_status", "moe_status_string",
     "moe_quantize_mxfp8", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
     "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
+    "moe_pack_expert_weights",
 )
 
 
@@ -77,6 +78,7 @@ _SIGS = {
                                _sz, _vp]),
     "moe_min_minibatch": (_i, [_i, _i, _i, _i, _i]),
     "moe_layout_noalloc": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_pack_expert_weights": (_i, [_shp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -134,6 +136,15 @@ def moe_quantize_mxfp8(inp: torch.Tensor, codes: torch.Tensor, scales: torch.Ten
     rows = inp.numel() // K
     _check("moe_quantize_mxfp8", _lib.moe_quantize_mxfp8(_p(inp), dt, rows, K, _p(codes), _p(scales),
                                                          _stream(stream)))
+
+
+def moe_pack_expert_weights(shape: Shape, w_gate_up, w_gu_scales, w_down, w_d_scales,
+                            packed_gate_up, packed_gu_scales, packed_down, packed_d_scales,
+                            stream=None) -> None:
+    _check("moe_pack_expert_weights", _lib.moe_pack_expert_weights(
+        ctypes.byref(shape), _p(w_gate_up), _p(w_gu_scales), _p(w_down), _p(w_d_scales),
+        _p(packed_gate_up), _p(packed_gu_scales), _p(packed_down), _p(packed_d_scales),
+        _stream(stream)))
 
 
 def _wsz(ws):
