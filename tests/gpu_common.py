@@ -28,3 +28,16 @@ def need_cuda():
     import pytest
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+
+
+def check_routing(g_idx, ref_idx, ref_logits, gap, tau=TIE_TAU):
+    """Routing of every token away from selection near-ties: the selected expert
+    set equals the oracle's (unique), and the kernel's order is descending in the
+    FP64 logits up to tau (the order of near-equal selected logits is not unique).
+    Returns the fraction of tokens checked."""
+    import numpy as np
+    ok = gap >= tau
+    np.testing.assert_array_equal(np.sort(g_idx[ok], axis=1), np.sort(ref_idx[ok], axis=1))
+    lg = np.take_along_axis(ref_logits, g_idx.astype(np.int64), axis=1)
+    assert np.all(np.diff(lg[ok], axis=1) <= tau)
+    return ok.mean()

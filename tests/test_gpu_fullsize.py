@@ -1,0 +1,91 @@
+"""Full-size parity for the DeepSeek-V3-shaped layers (N=8192 or 16384, H=7168,
+I=2048, E=256, top-8, MXFP8): routing of every token and the outputs of a seeded
+sample of tokens against the oracle, the hottest expert's outputs in the skewed
+layer, and the persistent fused forward equal to the staged one bit for bit --
+with the default ring and with rings of 64, 256 and 1024 slots."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_common import TIE_TAU, TOL, check_routing, need_cuda, row_rel_err, to_np
+from token_dispatch_expert_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(name, params=None):
+    need_cuda()
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)            # drawn on the device
+    layer = MoeLayer(w, inp, params=params)
+    return w, inp, layer
+
+
+def _oracle_weights(inp, dtype):
+    return lambda e: O.expert_operands(inp["w_gate_up"][e].cpu(), inp["w_down"][e].cpu(), dtype)
+
+
+@pytest.mark.parametrize("name,sample", [("dsv3_mxfp8", 96), ("dsv3_mxfp8_skew", 64),
+                                         ("dsv3_mxfp8_skew_16k", 32)])
+def test_fullsize_sampled_parity_and_fused_equality(name, sample):
+    w, inp, layer = _setup(name)
+    staged = layer.forward().clone()
+    idx = to_np(layer.idx)
+    fused = layer.forward(fused=True)
+    assert layer.device_status() == 0
+    assert torch.equal(fused, staged)
+    toks = np.sort(np.random.default_rng(0).choice(w.N, size=sample, replace=False))
+    ref = O.forward(inp, w.E, w.k, w.S, w.dtype, tokens=toks, weights=_oracle_weights(inp, w.dtype))
+    assert check_routing(idx, ref["idx"], ref["logits"], ref["gap"]) > 0.97   # every token
+    ok = (ref["gap"] >= TIE_TAU)[toks]
+    err = row_rel_err(to_np(staged)[toks][ok], ref["out"][ok])
+    assert err.max() < TOL[w.dtype], err.max()
+    if w.skew:
+        counts = np.bincount(ref["idx"].ravel(), minlength=w.E)
+        print(f"{name}: max/mean expert load {counts.max() / counts.mean():.1f}, "
+              f"{(counts == 0).sum()} empty experts")
+
+
+def test_fullsize_hottest_expert_rows():
+    """All-token expert of the skewed layer: 512 of its slot rows through the
+    expert FFN entry point against the oracle's FFN of those rows."""
+    from token_dispatch_expert_top_gb300 import moe as M
+    w, inp, layer = _setup("dsv3_mxfp8_skew")
+    layer.forward()
+    shape = layer.shape
+    counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(w.E + 1, dtype=torch.int32, device="cuda")
+    sched = torch.empty((w.T, 2), dtype=torch.int32, device="cuda")
+    inv = torch.empty((w.N, w.k), dtype=torch.int32, device="cuda")
+    M.moe_layout(layer.idx, shape, counts, offsets, sched, inv, layer.ws)
+    from token_dispatch_expert_top_gb300.layer import quantize_mxfp8
+    xq, xs = quantize_mxfp8(layer.x)
+    rows = (sched[:, 0].long() * w.rows_per_shard + sched[:, 1].long())
+    a, a_s = xq[rows].contiguous(), xs[rows].contiguous()
+    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    M.moe_expert_ffn(a, a_s, offsets, layer.wgu, layer.wgu_sf, layer.wd, layer.wd_sf, shape, y, layer.ws)
+    assert M.moe_last_device_status(layer.ws) == 0
+    cnt = to_np(counts)
+    e = int(cnt.argmax())
+    off = to_np(offsets)
+    pick = np.sort(np.random.default_rng(1).choice(np.arange(off[e], off[e + 1]), 512, replace=False))
+    tok = to_np(rows)[pick]
+    a64 = O.mxfp8_values(O._f64(inp["x"][torch.from_numpy(tok).cuda()]))
+    wg, wu, wd = _oracle_weights(inp, w.dtype)(e)
+    ref = O.expert_ffn(a64, wg, wu, wd, w.dtype)
+    err = row_rel_err(to_np(y)[pick], ref)
+    assert err.max() < TOL[w.dtype], (e, cnt[e], err.max())
+
+
+@pytest.mark.parametrize("ring", [64, 256, 1024])
+def test_fullsize_skew_ring_sweep_bitwise(ring):
+    from token_dispatch_expert_top_gb300 import moe as M
+    need_cuda()
+    p = M.Params(ring, ring // 2, 0, 0, 0, 0)
+    w, inp, layer = _setup("dsv3_mxfp8_skew", params=p)
+    staged = layer.forward().clone()
+    fused = layer.forward(fused=True)
+    assert layer.device_status() == 0
+    assert torch.equal(fused, staged)

@@ -72,6 +72,9 @@ WORKLOADS = {
     # 32 experts, so a capture holds ~1.4 GB of weights instead of 11.6 GB.
     "dsv3_mxfp8_e32": Workload("dsv3_mxfp8_e32", N=1024, H=7168, I=2048, E=32, k=8, S=8,
                                dtype="mxfp8"),
+    # The forward half of the 16384-token skewed layer (N=16384, 128 shards of 128).
+    "dsv3_mxfp8_skew_16k": Workload("dsv3_mxfp8_skew_16k", N=16384, H=7168, I=2048, E=256, k=8,
+                                    S=128, dtype="mxfp8", skew=3.0),
     # Profiling stand-in for the router pass: DeepSeek-V3 router shape (N=8192,
     # H=7168, E=256, top-8) with small experts (I=128), ~3 GB on the device.
     "dsv3_router_prof": Workload("dsv3_router_prof", N=8192, H=7168, I=128, E=256, k=8, S=64,
@@ -79,7 +82,8 @@ WORKLOADS = {
 }
 
 # Workloads whose tensors are drawn on the device generator (too large for the host).
-DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_e32", "dsv3_router_prof"}
+DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_e32", "dsv3_router_prof",
+                "dsv3_mxfp8_skew_16k"}
 
 
 def master_dtype(w: Workload) -> torch.dtype:
