@@ -37,6 +37,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_PER_BF16 = 2.0      # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The figure of the slowest rank: all_reduce(MAX) over the process group (any
+    backend), the value itself on one rank."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank_step: float, steps: int, t_ms: float, world: int) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (t_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -214,12 +229,9 @@ def gpu_arm(args, rank, world):
     status = layer.device_status()
     if status != 0:
         raise RuntimeError(f"device status {M.status_name(status)} in timed region")
-    if world > 1:
-        t = torch.tensor([t_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_ms = float(t.item())
+    t_ms = max_over_ranks(t_ms, world, dev)
     ms_per_step = t_ms / args.steps
-    tokens_per_s = world * w.N * args.steps / (t_ms / 1e3)
+    tokens_per_s = job_rate(w.N, args.steps, t_ms, world)
 
     # ---- stage breakdown through the individual entry points (same kernels)
     st = StagedStep(layer)
@@ -254,11 +266,8 @@ def gpu_arm(args, rank, world):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * w.N * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e = {"value": job_rate(w.N, args.steps, e2e_ms, world), "unit": "tokens/s",
            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
            "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 

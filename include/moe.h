@@ -31,6 +31,8 @@
  *     status word at the start of the workspace (first error wins) and read with
  *     moe_last_device_status().  Kernels that detect one skip the offending work
  *     and return; they never trap.
+ *   - The workspace must be 32-byte aligned (MOE_ERR_WORKSPACE otherwise); the
+ *     library carves 256-byte-aligned regions out of it.
  *   - Row-major layouts throughout.  Expert weights are quantised (MXFP8) and
  *     repacked into GEMM tile images once, by moe_quantize_mxfp8 and
  *     moe_pack_expert_weights, before any forward call.
@@ -184,8 +186,15 @@ int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, in
  *   shard_scales : DEVICE array of S device pointers to [N/S][H/32] scales
  *                  (MXFP8 only; NULL otherwise)
  *   sched        : [T][2] from moe_layout
- *   ring, ring_scales : [ring_slots][row] destination (ring_scales MXFP8 only)
- * 16-byte vector loads and stores, one warp per slot row. */
+ *   ring, ring_scales : [ring_slots][row] destination (ring_scales MXFP8 only),
+ *                  16-byte aligned
+ * Shard row bases must be 16-byte aligned: a schedule entry whose source row is
+ * not (or lies outside its shard) is skipped and recorded as
+ * MOE_ERR_DEVICE_CHECK.  When both the row and its scale row are multiples of 16
+ * bytes, rows move through the bulk-copy engine (per warp, one lane streams its
+ * slots through a ring of shared-memory row buffers: bulk load, then bulk store;
+ * source rows are kept in L2, ring rows streamed out); otherwise one warp per
+ * slot row copies with 16- or 4-byte vector loads and stores. */
 int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
                       const moe_shape_t* shape, const int32_t* sched, int slot_begin,
                       int slot_count, void* ring, void* ring_scales, int ring_slots,
@@ -203,7 +212,7 @@ int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_sc
  *   w_gate_up, w_gu_scales, w_down, w_d_scales : the expert weights in the
  *                 tile-packed layout written by moe_pack_expert_weights (W_gate /
  *                 W_up / W_down; scales NULL unless MXFP8)
- *   y           : [T][H] FP32 (MOE_F32) or BF16                        (out)
+ *   y           : [T][H] FP32 (MOE_F32) or BF16, 32-byte aligned       (out)
  * BF16 / MXFP8 run on tcgen05 tensor cores (128x256 tiles, A by TMA, B by bulk
  * copies of packed tiles, accumulators in tensor memory) and need H % 256 == 0 and
  * I % 128 == 0; MOE_F32 runs a SIMT kernel. */

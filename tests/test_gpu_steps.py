@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_common import TIE_TAU, TOL, need_cuda, row_rel_err, to_np
+from gpu_common import TIE_TAU, TOL, check_routing, need_cuda, row_rel_err, to_np
 from token_dispatch_expert_top_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -88,9 +88,7 @@ def test_route_topk(M, w):
     ref = O.router_logits(inp["x"], inp["w_router"], inp["bias"])
     assert np.abs(g_logits - ref).max() < 1e-4 * max(1.0, np.abs(ref).max())
     r_idx, _ = O.route_topk(ref, w.k)
-    ok = O.topk_gap(ref, w.k) >= TIE_TAU
-    assert ok.mean() > 0.98
-    np.testing.assert_array_equal(g_idx[ok], r_idx[ok])
+    assert check_routing(g_idx, r_idx, ref, O.topk_gap(ref, w.k)) > 0.98
 
 
 @pytest.mark.parametrize("N,H,E,k", [(640, 512, 256, 8), (200, 1024, 32, 4), (8192, 7168, 256, 8)])
@@ -165,10 +163,12 @@ def test_layout_reports_out_of_range_expert(M):
 
 
 # ------------------------------------------------------------------------ dispatch
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "mxfp8"])
-def test_dispatch_pull_rows_by_schedule(M, dtype):
+# Rows of 16-byte multiples go through the bulk-copy kernel; MXFP8 at H=256 has
+# 8-byte scale rows and takes the vector-load kernel.
+@pytest.mark.parametrize("dtype,H", [("f32", 128), ("bf16", 1024), ("mxfp8", 1024), ("mxfp8", 256)])
+def test_dispatch_pull_rows_by_schedule(M, dtype, H):
     rng = np.random.default_rng(3)
-    N, H, E, k, S = 512, 1024 if dtype != "f32" else 128, 16, 4, 8,
+    N, E, k, S = 512, 16, 4, 8
     w = synth.Workload("pull", N=N, H=H, I=128, E=E, k=k, S=S, dtype=dtype)
     shape = M.Shape.of(w)
     ws = _ws(M, shape)

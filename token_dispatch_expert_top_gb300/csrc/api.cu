@@ -139,7 +139,7 @@ int check_shape(const moe_shape_t* s) {
 }
 
 int check_ws(const moe_shape_t* s, const moe_params_t* p, void* ws, size_t bytes) {
-    if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    if (!ws || ((uintptr_t)ws & 31)) return MOE_ERR_WORKSPACE;
     if (bytes < make_plan(*s, p).total) return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
@@ -342,7 +342,8 @@ int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_sc
     return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, slot_begin, slot_count,
                                             s.S, s.N / s.S, row_bytes, scale_bytes, ring,
                                             ring_scales, ring_slots, num_sms_current(),
-                                            at<WsHeader>(workspace, 0), (cudaStream_t)stream));
+                                            at<WsHeader>(workspace, 0), kDefaultTimeoutNs,
+                                            (cudaStream_t)stream));
 }
 
 int moe_expert_ffn(const void* a, const void* a_scales, const int32_t* offsets,
@@ -358,7 +359,7 @@ int moe_expert_ffn(const void* a, const void* a_scales, const int32_t* offsets,
     const bool mx = s.dtype == MOE_MXFP8;
     if (!a || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
     if (mx && (!a_scales || !w_gu_scales || !w_d_scales)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
+    if (!aligned16(a) || !aligned16(w_gate_up) || !aligned16(w_down) || ((uintptr_t)y & 31))
         return MOE_ERR_INVALID_ARG;
     if (mx && (((uintptr_t)a_scales & 3) || ((uintptr_t)w_gu_scales & 3) || ((uintptr_t)w_d_scales & 3)))
         return MOE_ERR_INVALID_ARG;
@@ -432,7 +433,8 @@ int moe_forward(const void* x, const void* w_router, const float* bias, const vo
     void* ring_sf = mx ? at<void>(ws, pl.ring_sf) : nullptr;
     rc = cuda_status(launch_dispatch_pull((const void* const*)tab, (const void* const*)tab_sf, sched,
                                           0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
-                                          ring_sf, pl.ring_slots, num_sms_current(), hdr, st));
+                                          ring_sf, pl.ring_slots, num_sms_current(), hdr,
+                                          timeout_of(params), st));
     if (rc) return rc;
     // 4. grouped SwiGLU expert FFN
     void* y = at<void>(ws, pl.y);

@@ -116,6 +116,7 @@ struct FusedArgs {
     int G;                    // gather CTAs (blockIdx.x < G)
     int row_bytes, sf_bytes;  // gathered row and its scales
     int skip_ready;           // test hook: minibatch whose gather_done is never bumped (-1: none)
+    int plan_smem;            // compute CTAs keep tbase / pbase / elo in shared memory
     WsHeader* ws;
     unsigned long long timeout_ns;
 };
@@ -198,27 +199,35 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
 struct MinibatchTiles {
     const FusedArgs* a;
     const int32_t* off;       // offsets in shared memory
+    const int32_t *tb, *pb, *el;   // the plan's tbase / pbase / elo (shared memory when they fit)
     int nt1, nt2, c0, C;      // N tiles of GEMM1 / GEMM2, this CTA's index among C
     __device__ int first() const { return c0; }
     __device__ int next(int t) const { return t + C; }
-    __device__ int count() const { return a->plan.tbase[2 * a->nmb]; }
+    __device__ int count() const { return tb[2 * a->nmb]; }
+    __device__ int kind_of(int t) const {
+        int lo = 0, hi = 2 * a->nmb;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tb[mid] <= t) lo = mid; else hi = mid;
+        }
+        return segment_of(lo, a->nmb, a->NR >= 2).kind;
+    }
     __device__ TileInfo tile(int t) const {
-        const FusedPlan& pl = a->plan;
         int lo = 0, hi = 2 * a->nmb;   // last segment j with tbase[j] <= t
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (pl.tbase[mid] <= t) lo = mid; else hi = mid;
+            if (tb[mid] <= t) lo = mid; else hi = mid;
         }
         const Segment sg = segment_of(lo, a->nmb, a->NR >= 2);
         const int b = sg.b;
-        const int P = pl.pbase[b + 1] - pl.pbase[b];
-        const int local = t - pl.tbase[lo];
+        const int P = pb[b + 1] - pb[b];
+        const int local = t - tb[lo];
         TileInfo tl;
         tl.kind = sg.kind;
         tl.n = local / P;
         const int mi = local % P;
         const int s_lo = b * a->MB, s_hi = min(s_lo + a->MB, a->T);
-        int e = pl.elo[b], m = mi;
+        int e = el[b], m = mi;
         for (; e < a->E; ++e) {
             const int len = min(off[e + 1], s_hi) - max(off[e], s_lo);
             const int mt = len > 0 ? (len + tc::BM - 1) / tc::BM : 0;
@@ -240,7 +249,7 @@ struct MinibatchTiles {
         tl.out_row0 = tl.kind == 0 ? ring_row : piece0;
         tl.nrows = min(piece_end - piece0, tc::BM);
         tl.mb = b;
-        tl.midx = pl.pbase[b] + mi;
+        tl.midx = pb[b] + mi;
         return tl;
     }
     __device__ bool wait_inputs(const TileInfo& tl, const Pipe& p) const {
@@ -334,43 +343,75 @@ __device__ void gather_role(const FusedArgs& a, unsigned long long deadline, int
 }
 
 // Combine role (every CTA, after all GEMM2 tiles): out[n] = sum_j g[n][j] y[inv[n][j]]
-// in FP32, fixed j order, one warp per (token, 256-column chunk).
+// in FP32, fixed j order, one warp per (token, 256-column chunk).  Only one CTA of
+// 12 warps fits on an SM here, so each warp takes two items at a time and issues
+// the loads of up to eight slot rows of both before it accumulates (same order
+// of additions as the stand-alone combine kernel).
 __device__ void combine_role(const FusedArgs& a) {
+    constexpr int IW = 2, JB = 8;
     const int lane = threadIdx.x & 31;
     const int chunks = (a.H + 255) / 256;
     const int64_t items = (int64_t)a.N * chunks;
     const int64_t gw = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t it = gw; it < items; it += nw) {
-        const int n = (int)(it / chunks);
-        const int col = (int)(it % chunks) * 256 + lane * 8;
-        const int my_slot = lane < a.k ? a.inv[(int64_t)n * a.k + lane] : 0;
-        const float my_g = lane < a.k ? a.gate[(int64_t)n * a.k + lane] : 0.f;
-        float acc[8];
+    for (int64_t it0 = gw * IW; it0 < items; it0 += nw * IW) {
+        int n[IW], col[IW], my_slot[IW];
+        float my_g[IW], acc[IW][8];
+        bool live[IW];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) acc[v] = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-            const float g = __shfl_sync(0xffffffffu, my_g, j);
-            if (slot < 0 || slot >= a.T) {
-                if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
-                continue;
+        for (int i = 0; i < IW; ++i) {
+            const int64_t it = it0 + i;
+            live[i] = it < items;
+            n[i] = live[i] ? (int)(it / chunks) : 0;
+            col[i] = live[i] ? (int)(it % chunks) * 256 + lane * 8 : a.H;
+            my_slot[i] = (live[i] && lane < a.k) ? a.inv[(int64_t)n[i] * a.k + lane] : 0;
+            my_g[i] = (live[i] && lane < a.k) ? a.gate[(int64_t)n[i] * a.k + lane] : 0.f;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) acc[i][v] = 0.f;
+        }
+        for (int j0 = 0; j0 < a.k; j0 += JB) {
+            uint4 q[IW][JB];
+            float g[IW][JB];
+            uint32_t use[IW] = {0u, 0u};
+#pragma unroll
+            for (int u = 0; u < JB; ++u) {
+                const int j = j0 + u;
+#pragma unroll
+                for (int i = 0; i < IW; ++i) {
+                    const int slot = __shfl_sync(0xffffffffu, my_slot[i], j & 31);
+                    g[i][u] = __shfl_sync(0xffffffffu, my_g[i], j & 31);
+                    if (!live[i] || j >= a.k) continue;
+                    if (slot < 0 || slot >= a.T) {
+                        if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
+                        continue;
+                    }
+                    if (col[i] < a.H) {
+                        // y was stored by other CTAs of this launch: read it through L2
+                        q[i][u] = ld_cg_v4(a.y + ((int64_t)slot * a.H + col[i]) * 2);
+                        use[i] |= 1u << u;
+                    }
+                }
             }
-            if (col < a.H) {
-                // y was stored by other CTAs of this launch: read it through L2
-                const uint4 q = ld_cg_v4(a.y + ((int64_t)slot * a.H + col) * 2);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    acc[2 * p] = fmaf(g, bf16_to_f32((uint16_t)(w[p] & 0xFFFF)), acc[2 * p]);
-                    acc[2 * p + 1] = fmaf(g, bf16_to_f32((uint16_t)(w[p] >> 16)), acc[2 * p + 1]);
+            for (int u = 0; u < JB; ++u) {
+#pragma unroll
+                for (int i = 0; i < IW; ++i) {
+                    if (!(use[i] & (1u << u))) continue;
+                    const uint32_t w[4] = {q[i][u].x, q[i][u].y, q[i][u].z, q[i][u].w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        acc[i][2 * p] = fmaf(g[i][u], bf16_to_f32((uint16_t)(w[p] & 0xFFFF)), acc[i][2 * p]);
+                        acc[i][2 * p + 1] = fmaf(g[i][u], bf16_to_f32((uint16_t)(w[p] >> 16)), acc[i][2 * p + 1]);
+                    }
                 }
             }
         }
-        if (col < a.H)
-            st_v4(a.out + ((int64_t)n * a.H + col) * 2,
-                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+#pragma unroll
+        for (int i = 0; i < IW; ++i)
+            if (live[i] && col[i] < a.H)
+                st_v4(a.out + ((int64_t)n[i] * a.H + col[i]) * 2,
+                      make_uint4(pack_bf16x2(acc[i][0], acc[i][1]), pack_bf16x2(acc[i][2], acc[i][3]),
+                                 pack_bf16x2(acc[i][4], acc[i][5]), pack_bf16x2(acc[i][6], acc[i][7])));
     }
 }
 
@@ -388,10 +429,25 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     if ((int)blockIdx.x < a.G) {
         gather_role(a, deadline, s2.n_tiles);
     } else {
+        // the tile decode runs at every tile boundary in four roles: keep what it
+        // reads in shared memory (the plan was written by the previous launch)
         int32_t* off = reinterpret_cast<int32_t*>(smem + tc::OFF_TAIL);
         for (int e = threadIdx.x; e <= a.E; e += blockDim.x) off[e] = a.offsets[e];
+        const int32_t *tb = pl.tbase, *pb = pl.pbase, *el = pl.elo;
+        if (a.plan_smem) {
+            int32_t* stb = off + (a.E + 1);
+            int32_t* spb = stb + (2 * a.nmb + 1);
+            int32_t* sel = spb + (a.nmb + 1);
+            for (int i = threadIdx.x; i <= 2 * a.nmb; i += blockDim.x) stb[i] = pl.tbase[i];
+            for (int i = threadIdx.x; i <= a.nmb; i += blockDim.x) spb[i] = pl.pbase[i];
+            for (int i = threadIdx.x; i < a.nmb; i += blockDim.x) sel[i] = pl.elo[i];
+            tb = stb;
+            pb = spb;
+            el = sel;
+        }
         __syncthreads();
-        MinibatchTiles src{&a, off, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G, (int)gridDim.x - a.G};
+        MinibatchTiles src{&a, off, tb, pb, el, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G,
+                           (int)gridDim.x - a.G};
         GemmMaps maps;
         maps.a[0] = &tmA1;
         maps.a[1] = &tmA2;
@@ -466,7 +522,10 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     a.ws = c.ffn.ws;
     a.timeout_ns = c.ffn.timeout_ns;
 
-    const size_t smem = 1024 + tc::OFF_TAIL + sizeof(int32_t) * (c.E + 1);
+    size_t smem = 1024 + tc::OFF_TAIL + sizeof(int32_t) * (c.E + 1);
+    const size_t plan_bytes = sizeof(int32_t) * ((size_t)4 * c.nmb + 2);
+    a.plan_smem = smem + plan_bytes <= (size_t)227 * 1024 ? 1 : 0;
+    if (a.plan_smem) smem += plan_bytes;
     void* kern = c.ffn.mx ? (void*)fused_forward_kernel<true> : (void*)fused_forward_kernel<false>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -11,27 +11,30 @@ namespace moe {
 constexpr int kGatherWarps = 8;
 
 // Copy a row of n16 16-byte units (plus an optional second row of m16 units, the
-// scales) with every load of a batch issued before any store: up to 16 + 1
-// 16-byte loads in flight per lane.
+// scales) with every load of a batch issued before any store: up to 8 + 1
+// 16-byte loads in flight per lane (a shallow batch keeps registers low, so many
+// warps per SM keep enough bytes in flight).  Sources are read k times over the
+// dispatch, so their lines are kept in L2; ring rows are streamed out.
 __device__ __forceinline__ void copy_rows_v4(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                                              int n16, uint8_t* __restrict__ dst2,
                                              const uint8_t* __restrict__ src2, int m16, int lane) {
-    constexpr int U = 16;
+    constexpr int U = 8;
+    const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
     for (int b = 0; b < n16 || b < m16; b += 32 * U) {
         uint4 v[U], w;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = b + lane + 32 * u;
-            if (j < n16) v[u] = ld_nc_v4(src + 16 * (int64_t)j);
+            if (j < n16) v[u] = ld_nc_v4_hint(src + 16 * (int64_t)j, keep);
         }
         const int j2 = b + lane;
-        if (j2 < m16) w = ld_nc_v4(src2 + 16 * (int64_t)j2);
+        if (j2 < m16) w = ld_nc_v4_hint(src2 + 16 * (int64_t)j2, keep);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = b + lane + 32 * u;
-            if (j < n16) st_v4(dst + 16 * (int64_t)j, v[u]);
+            if (j < n16) st_v4_hint(dst + 16 * (int64_t)j, v[u], stream);
         }
-        if (j2 < m16) st_v4(dst2 + 16 * (int64_t)j2, w);
+        if (j2 < m16) st_v4_hint(dst2 + 16 * (int64_t)j2, w, stream);
     }
 }
 
@@ -42,7 +45,7 @@ __device__ __forceinline__ void copy_u32(uint8_t* dst, const uint8_t* src, int n
 }
 
 // One warp per slot, grid-stride.  Slot t goes to ring row t % ring_slots.
-__global__ void __launch_bounds__(kGatherWarps * 32) dispatch_pull_kernel(
+__global__ void __launch_bounds__(kGatherWarps * 32, 2) dispatch_pull_kernel(
     const uint8_t* const* __restrict__ shard_rows, const uint8_t* const* __restrict__ shard_scales,
     const int32_t* __restrict__ sched, int slot_begin, int slot_count, int S, int rows_per_shard,
     int row_bytes, int scale_bytes, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales,
@@ -75,12 +78,151 @@ __global__ void __launch_bounds__(kGatherWarps * 32) dispatch_pull_kernel(
     }
 }
 
+// ----------------------------------------------------------- bulk-copy variant
+// Rows whose code and scale lengths are multiples of 16 bytes move through the
+// bulk-copy engine: in each warp one lane streams its slots through a ring of
+// row buffers in shared memory -- a bulk load (source row kept in L2: it is read
+// k times over the dispatch) then a bulk store of the same buffer (ring rows
+// streamed out) -- so a few threads per SM keep ~100 KB+ in flight without
+// holding the data in registers.  A buffer is refilled once the bulk store that
+// read it is LAG stores old and has finished reading (bulk-group accounting).
+constexpr int kBulkWarps = 4;
+constexpr int kBulkLag = 2;
+constexpr int kBulkMaxBuf = 16;
+
+__global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
+    const uint8_t* const* __restrict__ shard_rows, const uint8_t* const* __restrict__ shard_scales,
+    const int32_t* __restrict__ sched, int slot_begin, int slot_count, int S, int rows_per_shard,
+    int row_bytes, int scale_bytes, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales,
+    int ring_slots, int nbuf, WsHeader* ws, unsigned long long timeout_ns) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort[kBulkWarps];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int unit = row_bytes + scale_bytes;
+    uint8_t* buf = smem + (size_t)warp * nbuf * unit;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkWarps * nbuf * unit) + warp * kBulkMaxBuf;
+    if (lane == 0) {
+        for (int b = 0; b < nbuf; ++b) mbar_init(&bars[b], 1);
+        s_abort[warp] = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // This warp's slots: chunks of 32 consecutive slots, chunk c = gw + i * nw.
+    const int gw = blockIdx.x * kBulkWarps + warp, nw = gridDim.x * kBulkWarps;
+    const int nchunks = (slot_count + 31) / 32;
+    if (gw >= nchunks) return;
+    const int my_chunks = (nchunks - gw + nw - 1) / nw;
+    const int last = gw + (my_chunks - 1) * nw;
+    const int total = (my_chunks - 1) * 32 + min(32, slot_count - last * 32);
+    auto slot_of = [&](int q) { return (gw + (q >> 5) * nw) * 32 + (q & 31); };
+
+    const unsigned long long deadline = globaltimer_ns() + timeout_ns;
+    const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+    volatile int* abort_flag = &s_abort[warp];
+    uint32_t bad = 0;          // bit b: buffer b holds a slot whose schedule entry is invalid
+    int chunk_sched_q = -1;    // first q of the chunk whose schedule entries the lanes hold
+    int my_s = 0, my_r = 0;
+
+    // Issue the bulk load of the q-th slot into buffer q % nbuf (all lanes call;
+    // lane 0 issues).
+    auto load = [&](int q) {
+        const int c0 = q & ~31;
+        if (c0 != chunk_sched_q) {
+            chunk_sched_q = c0;
+            const int i = slot_of(c0) + lane;
+            if (i < slot_count) {
+                const int t = slot_begin + i;
+                my_s = sched[2 * (int64_t)t];
+                my_r = sched[2 * (int64_t)t + 1];
+            }
+        }
+        const int sidx = __shfl_sync(0xffffffffu, my_s, q & 31);
+        const int ridx = __shfl_sync(0xffffffffu, my_r, q & 31);
+        if (lane == 0) {
+            const int b = q % nbuf;
+            uint8_t* dst = buf + (size_t)b * unit;
+            bool ok = sidx >= 0 && sidx < S && ridx >= 0 && ridx < rows_per_shard;
+            const uint8_t* src = ok ? shard_rows[sidx] + (int64_t)ridx * row_bytes : nullptr;
+            const uint8_t* ssrc = (ok && scale_bytes) ? shard_scales[sidx] + (int64_t)ridx * scale_bytes : nullptr;
+            if (ok && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(ssrc)) & 15)) ok = false;
+            if (ok) {
+                bad &= ~(1u << b);
+                mbar_arrive_expect_tx(&bars[b], (uint32_t)unit);
+                bulk_load_hint(dst, src, (uint32_t)row_bytes, &bars[b], keep);
+                if (scale_bytes) bulk_load_hint(dst + row_bytes, ssrc, (uint32_t)scale_bytes, &bars[b], keep);
+            } else {
+                set_status(ws, MOE_ERR_DEVICE_CHECK);
+                bad |= 1u << b;
+                mbar_arrive(&bars[b]);
+            }
+        }
+    };
+
+    const int pre = min(nbuf, total);
+    for (int q = 0; q < pre; ++q) load(q);
+    int q = 0;
+    for (; q < total; ++q) {
+        if (lane == 0) {
+            const int b = q % nbuf;
+            if (!mbar_wait_bounded(&bars[b], (uint32_t)((q / nbuf) & 1), abort_flag, ws, deadline)) {
+                // give up: nothing more is issued; drain what is in flight below
+            } else if (!(bad & (1u << b))) {
+                fence_proxy_async_smem();
+                const int64_t dr = (slot_begin + slot_of(q)) % ring_slots;
+                const uint8_t* src = buf + (size_t)b * unit;
+                bulk_store_hint(ring + dr * row_bytes, src, (uint32_t)row_bytes, stream);
+                if (scale_bytes)
+                    bulk_store_hint(ring_scales + dr * scale_bytes, src + row_bytes, (uint32_t)scale_bytes, stream);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<kBulkLag>();
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const int qn = q - kBulkLag + nbuf;     // refill the buffer whose store is now LAG old
+        if (q >= kBulkLag && qn < total) load(qn);
+    }
+    if (lane == 0) {
+        if (*abort_flag) {
+            // let loads already issued land before the block's shared memory goes away
+            const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+            while (globaltimer_ns() < d2) {
+            }
+        }
+        bulk_wait_group_all();
+    }
+}
+
 cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
                                  const int32_t* sched, int slot_begin, int slot_count, int S,
                                  int rows_per_shard, int row_bytes, int scale_bytes, void* ring,
                                  void* ring_scales, int ring_slots, int num_sms, WsHeader* ws,
-                                 cudaStream_t stream) {
+                                 unsigned long long timeout_ns, cudaStream_t stream) {
     if (slot_count <= 0) return cudaSuccess;
+    const int unit = row_bytes + scale_bytes;
+    const int kSmemBudget = 200 * 1024;
+    const int bars_bytes = kBulkWarps * kBulkMaxBuf * 8;
+    int nbuf = unit > 0 ? (kSmemBudget - bars_bytes) / (kBulkWarps * unit) : 0;
+    if (nbuf > kBulkMaxBuf) nbuf = kBulkMaxBuf;
+    const bool bulk = row_bytes % 16 == 0 && scale_bytes % 16 == 0 && nbuf >= kBulkLag + 2 &&
+                      (reinterpret_cast<uintptr_t>(ring) & 15) == 0 &&
+                      (scale_bytes == 0 || (reinterpret_cast<uintptr_t>(ring_scales) & 15) == 0);
+    if (bulk) {
+        const size_t smem = (size_t)kBulkWarps * nbuf * unit + bars_bytes;
+        cudaError_t e = cudaFuncSetAttribute(dispatch_bulk_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int per_sm = (int)((227 * 1024) / (smem + 1024));
+        if (per_sm < 1) per_sm = 1;
+        const int nchunks = (slot_count + 31) / 32;
+        int blocks = (nchunks + kBulkWarps - 1) / kBulkWarps;
+        if (blocks > num_sms * per_sm) blocks = num_sms * per_sm;
+        dispatch_bulk_kernel<<<blocks, kBulkWarps * 32, smem, stream>>>(
+            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, slot_begin,
+            slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring, (uint8_t*)ring_scales,
+            ring_slots, nbuf, ws, timeout_ns);
+        return cudaGetLastError();
+    }
     int blocks = (slot_count + kGatherWarps - 1) / kGatherWarps;
     if (blocks > num_sms * 8) blocks = num_sms * 8;
     dispatch_pull_kernel<<<blocks, kGatherWarps * 32, 0, stream>>>(

@@ -19,7 +19,8 @@
 //               half the columns, drain the FP32 accumulator into registers,
 //               release it, then apply SwiGLU (+ MXFP8 quantisation of h along I)
 //               or BF16 conversion and store.
-// A tile is GEMM1 (+SwiGLU; kind 0) or GEMM2 (kind 1).  The source decides the
+// A tile is GEMM1 (+SwiGLU; kind 0) or GEMM2 (kind 1).  The source (first / next
+// / count / kind_of / tile / wait_inputs / tile_stored) decides the
 // order, where each tile's A rows come from, where its output goes, and what a
 // tile waits for before its A operand (or its A scales) may be loaded -- nothing
 // for the stand-alone kernels; the gather or GEMM1 counters in the fused kernel,
@@ -189,8 +190,7 @@ __device__ void mma_role(const Pipe& p, const GemmSide* sides, Src& src) {
     const uint32_t d_tmem = p.tmem_base;
     bool ok = true;
     for (int t = src.first(); ok && t < src.count(); t = src.next(t)) {
-        const TileInfo tl = src.tile(t);
-        const int KB = sides[tl.kind].K / (MX ? 128 : 64);
+        const int KB = sides[src.kind_of(t)].K / (MX ? 128 : 64);   // the issuer needs only the tile's K
         if (!mbar_wait_bounded(p.tempty, acc_phase ^ 1, p.abort_flag, p.ws, p.deadline)) break;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
@@ -329,70 +329,63 @@ __device__ void epilogue_role(const Pipe& p, const GemmSide* sides, Src& src) {
         const int64_t row = tl.out_row0 + r;
         const uint32_t tq = p.tmem_base + ((uint32_t)(32 * q) << 16);
         if (tl.kind == 0) {
-            // GEMM1: h = silu(gate) * up over this warp's 64 of the 128 h columns
-            uint32_t pk[2][16];
-            uint8_t sc[2];
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int c = half * 2 + c2;
-                uint32_t g[32], u[32];
-                tmem_ld_32x32b_x32(tq + 32 * c, g);
-                tmem_ld_32x32b_x32(tq + 128 + 32 * c, u);
-                tmem_ld_wait();
-                float hv[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) hv[i] = silu_f32(__uint_as_float(g[i])) * __uint_as_float(u[i]);
-                if constexpr (MX) {
-                    sc[c2] = mx_quantize32(hv, pk[c2]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[c2][i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-                }
-            }
+            // GEMM1: h = silu(gate) * up over this warp's 64 of the 128 h columns.
+            // All four accumulator chunks are read with one wait and the
+            // accumulator is released before any arithmetic.
+            uint32_t g0[32], u0[32], g1[32], u1[32];
+            tmem_ld_32x32b_x32(tq + 32 * (half * 2), g0);
+            tmem_ld_32x32b_x32(tq + 128 + 32 * (half * 2), u0);
+            tmem_ld_32x32b_x32(tq + 32 * (half * 2 + 1), g1);
+            tmem_ld_32x32b_x32(tq + 128 + 32 * (half * 2 + 1), u1);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p.tempty);
-            if (valid) {
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int col = tl.n * 128 + 32 * (half * 2 + c2);
-                    if constexpr (MX) {
-                        uint8_t* dst = sd.out + row * sd.out_ld + col;
-                        st_v4(dst, make_uint4(pk[c2][0], pk[c2][1], pk[c2][2], pk[c2][3]));
-                        st_v4(dst + 16, make_uint4(pk[c2][4], pk[c2][5], pk[c2][6], pk[c2][7]));
-                        sd.out_sf[row * (sd.out_ld / 32) + col / 32] = sc[c2];
-                    } else {
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const uint32_t* g = c2 ? g1 : g0;
+                const uint32_t* u = c2 ? u1 : u0;
+                float hv[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) hv[i] = silu_f32(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+                const int col = tl.n * 128 + 32 * (half * 2 + c2);
+                uint32_t pk[16];
+                if constexpr (MX) {
+                    const uint8_t sc = mx_quantize32(hv, pk);
+                    if (valid) {
+                        st_v8(sd.out + row * sd.out_ld + col, pk);
+                        sd.out_sf[row * (sd.out_ld / 32) + col / 32] = sc;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+                    if (valid) {
                         uint8_t* dst = sd.out + (row * sd.out_ld + col) * 2;
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp)
-                            st_v4(dst + 16 * pp, make_uint4(pk[c2][4 * pp], pk[c2][4 * pp + 1],
-                                                            pk[c2][4 * pp + 2], pk[c2][4 * pp + 3]));
+                        st_v8(dst, pk);
+                        st_v8(dst + 32, pk + 8);
                     }
                 }
             }
         } else {
-            // GEMM2: y tile in BF16, this warp's 128 of the 256 columns
-            uint32_t pk[4][16];
+            // GEMM2: y tile in BF16, this warp's 128 of the 256 columns (one wait,
+            // release, then convert and store)
+            uint32_t v[4][32];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[c4][i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            }
+            for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v[c4]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p.tempty);
-            if (valid) {
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(v[c4][2 * i]), __uint_as_float(v[c4][2 * i + 1]));
+                if (valid) {
                     uint8_t* dst = sd.out + (row * sd.out_ld + tl.n * BN + 32 * (half * 4 + c4)) * 2;
-#pragma unroll
-                    for (int pp = 0; pp < 4; ++pp)
-                        st_v4(dst + 16 * pp, make_uint4(pk[c4][4 * pp], pk[c4][4 * pp + 1],
-                                                        pk[c4][4 * pp + 2], pk[c4][4 * pp + 3]));
+                    st_v8(dst, pk);
+                    st_v8(dst + 32, pk + 8);
                 }
             }
         }

@@ -43,6 +43,7 @@ struct ExpertTiles {
     __device__ int first() const { return blockIdx.x; }
     __device__ int next(int t) const { return t + gridDim.x; }
     __device__ int count() const { return total; }
+    __device__ int kind_of(int) const { return kind; }
     __device__ TileInfo tile(int t) const {
         const int q = t / n_tiles;
         int lo = 0, hi = E;  // last e with mpre[e] <= q

@@ -32,7 +32,7 @@ cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* cons
                                  const int32_t* sched, int slot_begin, int slot_count, int S,
                                  int rows_per_shard, int row_bytes, int scale_bytes, void* ring,
                                  void* ring_scales, int ring_slots, int num_sms, WsHeader* ws,
-                                 cudaStream_t stream);
+                                 unsigned long long timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* gate, int N, int H,
                            int k, int T, int dtype, void* out, int num_sms, WsHeader* ws,
