@@ -192,11 +192,16 @@ def test_dispatch_pull_rows_by_schedule(M, dtype, H):
     assert M.moe_last_device_status(ws) == 0
     allrows = torch.cat(shards).cpu()
     allsf = torch.cat(sc).cpu()
+    got, got_sf = ring.cpu(), ring_sf.cpu()
+    written = set()
     for t in range(begin, begin + count):
         src = sched_np[t, 0] * rows + sched_np[t, 1]
-        assert torch.equal(ring[t % R].cpu(), allrows[src])
+        assert torch.equal(got[t % R], allrows[src])
         if mx:
-            assert torch.equal(ring_sf[t % R].cpu(), allsf[src])
+            assert torch.equal(got_sf[t % R], allsf[src])
+        written.add(t % R)
+    untouched = [r for r in range(R) if r not in written]
+    assert not got[untouched].any()                 # nothing outside the slot range
 
 
 # ------------------------------------------------------------------------- combine

@@ -37,7 +37,7 @@ size_t op_elem(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2
 struct FusedGeom {
     int G, C;       // gather CTAs, compute CTAs
     int MB, R;      // slots per minibatch, ring slots (a multiple of MB)
-    int nmb;        // minibatches
+    int nmb;        // bound on the minibatch count (every minibatch but the last holds >= MB/2 slots)
     int status;     // MOE_OK, or why these params cannot run
 };
 
@@ -65,7 +65,7 @@ FusedGeom resolve_fused(const moe_shape_t& s, const moe_params_t* p, int max_cta
     if (g.MB < 1) g.MB = 1;
     g.R = (p && p->ring_slots > 0) ? p->ring_slots : (4 * g.MB < Tp ? 4 * g.MB : ((Tp + g.MB - 1) / g.MB) * g.MB);
     if (g.R < g.MB || g.R % g.MB != 0) g.status = MOE_ERR_INVALID_ARG;
-    g.nmb = (T + g.MB - 1) / g.MB;
+    g.nmb = T > 0 ? 2 * ((T + g.MB - 1) / g.MB) + 1 : 0;
     return g;
 }
 

@@ -87,11 +87,14 @@ __host__ __device__ __forceinline__ Segment segment_of(int j, int nmb, bool inte
     return (j & 1) ? Segment{0, (j + 1) >> 1} : Segment{1, (j >> 1) - 1};
 }
 
-// Counters and plan arrays in the workspace (int32 unless noted).
+// Counters and plan arrays in the workspace (int32).  nmb is the number of
+// minibatches the plan kernel cut (at most the host's bound nmb_max).
 struct FusedPlan {
     int* tbase;        // [2*nmb+1] tile prefix over the segments of the schedule
     int* pbase;        // [nmb+1] m-tile prefix over minibatches (P_b each)
     int* elo;          // [nmb] first expert overlapping minibatch b
+    int* cut;          // [nmb+1] first slot of minibatch b; cut[nmb] = T
+    int* nmb;          // [1] minibatches
     int* gather_done;  // [nmb] gather CTAs done with minibatch b
     int* g1_done;      // [pbase[nmb]] epilogue-warp reports of GEMM1 tiles per m-tile
     int* g2_done;      // [nmb] epilogue-warp reports of GEMM2 tiles per minibatch
@@ -112,7 +115,7 @@ struct FusedArgs {
     uint8_t* y;               // [T][H] BF16
     uint8_t* out;             // [N][H] BF16
     int N, H, E, k, S, T;
-    int MB, NR, nmb;          // minibatch, ring buffers, minibatches
+    int MB, NR, nmb_max;      // minibatch capacity, ring buffers, bound on the minibatch count
     int G;                    // gather CTAs (blockIdx.x < G)
     int row_bytes, sf_bytes;  // gathered row and its scales
     int skip_ready;           // test hook: minibatch whose gather_done is never bumped (-1: none)
@@ -121,17 +124,54 @@ struct FusedArgs {
     unsigned long long timeout_ns;
 };
 
-// One block: per-minibatch m-tile counts, prefixes, first experts; zero counters.
+// End of the minibatch that starts at slot lo (slots in expert order, at most MB
+// of them).  It ends on an expert boundary when one falls in the second half of
+// the minibatch, else inside the expert that crosses lo + MB at a whole number of
+// 128-row m-tiles from that expert's start, so minibatch edges cut as few experts
+// (extra ragged m-tiles, a second pass over their weights) as possible.  Every
+// minibatch but the last holds at least max(1, MB/2) slots.
+__device__ int minibatch_cut(const int32_t* off, int E, int T, int MB, int lo) {
+    const int target = lo + MB;
+    if (target >= T) return T;
+    const int half = MB / 2 > 1 ? MB / 2 : 1;
+    int a = 0, z = E - 1;                 // expert e with off[e] < target <= off[e+1]
+    while (a < z) {
+        const int mid = (a + z) >> 1;
+        if (off[mid + 1] >= target) z = mid; else a = mid + 1;
+    }
+    if (off[a + 1] == target) return target;
+    if (off[a] - lo >= half) return off[a];
+    const int c2 = off[a] + ((target - off[a]) / tc::BM) * tc::BM;
+    if (c2 - lo >= half) return c2;
+    return target;
+}
+
+// One block: cuts the slots into minibatches, then per-minibatch m-tile counts,
+// prefixes and first experts; zeroes the counters.
 __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restrict__ offsets, int E,
-                                                          int T, int MB, int nmb, int nt1, int nt2,
+                                                          int T, int MB, int nmb_max, int nt1, int nt2,
                                                           int interleave, FusedPlan plan,
-                                                          int counters_len, int* counters) {
+                                                          int counters_len, int* counters, WsHeader* ws) {
     extern __shared__ int32_t off[];
+    __shared__ int s_nmb;
     for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = offsets[e];
     for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        int b = 0, lo = 0;
+        while (lo < T && b < nmb_max) {
+            plan.cut[b++] = lo;
+            lo = minibatch_cut(off, E, T, MB, lo);
+        }
+        if (lo < T) set_status(ws, MOE_ERR_DEVICE_CHECK);   // cannot happen: the bound holds
+        plan.cut[b] = T;
+        *plan.nmb = b;
+        s_nmb = b;
+    }
+    __syncthreads();
+    const int nmb = s_nmb;
     for (int b = threadIdx.x; b < nmb; b += blockDim.x) {
-        const int lo = b * MB, hi = min(lo + MB, T);
+        const int lo = plan.cut[b], hi = plan.cut[b + 1];
         int a = 0, z = E;  // first e with off[e+1] > lo
         while (a < z) {
             const int mid = (a + z) >> 1;
@@ -194,46 +234,53 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
 }
 
 // Tiles of the fused schedule: per minibatch, its GEMM1 tiles then its GEMM2
-// tiles, each ordered N tile major, m-tile minor (as in the staged kernel), so
-// compute CTAs working at the same time share weight tiles in L2.
+// tiles, each ordered expert-major, then N tile, then m-tile (as in the staged
+// kernel), so compute CTAs working at the same time share both the weight tile
+// (same expert and N tile) and the token rows (same expert and m-tile) in L2.
+// (With the N tile outermost, the reuses of an A tile are a whole wave apart and
+// the weight stream evicts it from L2 in between.)
 struct MinibatchTiles {
+    static constexpr bool kLookahead = true;    // poll the next tile's inputs ahead of time
     const FusedArgs* a;
     const int32_t* off;       // offsets in shared memory
-    const int32_t *tb, *pb, *el;   // the plan's tbase / pbase / elo (shared memory when they fit)
+    const int32_t *tb, *pb, *el, *ct;   // the plan's tbase / pbase / elo / cut (shared memory when they fit)
+    int nmb;                  // minibatches
     int nt1, nt2, c0, C;      // N tiles of GEMM1 / GEMM2, this CTA's index among C
     __device__ int first() const { return c0; }
     __device__ int next(int t) const { return t + C; }
-    __device__ int count() const { return tb[2 * a->nmb]; }
+    __device__ int count() const { return tb[2 * nmb]; }
     __device__ int kind_of(int t) const {
-        int lo = 0, hi = 2 * a->nmb;
+        int lo = 0, hi = 2 * nmb;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (tb[mid] <= t) lo = mid; else hi = mid;
         }
-        return segment_of(lo, a->nmb, a->NR >= 2).kind;
+        return segment_of(lo, nmb, a->NR >= 2).kind;
     }
     __device__ TileInfo tile(int t) const {
-        int lo = 0, hi = 2 * a->nmb;   // last segment j with tbase[j] <= t
+        int lo = 0, hi = 2 * nmb;   // last segment j with tbase[j] <= t
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (tb[mid] <= t) lo = mid; else hi = mid;
         }
-        const Segment sg = segment_of(lo, a->nmb, a->NR >= 2);
+        const Segment sg = segment_of(lo, nmb, a->NR >= 2);
         const int b = sg.b;
-        const int P = pb[b + 1] - pb[b];
-        const int local = t - tb[lo];
+        const int nt = sg.kind == 0 ? nt1 : nt2;
+        int r = t - tb[lo];              // tile within the segment
         TileInfo tl;
         tl.kind = sg.kind;
-        tl.n = local / P;
-        const int mi = local % P;
-        const int s_lo = b * a->MB, s_hi = min(s_lo + a->MB, a->T);
-        int e = el[b], m = mi;
+        const int s_lo = ct[b], s_hi = ct[b + 1];
+        int e = el[b], mbase = 0, mt = 0;   // expert piece, its first m-tile index, its m-tiles
         for (; e < a->E; ++e) {
             const int len = min(off[e + 1], s_hi) - max(off[e], s_lo);
-            const int mt = len > 0 ? (len + tc::BM - 1) / tc::BM : 0;
-            if (m < mt) break;
-            m -= mt;
+            mt = len > 0 ? (len + tc::BM - 1) / tc::BM : 0;
+            if (r < mt * nt) break;
+            r -= mt * nt;
+            mbase += mt;
         }
+        const int m = e < a->E ? r % mt : 0;
+        tl.n = e < a->E ? r / mt : 0;
+        const int mi = mbase + m;
         int piece0, piece_end;
         if (e < a->E) {
             piece0 = max(off[e], s_lo) + m * tc::BM;   // first slot of the m-tile
@@ -252,17 +299,36 @@ struct MinibatchTiles {
         tl.midx = pb[b] + mi;
         return tl;
     }
+    // What a tile's A operand waits for: its minibatch's gather (every CTA takes
+    // part in minibatch 0, the gather CTAs alone in the others), or all GEMM1
+    // N tiles of its m-tile.
+    __device__ const int* dep_counter(const TileInfo& tl, int* target) const {
+        const FusedPlan& pl = a->plan;
+        if (tl.kind == 0) {
+            *target = tl.mb == 0 ? (int)gridDim.x : a->G;
+            return pl.gather_done + tl.mb;
+        }
+        *target = nt1 * tc::EPI_WARPS;
+        return pl.g1_done + tl.midx;
+    }
     __device__ bool wait_inputs(const TileInfo& tl, const Pipe& p) const {
         const FusedPlan& pl = a->plan;
-        const unsigned long long dl = p.deadline;
-        bool ok = tl.kind == 0
-                      ? wait_counter(pl.gather_done + tl.mb, a->G, pl.abort_g, a->ws, dl)
-                      : wait_counter(pl.g1_done + tl.midx, nt1 * tc::EPI_WARPS, pl.abort_g, a->ws, dl);
-        if (!ok) {
+        int target;
+        const int* ctr = dep_counter(tl, &target);
+        if (!wait_counter(ctr, target, pl.abort_g, a->ws, p.deadline)) {
             *p.abort_flag = 1;
             return false;
         }
         fence_proxy_async_all();   // the rows another CTA stored may now be read by TMA
+        return true;
+    }
+    // Non-blocking form for the producer's look-ahead: true (and fenced) if the
+    // tile's inputs are already complete.
+    __device__ bool poll_inputs(const TileInfo& tl) const {
+        int target;
+        const int* ctr = dep_counter(tl, &target);
+        if (ld_acquire(ctr) < target) return false;
+        fence_proxy_async_all();
         return true;
     }
     __device__ void tile_stored(const TileInfo& tl, const Pipe&) const {
@@ -301,14 +367,40 @@ __device__ __forceinline__ void copy_slot_row(uint8_t* __restrict__ dst, const u
     }
 }
 
-// Gather role: minibatch by minibatch, wait for the ring buffer, copy, publish.
-__device__ void gather_role(const FusedArgs& a, unsigned long long deadline, int nt2) {
+// Copy the rows of minibatch b into its ring buffer, warp gw of nw, then make
+// them visible to other CTAs' TMA and count this CTA in gather_done[b].
+__device__ void gather_minibatch(const FusedArgs& a, int b, int gw, int nw) {
     const int lane = threadIdx.x & 31;
+    const FusedPlan& pl = a.plan;
+    const int lo = pl.cut[b], hi = pl.cut[b + 1];
+    const int base = (b % a.NR) * a.MB;
+    for (int t = lo + gw; t < hi; t += nw) {
+        const int s = a.sched[2 * (int64_t)t];
+        const int r = a.sched[2 * (int64_t)t + 1];
+        if (s < 0 || s >= a.S || r < 0 || r >= a.N / a.S) {
+            if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
+            continue;
+        }
+        const int64_t dr = base + (t - lo);
+        const bool has_sf = a.sf_bytes > 0;
+        copy_slot_row(a.ring + dr * a.row_bytes, a.shard_rows[s] + (int64_t)r * a.row_bytes,
+                      a.row_bytes >> 4, has_sf ? a.ring_sf + dr * a.sf_bytes : nullptr,
+                      has_sf ? a.shard_sf[s] + (int64_t)r * a.sf_bytes : nullptr,
+                      has_sf ? a.sf_bytes >> 4 : 0, lane);
+    }
+    publish_fence();
+    __syncthreads();
+    if (threadIdx.x == 0 && b != a.skip_ready) atomicAdd(pl.gather_done + b, 1);
+}
+
+// Gather role: minibatch by minibatch (from 1: every CTA of the launch gathers
+// minibatch 0 first), wait for the ring buffer, copy, publish.
+__device__ void gather_role(const FusedArgs& a, int nmb, unsigned long long deadline, int nt2) {
     const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
     const int nw = a.G * (blockDim.x / 32);
     const FusedPlan& pl = a.plan;
     __shared__ int s_ok;
-    for (int b = 0; b < a.nmb; ++b) {
+    for (int b = 1; b < nmb; ++b) {
         if (threadIdx.x == 0) {
             bool ok = true;
             if (b >= a.NR) {
@@ -320,25 +412,7 @@ __device__ void gather_role(const FusedArgs& a, unsigned long long deadline, int
         }
         __syncthreads();
         if (!s_ok) return;
-        const int lo = b * a.MB, hi = min(lo + a.MB, a.T);
-        const int base = (b % a.NR) * a.MB;
-        for (int t = lo + gw; t < hi; t += nw) {
-            const int s = a.sched[2 * (int64_t)t];
-            const int r = a.sched[2 * (int64_t)t + 1];
-            if (s < 0 || s >= a.S || r < 0 || r >= a.N / a.S) {
-                if (lane == 0) set_status(a.ws, MOE_ERR_DEVICE_CHECK);
-                continue;
-            }
-            const int64_t dr = base + (t - lo);
-            const bool has_sf = a.sf_bytes > 0;
-            copy_slot_row(a.ring + dr * a.row_bytes, a.shard_rows[s] + (int64_t)r * a.row_bytes,
-                          a.row_bytes >> 4, has_sf ? a.ring_sf + dr * a.sf_bytes : nullptr,
-                          has_sf ? a.shard_sf[s] + (int64_t)r * a.sf_bytes : nullptr,
-                          has_sf ? a.sf_bytes >> 4 : 0, lane);
-        }
-        publish_fence();
-        __syncthreads();
-        if (threadIdx.x == 0 && b != a.skip_ready) atomicAdd(pl.gather_done + b, 1);
+        gather_minibatch(a, b, gw, nw);
     }
 }
 
@@ -425,28 +499,39 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const unsigned long long deadline = globaltimer_ns() + a.timeout_ns;
     const FusedPlan& pl = a.plan;
+    __shared__ int s_nmb;
+    if (threadIdx.x == 0) s_nmb = *pl.nmb;   // written by the plan launch before this one
+    __syncthreads();
+    const int nmb = s_nmb;
+    const int warps = blockDim.x / 32;
+
+    // the pipeline fills faster when every CTA gathers the first minibatch
+    if (nmb > 0) gather_minibatch(a, 0, blockIdx.x * warps + threadIdx.x / 32, gridDim.x * warps);
 
     if ((int)blockIdx.x < a.G) {
-        gather_role(a, deadline, s2.n_tiles);
+        gather_role(a, nmb, deadline, s2.n_tiles);
     } else {
         // the tile decode runs at every tile boundary in four roles: keep what it
         // reads in shared memory (the plan was written by the previous launch)
         int32_t* off = reinterpret_cast<int32_t*>(smem + tc::OFF_TAIL);
         for (int e = threadIdx.x; e <= a.E; e += blockDim.x) off[e] = a.offsets[e];
-        const int32_t *tb = pl.tbase, *pb = pl.pbase, *el = pl.elo;
+        const int32_t *tb = pl.tbase, *pb = pl.pbase, *el = pl.elo, *ct = pl.cut;
         if (a.plan_smem) {
             int32_t* stb = off + (a.E + 1);
-            int32_t* spb = stb + (2 * a.nmb + 1);
-            int32_t* sel = spb + (a.nmb + 1);
-            for (int i = threadIdx.x; i <= 2 * a.nmb; i += blockDim.x) stb[i] = pl.tbase[i];
-            for (int i = threadIdx.x; i <= a.nmb; i += blockDim.x) spb[i] = pl.pbase[i];
-            for (int i = threadIdx.x; i < a.nmb; i += blockDim.x) sel[i] = pl.elo[i];
+            int32_t* spb = stb + (2 * a.nmb_max + 1);
+            int32_t* sel = spb + (a.nmb_max + 1);
+            int32_t* sct = sel + a.nmb_max;
+            for (int i = threadIdx.x; i <= 2 * nmb; i += blockDim.x) stb[i] = pl.tbase[i];
+            for (int i = threadIdx.x; i <= nmb; i += blockDim.x) spb[i] = pl.pbase[i];
+            for (int i = threadIdx.x; i < nmb; i += blockDim.x) sel[i] = pl.elo[i];
+            for (int i = threadIdx.x; i <= nmb; i += blockDim.x) sct[i] = pl.cut[i];
             tb = stb;
             pb = spb;
             el = sel;
+            ct = sct;
         }
         __syncthreads();
-        MinibatchTiles src{&a, off, tb, pb, el, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G,
+        MinibatchTiles src{&a, off, tb, pb, el, ct, nmb, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G,
                            (int)gridDim.x - a.G};
         GemmMaps maps;
         maps.a[0] = &tmA1;
@@ -460,7 +545,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     // combine once every GEMM2 tile has been stored
     __shared__ int s_go;
     if (threadIdx.x == 0) {
-        const int target = pl.pbase[a.nmb] * s2.n_tiles * tc::EPI_WARPS;
+        const int target = pl.pbase[nmb] * s2.n_tiles * tc::EPI_WARPS;
         s_go = wait_counter(pl.g2_all, target, pl.abort_g, a.ws, deadline) ? 1 : 0;
     }
     __syncthreads();
@@ -472,16 +557,19 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     if (c.T == 0) return cudaSuccess;
     // plan arrays and counters live in one int region of the workspace
     int* w = c.plan_ints;
+    // (c.nmb is the bound on the minibatch count; the plan kernel cuts the actual ones)
     FusedPlan pl;
     pl.tbase = w;
     pl.pbase = w + (2 * c.nmb + 2);
     pl.elo = pl.pbase + (c.nmb + 1);
-    int* counters = pl.elo + (c.nmb + 1);
+    pl.cut = pl.elo + (c.nmb + 1);
+    int* counters = pl.cut + (c.nmb + 2);
     const int max_m = fused_max_mtiles(c.T, c.E, c.nmb);
     pl.gather_done = counters;
     pl.g2_done = counters + c.nmb;
     pl.g2_all = counters + 2 * c.nmb;
     pl.abort_g = counters + 2 * c.nmb + 1;
+    pl.nmb = counters + 2 * c.nmb + 2;
     pl.g1_done = counters + 2 * c.nmb + 8;
     const int counters_len = 2 * c.nmb + 8 + max_m;
 
@@ -490,7 +578,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     if (!encode_ffn_maps(c.ffn, &m, &s1, &s2)) return cudaErrorInvalidValue;
     fused_plan_kernel<<<1, 1024, sizeof(int32_t) * (c.E + 1), stream>>>(
         c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles, s2.n_tiles, (c.R / c.MB) >= 2 ? 1 : 0, pl,
-        counters_len, counters);
+        counters_len, counters, c.ffn.ws);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
@@ -514,7 +602,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     a.T = c.T;
     a.MB = c.MB;
     a.NR = c.R / c.MB;
-    a.nmb = c.nmb;
+    a.nmb_max = c.nmb;
     a.G = c.G;
     a.row_bytes = c.row_bytes;
     a.sf_bytes = c.sf_bytes;
@@ -523,7 +611,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     a.timeout_ns = c.ffn.timeout_ns;
 
     size_t smem = 1024 + tc::OFF_TAIL + sizeof(int32_t) * (c.E + 1);
-    const size_t plan_bytes = sizeof(int32_t) * ((size_t)4 * c.nmb + 2);
+    const size_t plan_bytes = sizeof(int32_t) * ((size_t)5 * c.nmb + 3);
     a.plan_smem = smem + plan_bytes <= (size_t)227 * 1024 ? 1 : 0;
     if (a.plan_smem) smem += plan_bytes;
     void* kern = c.ffn.mx ? (void*)fused_forward_kernel<true> : (void*)fused_forward_kernel<false>;

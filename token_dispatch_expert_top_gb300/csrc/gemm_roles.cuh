@@ -146,14 +146,27 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
     using namespace tc;
     int stage = 0, g = 0;
     uint32_t phase = 0, gphase = 0;
+    // Look-ahead: a few K-stages before the end of a tile, decode the next tile and
+    // poll (without blocking) whether its inputs are complete, so that the common
+    // case crosses the tile boundary without a dependency round trip.
+    TileInfo tl_next{};
+    bool have_next = false, next_ready = false;
     for (int t = src.first(); t < src.count(); t = src.next(t)) {
-        const TileInfo tl = src.tile(t);
+        const TileInfo tl = have_next ? tl_next : src.tile(t);
         const GemmSide& sd = sides[tl.kind];
-        if (!src.wait_inputs(tl, p)) return;
+        if (!next_ready && !src.wait_inputs(tl, p)) return;
+        have_next = next_ready = false;
         const bool sf_tma = MX && sd.sf_tma;
         const int KB = sd.K / (MX ? 128 : 64);
         const int64_t tile0 = ((int64_t)tl.e * sd.n_tiles + tl.n) * KB;   // first packed K-stage
+        const int tn = src.next(t);
+        const int poll_at = KB > 3 ? KB - 3 : 0;
         for (int kb = 0; kb < KB; ++kb) {
+            if (Src::kLookahead && kb == poll_at && tn < src.count()) {
+                tl_next = src.tile(tn);
+                have_next = true;
+                next_ready = src.poll_inputs(tl_next);
+            }
             if (sf_tma && (kb & 3) == 0) {
                 if (!mbar_wait_bounded(&p.sempty[g], gphase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
                 mbar_arrive_expect_tx(&p.sfull[g], SFSA_BYTES);

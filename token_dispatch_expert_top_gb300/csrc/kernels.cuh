@@ -86,9 +86,9 @@ cudaError_t launch_pack_weights(const PackCall& c, cudaStream_t stream);
 // pieces.
 inline int fused_max_mtiles(int T, int E, int nmb) { return T / 128 + E + 2 * nmb + 8; }
 // int32 entries of the plan + counter region: tbase [2nmb+2], pbase [nmb+1],
-// elo [nmb+1], then the counters
+// elo [nmb+1], cut [nmb+2], then the counters
 inline size_t fused_plan_ints(int T, int E, int nmb) {
-    return (size_t)(2 * nmb + 2) + 2 * (nmb + 1) + 2 * nmb + 8 + fused_max_mtiles(T, E, nmb);
+    return (size_t)(2 * nmb + 2) + 2 * (nmb + 1) + (nmb + 2) + 2 * nmb + 8 + fused_max_mtiles(T, E, nmb);
 }
 struct FusedCall {
     TcFfnCall ffn;            // a = ring [R][H], h = ring [R][I], y = [T][H]
