@@ -493,7 +493,8 @@ template <bool MX>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     fused_forward_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
                          const __grid_constant__ CUtensorMap tmS1a, const __grid_constant__ CUtensorMap tmS2a,
-                         const GemmSide s1, const GemmSide s2, const FusedArgs a) {
+                         const __grid_constant__ GemmSide s1, const __grid_constant__ GemmSide s2,
+                         const __grid_constant__ FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -533,12 +534,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         __syncthreads();
         MinibatchTiles src{&a, off, tb, pb, el, ct, nmb, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G,
                            (int)gridDim.x - a.G};
-        GemmMaps maps;
-        maps.a[0] = &tmA1;
-        maps.a[1] = &tmA2;
-        maps.sfa[0] = &tmS1a;
-        maps.sfa[1] = &tmS2a;
-        GemmSide sides[2] = {s1, s2};
+        const GemmMaps maps{&tmA1, &tmA2, &tmS1a, &tmS2a};
+        const GemmSides sides{&s1, &s2};
         run_gemm_pipeline<MX>(smem, maps, sides, src, a.ws, a.timeout_ns);
     }
 

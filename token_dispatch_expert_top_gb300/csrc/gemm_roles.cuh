@@ -76,9 +76,20 @@ struct GemmSide {
     int out_ld;               // row length of out in elements
 };
 
+// The tensor maps of both GEMMs, picked by tile kind with a select (no indexed
+// array, which would live in local memory).
 struct GemmMaps {
-    const CUtensorMap* a[2];
-    const CUtensorMap* sfa[2];
+    const CUtensorMap *a0, *a1;       // A operand of GEMM1 / GEMM2
+    const CUtensorMap *sfa0, *sfa1;   // A scales (TMA-staged) of GEMM1 / GEMM2
+    __device__ const CUtensorMap* a(int kind) const { return kind ? a1 : a0; }
+    __device__ const CUtensorMap* sfa(int kind) const { return kind ? sfa1 : sfa0; }
+};
+
+// The two GEMM descriptions, picked the same way.  They point at kernel
+// parameters declared __grid_constant__, so nothing is copied to local memory.
+struct GemmSides {
+    const GemmSide *s0, *s1;
+    __device__ const GemmSide& operator[](int kind) const { return kind ? *s1 : *s0; }
 };
 
 struct TileInfo {
@@ -142,7 +153,7 @@ __device__ __forceinline__ void pipe_init(Pipe& p, uint8_t* smem, WsHeader* ws) 
 
 // ------------------------------------------------------------------ TMA producer
 template <bool MX, class Src>
-__device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSide* sides, Src& src) {
+__device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSides& sides, Src& src) {
     using namespace tc;
     int stage = 0, g = 0;
     uint32_t phase = 0, gphase = 0;
@@ -170,7 +181,7 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
             if (sf_tma && (kb & 3) == 0) {
                 if (!mbar_wait_bounded(&p.sempty[g], gphase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
                 mbar_arrive_expect_tx(&p.sfull[g], SFSA_BYTES);
-                tma_load_2d(p.smem + OFF_SFSA + g * SFSA_BYTES, maps.sfa[tl.kind], &p.sfull[g], kb * 4,
+                tma_load_2d(p.smem + OFF_SFSA + g * SFSA_BYTES, maps.sfa(tl.kind), &p.sfull[g], kb * 4,
                             tl.a_row0);
                 if (++g == SFG) {
                     g = 0;
@@ -181,7 +192,7 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
             uint8_t* sa = p.smem + OFF_A + stage * A_BYTES;
             uint8_t* sb = p.smem + OFF_B + stage * B_BYTES;
             mbar_arrive_expect_tx(&p.full[stage], A_BYTES + B_BYTES + (MX ? SFB_BYTES : 0));
-            tma_load_2d(sa, maps.a[tl.kind], &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
+            tma_load_2d(sa, maps.a(tl.kind), &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
             bulk_load(sb, sd.b_pk + (tile0 + kb) * B_TILE, B_TILE, &p.full[stage]);
             if (MX)
                 bulk_load(p.smem + OFF_SFB + stage * SFB_BYTES, sd.sfb_pk + (tile0 + kb) * SFB_TILE,
@@ -196,7 +207,7 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
 
 // ------------------------------------------------------------------- MMA issuer
 template <bool MX, class Src>
-__device__ void mma_role(const Pipe& p, const GemmSide* sides, Src& src) {
+__device__ void mma_role(const Pipe& p, const GemmSides& sides, Src& src) {
     using namespace tc;
     int stage = 0;
     uint32_t phase = 0, acc_phase = 0;
@@ -251,7 +262,7 @@ __device__ void mma_role(const Pipe& p, const GemmSide* sides, Src& src) {
 // holds the four K-step scales of row 32j + r.  tcgen05.cp moves that block into
 // tensor memory; the B scales arrive already packed this way.
 template <class Src>
-__device__ void sf_role(const Pipe& p, const GemmSide* sides, Src& src) {
+__device__ void sf_role(const Pipe& p, const GemmSides& sides, Src& src) {
     using namespace tc;
     const int lane = threadIdx.x % 32;
     int stage = 0, g = 0;
@@ -326,7 +337,7 @@ __device__ void sf_role(const Pipe& p, const GemmSide* sides, Src& src) {
 
 // --------------------------------------------------------- epilogue (warps 4-11)
 template <bool MX, class Src>
-__device__ void epilogue_role(const Pipe& p, const GemmSide* sides, Src& src) {
+__device__ void epilogue_role(const Pipe& p, const GemmSides& sides, Src& src) {
     using namespace tc;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int q = warp & 3;
@@ -412,15 +423,15 @@ __device__ void epilogue_role(const Pipe& p, const GemmSide* sides, Src& src) {
 // Runs the four roles of the pipeline over src on this CTA (all 12 warps), then
 // releases tensor memory.  smem must be 1024-byte aligned.
 template <bool MX, class Src>
-__device__ void run_gemm_pipeline(uint8_t* smem, const GemmMaps& maps, const GemmSide* sides, Src& src,
+__device__ void run_gemm_pipeline(uint8_t* smem, const GemmMaps& maps, const GemmSides& sides, Src& src,
                                   WsHeader* ws, unsigned long long timeout_ns) {
     using namespace tc;
     Pipe p;
     pipe_init<MX>(p, smem, ws);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(maps.a[0]);
-        prefetch_tmap(maps.a[1]);
+        prefetch_tmap(maps.a0);
+        prefetch_tmap(maps.a1);
     }
     tc_fence_before();
     __syncthreads();

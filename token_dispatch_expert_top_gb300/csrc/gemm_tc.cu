@@ -74,7 +74,8 @@ struct ExpertTiles {
 template <bool MX, int KIND>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmSFA, const GemmSide side,
+                           const __grid_constant__ CUtensorMap tmSFA,
+                           const __grid_constant__ GemmSide side,
                            const int32_t* offsets, int E, WsHeader* ws,
                            unsigned long long timeout_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -103,10 +104,8 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     }
     __syncthreads();
     ExpertTiles src{offsets, mpre, E, side.n_tiles, KIND, mpre[E] * side.n_tiles};
-    GemmMaps maps;
-    maps.a[0] = maps.a[1] = &tmA;
-    maps.sfa[0] = maps.sfa[1] = &tmSFA;
-    GemmSide sides[2] = {side, side};
+    const GemmMaps maps{&tmA, &tmA, &tmSFA, &tmSFA};
+    const GemmSides sides{&side, &side};
     run_gemm_pipeline<MX>(smem, maps, sides, src, ws, timeout_ns);
 }
 

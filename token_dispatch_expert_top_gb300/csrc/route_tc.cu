@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS : 1);
+            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS / 2 : 1);   // MMA + the stage's quantiser group
         }
         mbar_init(tfull, 1);
         *abort_flag = 0;
@@ -153,46 +153,53 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         }
     } else if (warp >= 4 && warp < 12) {
         if constexpr (QUANT) {
-            // thread = (token row r, MX block b of the stage's 64 columns)
+            // thread = (token row r, stage parity): it quantises both MX blocks of
+            // its row in every other stage and writes them as two full 32-byte
+            // sectors plus one 2-byte scale store
             const int tq = (warp - 4) * 32 + lane;
             const int r = tq & (BM - 1);
-            const int b = tq >> 7;
+            const int par = tq >> 7;
             const int row = row0 + r;
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = par; kb < KB; kb += 2) {
+                const int stage = kb % STAGES;
+                const uint32_t phase = (uint32_t)((kb / STAGES) & 1);
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
                 const uint8_t* tile = smem + OFF_A + stage * A_BYTES + r * 128;
-                float v[32];
+                uint32_t codes[16];
+                uint8_t sc[2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    // 128-byte swizzle: 16-byte chunk cc of row r sits at chunk cc ^ (r % 8)
-                    const int cc = 4 * b + c;
-                    const uint4 q = *reinterpret_cast<const uint4*>(tile + ((cc ^ (r & 7)) << 4));
-                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                for (int b = 0; b < 2; ++b) {
+                    float v[32];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        v[8 * c + 2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
-                        v[8 * c + 2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
+                    for (int c = 0; c < 4; ++c) {
+                        // 128-byte swizzle: 16-byte chunk cc of row r sits at chunk cc ^ (r % 8)
+                        const int cc = 4 * b + c;
+                        const uint4 q = *reinterpret_cast<const uint4*>(tile + ((cc ^ (r & 7)) << 4));
+                        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            v[8 * c + 2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
+                            v[8 * c + 2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
+                        }
                     }
+                    uint32_t cb[8];
+                    sc[b] = mx_quantize32(v, cb);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) codes[8 * b + i] = cb[i];
                 }
-                uint32_t codes[8];
-                const uint8_t sc = mx_quantize32(v, codes);
                 if (row < args.N) {
-                    uint8_t* dst = args.xq + (int64_t)row * args.H + kb * 64 + 32 * b;
-                    st_v4(dst, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-                    st_v4(dst + 16, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-                    args.xq_sf[(int64_t)row * (args.H / 32) + kb * 2 + b] = sc;
+                    uint8_t* dst = args.xq + (int64_t)row * args.H + kb * 64;
+                    st_v8(dst, codes);
+                    st_v8(dst + 32, codes + 8);
+                    *reinterpret_cast<uint16_t*>(args.xq_sf + (int64_t)row * (args.H / 32) + kb * 2) =
+                        (uint16_t)(sc[0] | (sc[1] << 8));
                 }
-                // Release the stage only after every lane has consumed what it read
-                // (its codes are computed from all of them), so the next TMA refill
-                // of this stage cannot overtake a lane's shared-memory reads.
+                // Release the stage only after every lane has consumed what it read:
+                // the stores above use all of it, and the proxy fence orders these
+                // generic-proxy reads before the next TMA (async-proxy) refill.
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1;
-                }
             }
         }
     } else if (warp >= 12) {
