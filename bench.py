@@ -52,6 +52,15 @@ def job_rate(units_per_rank_step: float, steps: int, t_ms: float, world: int) ->
     return world * units_per_rank_step * steps / (t_ms / 1e3)
 
 
+# DRAM bytes (read + write) of one moe_expert_ffn call (its two grouped-GEMM
+# launches), from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the 32-expert DeepSeek-V3 stand-in (N=1024, same 256 slots per expert): GEMM1
+# 1.0428 + 0.0179 GB, GEMM2 0.5020 + 0.0980 GB.  The full layer has 8x the experts
+# and 8x the slots at the same load per expert, and both the weight and the
+# activation bytes grow in proportion, so a full call moves 8x that.
+FFN_TRAFFIC_BYTES = {"dsv3_mxfp8": 8 * (1.0428 + 0.0179 + 0.5020 + 0.0980) * 1e9}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -304,7 +313,8 @@ def gpu_arm(args, rank, world):
         "bound": "tensor", "achieved": round(ffn_tflops, 2),
         "peak": round(tensor_peak, 1) if tensor_peak else None, "unit": "TFLOP/s",
         "frac": round(ffn_tflops / tensor_peak, 4) if tensor_peak else None,
-        "traffic": None, "peak_source": peak_note,
+        "traffic": (None if args.fused else FFN_TRAFFIC_BYTES.get(w.name)), "traffic_unit": "bytes",
+        "peak_source": peak_note,
         "algorithmic": f"{ffn_flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
     }
     hbm = peaks["hbm_gbs"]
