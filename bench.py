@@ -176,7 +176,7 @@ class StagedStep:
         M.moe_layout(self.idx, L.shape, self.counts, self.offsets, self.sched, self.inv, L.ws)
         if ev[2]:
             ev[2].record()
-        M.moe_dispatch_pull(self.tab, self.tab_sf, L.shape, self.sched, 0, w.T, self.ring,
+        M.moe_dispatch_pull(self.tab, self.tab_sf, L.shape, self.sched, self.inv, 0, w.T, self.ring,
                             self.ring_sf, w.T, L.ws)
         if ev[3]:
             ev[3].record()

@@ -179,25 +179,30 @@ int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, in
 
 /* Pull dispatch ([MoK-2.37x] section 02: the expert side reads the rows it needs,
  * knowing only the source shard and the row; it picks the local placement).
- * Copies slots [slot_begin, slot_begin + slot_count) into the ring: slot t goes
- * to ring row t % ring_slots.
+ * Copies slots [slot_begin, slot_begin + slot_count) into the ring: slot t gets
+ * row sched[t] = (shard, row) and goes to ring row t % ring_slots.
  *   shard_rows   : DEVICE array of S device pointers; shard s holds N/S rows of
  *                  H elements (FP32 / BF16) or H E4M3 codes (MXFP8)
  *   shard_scales : DEVICE array of S device pointers to [N/S][H/32] scales
  *                  (MXFP8 only; NULL otherwise)
  *   sched        : [T][2] from moe_layout
+ *   inv          : [N][k] from moe_layout, or NULL.  Given, the slots are visited
+ *                  in its order (token by token), so the k slots that pull the same
+ *                  source row come one after another and the row is fetched from
+ *                  HBM once; each slot still reads its own schedule entry.  NULL:
+ *                  slot order
  *   ring, ring_scales : [ring_slots][row] destination (ring_scales MXFP8 only),
  *                  16-byte aligned
  * Shard row bases must be 16-byte aligned: a schedule entry whose source row is
  * not (or lies outside its shard) is skipped and recorded as
  * MOE_ERR_DEVICE_CHECK.  When both the row and its scale row are multiples of 16
- * bytes, rows move through the bulk-copy engine (per warp, one lane streams its
- * slots through a ring of shared-memory row buffers: bulk load, then bulk store;
- * source rows are kept in L2, ring rows streamed out); otherwise one warp per
- * slot row copies with 16- or 4-byte vector loads and stores. */
+ * bytes, rows move through the bulk-copy engine (per warp, one lane streams slots
+ * through a ring of shared-memory row buffers: bulk load, then bulk store);
+ * otherwise one warp per slot row copies with 16- or 4-byte vector loads and
+ * stores, in slot order. */
 int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                      const moe_shape_t* shape, const int32_t* sched, int slot_begin,
-                      int slot_count, void* ring, void* ring_scales, int ring_slots,
+                      const moe_shape_t* shape, const int32_t* sched, const int32_t* inv,
+                      int slot_begin, int slot_count, void* ring, void* ring_scales, int ring_slots,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* Grouped SwiGLU expert FFN over expert-contiguous slot rows ([MoK-2.37x]

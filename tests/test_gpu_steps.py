@@ -163,10 +163,12 @@ def test_layout_reports_out_of_range_expert(M):
 
 
 # ------------------------------------------------------------------------ dispatch
-# Rows of 16-byte multiples go through the bulk-copy kernel; MXFP8 at H=256 has
-# 8-byte scale rows and takes the vector-load kernel.
+# Rows of 16-byte multiples go through the bulk-copy kernel (slot order, or token
+# order through inv); MXFP8 at H=256 has 8-byte scale rows and takes the
+# vector-load kernel.
+@pytest.mark.parametrize("token_order", [False, True], ids=["slot_order", "token_order"])
 @pytest.mark.parametrize("dtype,H", [("f32", 128), ("bf16", 1024), ("mxfp8", 1024), ("mxfp8", 256)])
-def test_dispatch_pull_rows_by_schedule(M, dtype, H):
+def test_dispatch_pull_rows_by_schedule(M, dtype, H, token_order):
     rng = np.random.default_rng(3)
     N, E, k, S = 512, 16, 4, 8
     w = synth.Workload("pull", N=N, H=H, I=128, E=E, k=k, S=S, dtype=dtype)
@@ -179,15 +181,16 @@ def test_dispatch_pull_rows_by_schedule(M, dtype, H):
     tab = torch.tensor([t.data_ptr() for t in shards], dtype=torch.int64, device="cuda")
     tab_sf = torch.tensor([t.data_ptr() for t in sc], dtype=torch.int64, device="cuda")
     idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
-    _, _, sched_np, _ = O.layout(idx, E, S)
+    _, _, sched_np, inv_np = O.layout(idx, E, S)
     sched = torch.from_numpy(sched_np).cuda()
+    inv = torch.from_numpy(inv_np).cuda() if token_order else None
     T = N * k
     R = 640                                  # ring smaller than T: slots wrap
     ring = torch.zeros((R, H * elem), dtype=torch.uint8, device="cuda")
     ring_sf = torch.zeros((R, H // 32), dtype=torch.uint8, device="cuda")
     mx = dtype == "mxfp8"
     begin, count = 1400, 600              # rows 1400..1999 wrap past R
-    M.moe_dispatch_pull(tab, tab_sf if mx else None, shape, sched, begin, count, ring,
+    M.moe_dispatch_pull(tab, tab_sf if mx else None, shape, sched, inv, begin, count, ring,
                         ring_sf if mx else None, R, ws)
     assert M.moe_last_device_status(ws) == 0
     allrows = torch.cat(shards).cpu()

@@ -323,8 +323,8 @@ int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, in
 }
 
 int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                      const moe_shape_t* shape, const int32_t* sched, int slot_begin,
-                      int slot_count, void* ring, void* ring_scales, int ring_slots,
+                      const moe_shape_t* shape, const int32_t* sched, const int32_t* inv,
+                      int slot_begin, int slot_count, void* ring, void* ring_scales, int ring_slots,
                       void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_shape(shape);
     if (rc) return rc;
@@ -339,8 +339,8 @@ int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_sc
     if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
     const int row_bytes = s.H * (int)op_elem(s.dtype);
     const int scale_bytes = mx ? s.H / 32 : 0;
-    return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, slot_begin, slot_count,
-                                            s.S, s.N / s.S, row_bytes, scale_bytes, ring,
+    return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, inv, T, slot_begin,
+                                            slot_count, s.S, s.N / s.S, row_bytes, scale_bytes, ring,
                                             ring_scales, ring_slots, num_sms_current(),
                                             at<WsHeader>(workspace, 0), kDefaultTimeoutNs,
                                             (cudaStream_t)stream));
@@ -432,7 +432,7 @@ int moe_forward(const void* x, const void* w_router, const float* bias, const vo
     void* ring = at<void>(ws, pl.ring);
     void* ring_sf = mx ? at<void>(ws, pl.ring_sf) : nullptr;
     rc = cuda_status(launch_dispatch_pull((const void* const*)tab, (const void* const*)tab_sf, sched,
-                                          0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
+                                          inv, T, 0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
                                           ring_sf, pl.ring_slots, num_sms_current(), hdr,
                                           timeout_of(params), st));
     if (rc) return rc;

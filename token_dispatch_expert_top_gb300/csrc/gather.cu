@@ -86,17 +86,24 @@ __global__ void __launch_bounds__(kGatherWarps * 32, 2) dispatch_pull_kernel(
 // streamed out) -- so a few threads per SM keep ~100 KB+ in flight without
 // holding the data in registers.  A buffer is refilled once the bulk store that
 // read it is LAG stores old and has finished reading (bulk-group accounting).
+// With `order` (the inverse map [N][k], flattened) the slots are visited token by
+// token: the k slots that pull the same source row come one after another, so the
+// row is fetched from HBM once and the other k-1 loads hit L2.  Each slot still
+// takes its (shard, row) from its schedule entry; slots outside [slot_begin,
+// slot_begin + slot_count) are skipped.
 constexpr int kBulkWarps = 4;
 constexpr int kBulkLag = 2;
 constexpr int kBulkMaxBuf = 16;
 
 __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
     const uint8_t* const* __restrict__ shard_rows, const uint8_t* const* __restrict__ shard_scales,
-    const int32_t* __restrict__ sched, int slot_begin, int slot_count, int S, int rows_per_shard,
-    int row_bytes, int scale_bytes, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales,
-    int ring_slots, int nbuf, WsHeader* ws, unsigned long long timeout_ns) {
+    const int32_t* __restrict__ sched, const int32_t* __restrict__ order, int npos, int slot_begin,
+    int slot_count, int S, int rows_per_shard, int row_bytes, int scale_bytes,
+    uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales, int ring_slots, int nbuf, WsHeader* ws,
+    unsigned long long timeout_ns) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort[kBulkWarps];
+    __shared__ int s_slot[kBulkWarps][kBulkMaxBuf];   // destination slot of each row buffer
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int unit = row_bytes + scale_bytes;
     uint8_t* buf = smem + (size_t)warp * nbuf * unit;
@@ -108,21 +115,22 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
     }
     __syncwarp();
 
-    // This warp's slots: chunks of 32 consecutive slots, chunk c = gw + i * nw.
+    // This warp's positions (slots, or entries of order): chunks of 32 consecutive
+    // positions, chunk c = gw + i * nw.
     const int gw = blockIdx.x * kBulkWarps + warp, nw = gridDim.x * kBulkWarps;
-    const int nchunks = (slot_count + 31) / 32;
+    const int nchunks = (npos + 31) / 32;
     if (gw >= nchunks) return;
     const int my_chunks = (nchunks - gw + nw - 1) / nw;
     const int last = gw + (my_chunks - 1) * nw;
-    const int total = (my_chunks - 1) * 32 + min(32, slot_count - last * 32);
-    auto slot_of = [&](int q) { return (gw + (q >> 5) * nw) * 32 + (q & 31); };
+    const int total = (my_chunks - 1) * 32 + min(32, npos - last * 32);
+    auto pos_of = [&](int q) { return (gw + (q >> 5) * nw) * 32 + (q & 31); };
 
     const unsigned long long deadline = globaltimer_ns() + timeout_ns;
     const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
     volatile int* abort_flag = &s_abort[warp];
-    uint32_t bad = 0;          // bit b: buffer b holds a slot whose schedule entry is invalid
+    uint32_t bad = 0;          // bit b: buffer b holds nothing to store (skipped or invalid)
     int chunk_sched_q = -1;    // first q of the chunk whose schedule entries the lanes hold
-    int my_s = 0, my_r = 0;
+    int my_s = 0, my_r = 0, my_t = -1;
 
     // Issue the bulk load of the q-th slot into buffer q % nbuf (all lanes call;
     // lane 0 issues).
@@ -130,18 +138,29 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
         const int c0 = q & ~31;
         if (c0 != chunk_sched_q) {
             chunk_sched_q = c0;
-            const int i = slot_of(c0) + lane;
-            if (i < slot_count) {
-                const int t = slot_begin + i;
-                my_s = sched[2 * (int64_t)t];
-                my_r = sched[2 * (int64_t)t + 1];
+            const int i = pos_of(c0) + lane;
+            my_t = -1;
+            if (i < npos) {
+                const int t = order ? order[i] : slot_begin + i;
+                if (t >= slot_begin && t < slot_begin + slot_count) {
+                    my_t = t;
+                    my_s = sched[2 * (int64_t)t];
+                    my_r = sched[2 * (int64_t)t + 1];
+                }
             }
         }
         const int sidx = __shfl_sync(0xffffffffu, my_s, q & 31);
         const int ridx = __shfl_sync(0xffffffffu, my_r, q & 31);
+        const int tq = __shfl_sync(0xffffffffu, my_t, q & 31);
         if (lane == 0) {
             const int b = q % nbuf;
             uint8_t* dst = buf + (size_t)b * unit;
+            s_slot[warp][b] = tq;
+            if (tq < 0) {                  // not this call's slot
+                bad |= 1u << b;
+                mbar_arrive(&bars[b]);
+                return;
+            }
             bool ok = sidx >= 0 && sidx < S && ridx >= 0 && ridx < rows_per_shard;
             const uint8_t* src = ok ? shard_rows[sidx] + (int64_t)ridx * row_bytes : nullptr;
             const uint8_t* ssrc = (ok && scale_bytes) ? shard_scales[sidx] + (int64_t)ridx * scale_bytes : nullptr;
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
                 // give up: nothing more is issued; drain what is in flight below
             } else if (!(bad & (1u << b))) {
                 fence_proxy_async_smem();
-                const int64_t dr = (slot_begin + slot_of(q)) % ring_slots;
+                const int64_t dr = s_slot[warp][b] % ring_slots;
                 const uint8_t* src = buf + (size_t)b * unit;
                 bulk_store_hint(ring + dr * row_bytes, src, (uint32_t)row_bytes, stream);
                 if (scale_bytes)
@@ -194,9 +213,10 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
 }
 
 cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                                 const int32_t* sched, int slot_begin, int slot_count, int S,
-                                 int rows_per_shard, int row_bytes, int scale_bytes, void* ring,
-                                 void* ring_scales, int ring_slots, int num_sms, WsHeader* ws,
+                                 const int32_t* sched, const int32_t* order, int order_len,
+                                 int slot_begin, int slot_count, int S, int rows_per_shard,
+                                 int row_bytes, int scale_bytes, void* ring, void* ring_scales,
+                                 int ring_slots, int num_sms, WsHeader* ws,
                                  unsigned long long timeout_ns, cudaStream_t stream) {
     if (slot_count <= 0) return cudaSuccess;
     const int unit = row_bytes + scale_bytes;
@@ -214,13 +234,14 @@ cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* cons
         if (e != cudaSuccess) return e;
         int per_sm = (int)((227 * 1024) / (smem + 1024));
         if (per_sm < 1) per_sm = 1;
-        const int nchunks = (slot_count + 31) / 32;
+        const int npos = order ? order_len : slot_count;
+        const int nchunks = (npos + 31) / 32;
         int blocks = (nchunks + kBulkWarps - 1) / kBulkWarps;
         if (blocks > num_sms * per_sm) blocks = num_sms * per_sm;
         dispatch_bulk_kernel<<<blocks, kBulkWarps * 32, smem, stream>>>(
-            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, slot_begin,
-            slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring, (uint8_t*)ring_scales,
-            ring_slots, nbuf, ws, timeout_ns);
+            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, order, npos,
+            slot_begin, slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring,
+            (uint8_t*)ring_scales, ring_slots, nbuf, ws, timeout_ns);
         return cudaGetLastError();
     }
     int blocks = (slot_count + kGatherWarps - 1) / kGatherWarps;

@@ -28,10 +28,13 @@ cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_
                           int32_t* offsets, int32_t* sched, int32_t* inv, int32_t* cnt_scratch,
                           int32_t* base_scratch, WsHeader* ws, cudaStream_t stream);
 
+// order (nullable, order_len entries): visit the slots in this order (the
+// inverse map, flattened: source-row order), skipping those outside the range.
 cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                                 const int32_t* sched, int slot_begin, int slot_count, int S,
-                                 int rows_per_shard, int row_bytes, int scale_bytes, void* ring,
-                                 void* ring_scales, int ring_slots, int num_sms, WsHeader* ws,
+                                 const int32_t* sched, const int32_t* order, int order_len,
+                                 int slot_begin, int slot_count, int S, int rows_per_shard,
+                                 int row_bytes, int scale_bytes, void* ring, void* ring_scales,
+                                 int ring_slots, int num_sms, WsHeader* ws,
                                  unsigned long long timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_combine(const void* y, const int32_t* inv, const float* gate, int N, int H,

@@ -70,7 +70,7 @@ _SIGS = {
     "moe_quantize_mxfp8": (_i, [_vp, _i, _i64, _i64, _vp, _vp, _vp]),
     "moe_route_topk": (_i, [_vp, _vp, _vp, _shp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_layout": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "moe_dispatch_pull": (_i, [_vp, _vp, _shp, _vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
+    "moe_dispatch_pull": (_i, [_vp, _vp, _shp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
     "moe_expert_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _shp, _vp, _vp, _sz, _vp]),
     "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _prm, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -163,12 +163,13 @@ def moe_layout(idx, shape: Shape, counts, offsets, sched, inv, ws, stream=None) 
                                          _p(sched), _p(inv), _p(ws), _wsz(ws), _stream(stream)))
 
 
-def moe_dispatch_pull(shard_rows, shard_scales, shape: Shape, sched, slot_begin: int, slot_count: int,
-                      ring, ring_scales, ring_slots: int, ws, stream=None) -> None:
-    """shard_rows / shard_scales: int64 device tensors holding S device pointers."""
+def moe_dispatch_pull(shard_rows, shard_scales, shape: Shape, sched, inv, slot_begin: int,
+                      slot_count: int, ring, ring_scales, ring_slots: int, ws, stream=None) -> None:
+    """shard_rows / shard_scales: int64 device tensors holding S device pointers;
+    inv: the [N][k] inverse map (visit slots token by token) or None (slot order)."""
     _check("moe_dispatch_pull", _lib.moe_dispatch_pull(
-        _p(shard_rows), _p(shard_scales), ctypes.byref(shape), _p(sched), slot_begin, slot_count,
-        _p(ring), _p(ring_scales), ring_slots, _p(ws), _wsz(ws), _stream(stream)))
+        _p(shard_rows), _p(shard_scales), ctypes.byref(shape), _p(sched), _p(inv), slot_begin,
+        slot_count, _p(ring), _p(ring_scales), ring_slots, _p(ws), _wsz(ws), _stream(stream)))
 
 
 def moe_expert_ffn(a, a_scales, offsets, w_gate_up, w_gu_scales, w_down, w_d_scales, shape: Shape,
