@@ -64,11 +64,12 @@ class MoeLayer:
         self.gate = torch.empty((w.N, w.k), dtype=torch.float32, device=dev)
 
     def forward(self, x: torch.Tensor | None = None, fused: bool = False, params=None,
-                out: torch.Tensor | None = None):
+                out: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+        """One forward layer, enqueued on `stream` (default: torch's current stream)."""
         fn = M.moe_forward_fused if fused else M.moe_forward
         fn(self.x if x is None else x, self.w_router, self.bias, self.wgu, self.wgu_sf, self.wd,
            self.wd_sf, self.shape, params if params is not None else self.params,
-           self.out if out is None else out, self.idx, self.gate, self.ws)
+           self.out if out is None else out, self.idx, self.gate, self.ws, stream)
         return self.out if out is None else out
 
     def device_status(self) -> int:
