@@ -137,6 +137,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// Orders generic-proxy accesses to GLOBAL memory with async-proxy (TMA, bulk
+// copy) accesses.  Restricted to the global state space: the unrestricted form
+// also covers the CTA's shared memory, where the thread's own TMA loads may be
+// in flight.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// CTA-scope release store / acquire load of a shared-memory word.
+__device__ __forceinline__ void st_release_cta(volatile int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void*)p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(volatile int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32((const void*)p)) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -39,9 +39,6 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     return v;
 }
 
-__device__ __forceinline__ void fence_proxy_async_all() {
-    asm volatile("fence.proxy.async;" ::: "memory");
-}
 
 // Spin until *ctr >= target.  Gives up (false) when the global abort flag is
 // raised or the deadline passes (then it raises the flag and records a timeout).
@@ -65,7 +62,7 @@ __device__ bool wait_counter(const int* ctr, int target, int* abort_g, WsHeader*
 // Make this thread's global stores visible to other CTAs and to the TMA (async
 // proxy) of other CTAs before a counter is bumped.
 __device__ __forceinline__ void publish_fence() {
-    fence_proxy_async_all();
+    fence_proxy_async_global();
     __threadfence();
 }
 
@@ -240,7 +237,7 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
 // (With the N tile outermost, the reuses of an A tile are a whole wave apart and
 // the weight stream evicts it from L2 in between.)
 struct MinibatchTiles {
-    static constexpr bool kLookahead = true;    // poll the next tile's inputs ahead of time
+    static constexpr bool kDeps = true;         // tiles wait for other CTAs (a dependency thread checks)
     const FusedArgs* a;
     const int32_t* off;       // offsets in shared memory
     const int32_t *tb, *pb, *el, *ct;   // the plan's tbase / pbase / elo / cut (shared memory when they fit)
@@ -319,16 +316,7 @@ struct MinibatchTiles {
             *p.abort_flag = 1;
             return false;
         }
-        fence_proxy_async_all();   // the rows another CTA stored may now be read by TMA
-        return true;
-    }
-    // Non-blocking form for the producer's look-ahead: true (and fenced) if the
-    // tile's inputs are already complete.
-    __device__ bool poll_inputs(const TileInfo& tl) const {
-        int target;
-        const int* ctr = dep_counter(tl, &target);
-        if (ld_acquire(ctr) < target) return false;
-        fence_proxy_async_all();
+        fence_proxy_async_global();   // the rows another CTA stored may now be read by TMA
         return true;
     }
     __device__ void tile_stored(const TileInfo& tl, const Pipe&) const {

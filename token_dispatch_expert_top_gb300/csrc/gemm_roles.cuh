@@ -14,7 +14,10 @@
 //   warp 2      A scale-factor transposer (MXFP8): builds the [32 lanes][4 words]
 //               block of the A rows that tcgen05.cp moves into tensor memory (the
 //               B scales arrive already in that form)
-//   warp 3      idle after the prologue
+//   warp 3      dependency thread (tile sources whose tiles wait for other CTAs):
+//               runs ahead over the tile sequence, waits for each tile's inputs
+//               and raises a shared-memory counter that the producer checks, so
+//               the producer never stalls on a round trip to global memory
 //   warps 4-11  epilogue: two warps per tensor-memory lane quarter, each taking
 //               half the columns, drain the FP32 accumulator into registers,
 //               release it, then apply SwiGLU (+ MXFP8 quantisation of h along I)
@@ -51,7 +54,7 @@ constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr int OFF_SFSA = OFF_SFB + STAGES * SFB_BYTES;
 constexpr int OFF_BAR = OFF_SFSA + SFG * SFSA_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * SFG;        // full, empty, tfull, tempty, drain, sfull, sempty
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;           // tmem base, abort flag
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;           // tmem base, abort flag, ready count
 constexpr int OFF_TAIL = OFF_MISC + 16;                    // kernel-specific tail
 constexpr int TMEM_COLS = 512;
 constexpr int TCOL_SFA = 256;                              // + stage*4
@@ -106,6 +109,7 @@ struct Pipe {
     uint64_t *full, *empty, *tfull, *tempty, *drain, *sfull, *sempty;
     uint32_t tmem_base;
     volatile int* abort_flag;
+    volatile int* ready;      // tiles whose inputs the dependency thread has seen complete
     WsHeader* ws;
     unsigned long long deadline;
 };
@@ -128,6 +132,7 @@ __device__ __forceinline__ void pipe_init(Pipe& p, uint8_t* smem, WsHeader* ws) 
     p.sfull = p.tfull + 3;
     p.sempty = p.sfull + SFG;
     p.abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    p.ready = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
     p.ws = ws;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
@@ -143,6 +148,7 @@ __device__ __forceinline__ void pipe_init(Pipe& p, uint8_t* smem, WsHeader* ws) 
             mbar_init(&p.sempty[g], 1);
         }
         *p.abort_flag = 0;
+        *p.ready = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -157,27 +163,28 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
     using namespace tc;
     int stage = 0, g = 0;
     uint32_t phase = 0, gphase = 0;
-    // Look-ahead: a few K-stages before the end of a tile, decode the next tile and
-    // poll (without blocking) whether its inputs are complete, so that the common
-    // case crosses the tile boundary without a dependency round trip.
-    TileInfo tl_next{};
-    bool have_next = false, next_ready = false;
+    int ordinal = 0;          // tiles of this CTA so far
     for (int t = src.first(); t < src.count(); t = src.next(t)) {
-        const TileInfo tl = have_next ? tl_next : src.tile(t);
+        const TileInfo tl = src.tile(t);
         const GemmSide& sd = sides[tl.kind];
-        if (!next_ready && !src.wait_inputs(tl, p)) return;
-        have_next = next_ready = false;
+        if constexpr (Src::kDeps) {
+            // the dependency thread has acquired this tile's inputs (bounded wait)
+            ++ordinal;
+            uint32_t n = 0;
+            while (ld_acquire_cta(p.ready) < ordinal) {
+                if (*p.abort_flag) return;
+                if ((++n & 255u) == 0 && globaltimer_ns() > p.deadline) {
+                    *p.abort_flag = 1;
+                    set_status(p.ws, MOE_ERR_TIMEOUT);
+                    return;
+                }
+            }
+            fence_proxy_async_global();   // rows other CTAs stored may now be read by TMA
+        }
         const bool sf_tma = MX && sd.sf_tma;
         const int KB = sd.K / (MX ? 128 : 64);
         const int64_t tile0 = ((int64_t)tl.e * sd.n_tiles + tl.n) * KB;   // first packed K-stage
-        const int tn = src.next(t);
-        const int poll_at = KB > 3 ? KB - 3 : 0;
         for (int kb = 0; kb < KB; ++kb) {
-            if (Src::kLookahead && kb == poll_at && tn < src.count()) {
-                tl_next = src.tile(tn);
-                have_next = true;
-                next_ready = src.poll_inputs(tl_next);
-            }
             if (sf_tma && (kb & 3) == 0) {
                 if (!mbar_wait_bounded(&p.sempty[g], gphase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
                 mbar_arrive_expect_tx(&p.sfull[g], SFSA_BYTES);
@@ -202,6 +209,19 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
                 phase ^= 1;
             }
         }
+    }
+}
+
+// ----------------------------------------------------- dependency thread (warp 3)
+// Walks the same tile sequence as the producer, waits (bounded) for each tile's
+// inputs and publishes the count of ready tiles in shared memory.
+template <class Src>
+__device__ void deps_role(const Pipe& p, Src& src) {
+    int n = 0;
+    for (int t = src.first(); t < src.count(); t = src.next(t)) {
+        const TileInfo tl = src.tile(t);
+        if (!src.wait_inputs(tl, p)) return;
+        st_release_cta(p.ready, ++n);
     }
 }
 
@@ -445,7 +465,10 @@ __device__ void run_gemm_pipeline(uint8_t* smem, const GemmMaps& maps, const Gem
         if (lane == 0) mma_role<MX>(p, sides, src);
     } else if (warp == 2) {
         if constexpr (MX) sf_role(p, sides, src);
-    } else if (warp >= 4) {
+    } else if (warp == 3) {
+        if constexpr (Src::kDeps)
+            if (lane == 0) deps_role(p, src);
+    } else {
         epilogue_role<MX>(p, sides, src);
     }
 

@@ -37,7 +37,7 @@ namespace moe {
 // Tiles of one grouped GEMM over expert segments: expert-major, then N tile,
 // then M tile, so CTAs working on consecutive tiles share a weight tile in L2.
 struct ExpertTiles {
-    static constexpr bool kLookahead = false;   // inputs are always ready
+    static constexpr bool kDeps = false;        // inputs are always ready
     const int32_t* offsets;   // [E+1]
     const int32_t* mpre;      // [E+1] prefix of ceil(count_e / 128), in shared memory
     int E, n_tiles, kind, total;
@@ -67,7 +67,6 @@ struct ExpertTiles {
         return tl;
     }
     __device__ bool wait_inputs(const TileInfo&, const Pipe&) const { return true; }
-    __device__ bool poll_inputs(const TileInfo&) const { return true; }
     __device__ void tile_stored(const TileInfo&, const Pipe&) const {}
 };
 
