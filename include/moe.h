@@ -85,9 +85,9 @@ typedef struct {
  * two full GEMM waves, fixed-size ring token buffer reused as soon as a slot's
  * results have left).  timeout_ns bounds every device-side wait. */
 typedef struct {
-    int ring_slots;        /* ring capacity in token slots; 0 = T (no reuse)          */
-    int minibatch;         /* slots per handoff; 0 = two waves of GEMM1 tiles          */
-    int gather_ctas;       /* CTAs in the gather + combine role; 0 = default           */
+    int ring_slots;        /* ring capacity in token slots; 0 = 4 minibatches (<= T)  */
+    int minibatch;         /* slots per handoff; 0 = four waves of GEMM1 tiles         */
+    int gather_ctas;       /* CTAs in the gather + combine role; 0 = SMs / 25          */
     int compute_ctas;      /* CTAs in the expert-FFN role; 0 = all remaining SMs       */
     long long timeout_ns;  /* bound on each device-side wait; 0 = 2e9 (two seconds)    */
     int test_skip_ready;   /* test hook, 0 = off.  When m+1 > 0, the gather role never

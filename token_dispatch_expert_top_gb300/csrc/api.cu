@@ -48,7 +48,9 @@ FusedGeom resolve_fused(const moe_shape_t& s, const moe_params_t* p, int max_cta
     const int T = s.N * s.k;
     const int sms = num_sms_current();
     if (max_ctas <= 0) max_ctas = sms;
-    g.G = (p && p->gather_ctas > 0) ? p->gather_ctas : (sms >= 64 ? sms / 16 : 1);
+    // gather CTAs copy with the bulk-copy engine: ~1/25 of the SMs keeps up with the
+    // expert FFN's consumption of slots (6 of 152 on a GB300)
+    g.G = (p && p->gather_ctas > 0) ? p->gather_ctas : (sms >= 50 ? sms / 25 : 2);
     g.C = (p && p->compute_ctas > 0) ? p->compute_ctas : max_ctas - g.G;
     if (g.G < 1 || g.C < 1 || g.G + g.C > max_ctas) g.status = MOE_ERR_INVALID_ARG;
     const int Tp = T > 0 ? T : 1;
@@ -57,8 +59,9 @@ FusedGeom resolve_fused(const moe_shape_t& s, const moe_params_t* p, int max_cta
     } else if (p && p->ring_slots > 0) {
         g.MB = p->ring_slots >= 64 ? p->ring_slots / 2 : p->ring_slots;
     } else {
-        // two full waves of GEMM1 tiles over the compute SMs, in whole 32-slot units
-        const int waves = moe_min_minibatch(2, g.C > 0 ? g.C : 1, 128, 256, s.I);
+        // four full waves of GEMM1 tiles over the compute SMs (the pages ask for at
+        // least two; four measured faster), in whole 32-slot units
+        const int waves = moe_min_minibatch(4, g.C > 0 ? g.C : 1, 128, 256, s.I);
         g.MB = ((waves + 31) / 32) * 32;
     }
     if (g.MB > Tp) g.MB = Tp;

@@ -205,6 +205,12 @@ __device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, uint
                  "r"(smem_u32(src)), "r"(bytes), "l"(pol)
                  : "memory");
 }
+// Contiguous shared -> global copy by the bulk-copy engine, tracked by bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed bulk groups still read shared memory.
 template <int N>

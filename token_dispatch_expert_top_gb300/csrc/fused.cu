@@ -381,13 +381,120 @@ __device__ void gather_minibatch(const FusedArgs& a, int b, int gw, int nw) {
     if (threadIdx.x == 0 && b != a.skip_ready) atomicAdd(pl.gather_done + b, 1);
 }
 
+// Bulk-copy gather of one minibatch by one stream (lane 0 of a warp issues, all
+// lanes call): the stream's share of the slots moves through its ring of
+// shared-memory row buffers, a bulk load then a bulk store per slot, with up to
+// nbuf - LAG loads in flight.  q0 counts the positions this stream handled in
+// earlier minibatches, so each buffer's barrier phase carries on across
+// minibatches.  Returns the positions handled (every one arrives once on its
+// buffer's barrier, copied or not), or -1 when a wait gave up.
+constexpr int kGatherLag = 2;
+constexpr int kGatherMaxBuf = 16;
+constexpr int kGatherMaxStreams = 6;
+
+__device__ int gather_stream_bulk(const FusedArgs& a, int b, int gs, int ns, uint8_t* buf, uint64_t* bars,
+                                  int nbuf, int q0, volatile int* abort_flag, unsigned long long deadline) {
+    const int lane = threadIdx.x & 31;
+    const FusedPlan& pl = a.plan;
+    const int lo = pl.cut[b], hi = pl.cut[b + 1];
+    const int base = (b % a.NR) * a.MB;
+    const int unit = a.row_bytes + a.sf_bytes;
+    const int nslots = hi - lo;
+    const int nchunks = (nslots + 31) / 32;
+    if (gs >= nchunks) return 0;
+    const int my_chunks = (nchunks - gs + ns - 1) / ns;
+    const int last = gs + (my_chunks - 1) * ns;
+    const int total = (my_chunks - 1) * 32 + min(32, nslots - last * 32);
+    auto slot_of = [&](int q) { return lo + (gs + (q >> 5) * ns) * 32 + (q & 31); };
+    uint32_t bad = 0;
+    int chunk_q = -1, my_s = 0, my_r = 0;
+    auto load = [&](int q) {
+        const int c0 = q & ~31;
+        if (c0 != chunk_q) {
+            chunk_q = c0;
+            const int t = slot_of(c0) + lane;
+            if (t < hi) {
+                my_s = a.sched[2 * (int64_t)t];
+                my_r = a.sched[2 * (int64_t)t + 1];
+            }
+        }
+        const int sidx = __shfl_sync(0xffffffffu, my_s, q & 31);
+        const int ridx = __shfl_sync(0xffffffffu, my_r, q & 31);
+        if (lane == 0) {
+            const int bi = (q0 + q) % nbuf;
+            uint8_t* dst = buf + (size_t)bi * unit;
+            bool ok = sidx >= 0 && sidx < a.S && ridx >= 0 && ridx < a.N / a.S;
+            const uint8_t* src = ok ? a.shard_rows[sidx] + (int64_t)ridx * a.row_bytes : nullptr;
+            const uint8_t* ssrc = (ok && a.sf_bytes) ? a.shard_sf[sidx] + (int64_t)ridx * a.sf_bytes : nullptr;
+            if (ok && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(ssrc)) & 15)) ok = false;
+            if (ok) {
+                bad &= ~(1u << bi);
+                mbar_arrive_expect_tx(&bars[bi], (uint32_t)unit);
+                bulk_load(dst, src, (uint32_t)a.row_bytes, &bars[bi]);
+                if (a.sf_bytes) bulk_load(dst + a.row_bytes, ssrc, (uint32_t)a.sf_bytes, &bars[bi]);
+            } else {
+                set_status(a.ws, MOE_ERR_DEVICE_CHECK);
+                bad |= 1u << bi;
+                mbar_arrive(&bars[bi]);
+            }
+        }
+    };
+    const int pre = min(nbuf, total);
+    for (int q = 0; q < pre; ++q) load(q);
+    int q = 0;
+    for (; q < total; ++q) {
+        if (lane == 0) {
+            const int gq = q0 + q, bi = gq % nbuf;
+            if (mbar_wait_bounded(&bars[bi], (uint32_t)((gq / nbuf) & 1), abort_flag, a.ws, deadline) &&
+                !(bad & (1u << bi))) {
+                const int64_t dr = base + (slot_of(q) - lo);
+                const uint8_t* src = buf + (size_t)bi * unit;
+                bulk_store(a.ring + dr * a.row_bytes, src, (uint32_t)a.row_bytes);
+                if (a.sf_bytes) bulk_store(a.ring_sf + dr * a.sf_bytes, src + a.row_bytes, (uint32_t)a.sf_bytes);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<kGatherLag>();
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const int qn = q - kGatherLag + nbuf;
+        if (q >= kGatherLag && qn < total) load(qn);
+    }
+    if (lane == 0) {
+        bulk_wait_group_all();         // the stores are complete: the rows are in global memory
+        fence_proxy_async_global();    // ... and ordered before this thread's later generic accesses
+    }
+    __syncwarp();
+    return *abort_flag ? -1 : total;
+}
+
 // Gather role: minibatch by minibatch (from 1: every CTA of the launch gathers
-// minibatch 0 first), wait for the ring buffer, copy, publish.
-__device__ void gather_role(const FusedArgs& a, int nmb, unsigned long long deadline, int nt2) {
-    const int gw = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+// minibatch 0 first), wait for the ring buffer, copy, publish.  Rows of 16-byte
+// multiples go through the bulk-copy engine (up to six warps as streams, each
+// with its own row buffers in this CTA's shared memory); others are copied with
+// vector loads by every warp.
+__device__ void gather_role(const FusedArgs& a, int nmb, unsigned long long deadline, int nt2, uint8_t* smem) {
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x / 32) + warp;
     const int nw = a.G * (blockDim.x / 32);
     const FusedPlan& pl = a.plan;
     __shared__ int s_ok;
+    __shared__ int s_abort[kGatherMaxStreams];
+    const int unit = a.row_bytes + a.sf_bytes;
+    const int budget = tc::OFF_TAIL - kGatherMaxStreams * kGatherMaxBuf * 8;
+    int nstreams = unit > 0 ? budget / (4 * unit) : 0;
+    if (nstreams > kGatherMaxStreams) nstreams = kGatherMaxStreams;
+    const bool bulk = a.row_bytes % 16 == 0 && a.sf_bytes % 16 == 0 && nstreams >= 1;
+    int nbuf = bulk ? budget / (nstreams * unit) : 0;
+    if (nbuf > kGatherMaxBuf) nbuf = kGatherMaxBuf;
+    uint8_t* buf = smem + (size_t)warp * nbuf * unit;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nstreams * nbuf * unit) + warp * kGatherMaxBuf;
+    if (bulk && warp < nstreams && lane == 0) {
+        for (int i = 0; i < nbuf; ++i) mbar_init(&bars[i], 1);
+        s_abort[warp] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int q0 = 0;
     for (int b = 1; b < nmb; ++b) {
         if (threadIdx.x == 0) {
             bool ok = true;
@@ -400,7 +507,30 @@ __device__ void gather_role(const FusedArgs& a, int nmb, unsigned long long dead
         }
         __syncthreads();
         if (!s_ok) return;
-        gather_minibatch(a, b, gw, nw);
+        if (bulk) {
+            if (warp < nstreams) {
+                const int n = gather_stream_bulk(a, b, blockIdx.x * nstreams + warp, a.G * nstreams, buf, bars,
+                                                 nbuf, q0, &s_abort[warp], deadline);
+                if (n < 0) {
+                    if (lane == 0) {
+                        atomicExch(pl.abort_g, 1);
+                        // let loads already issued land before this CTA's shared memory goes away
+                        const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+                        while (globaltimer_ns() < d2) {
+                        }
+                    }
+                } else {
+                    q0 += n;
+                }
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                if (b != a.skip_ready) atomicAdd(pl.gather_done + b, 1);
+            }
+        } else {
+            gather_minibatch(a, b, gw, nw);
+        }
     }
 }
 
@@ -498,7 +628,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     if (nmb > 0) gather_minibatch(a, 0, blockIdx.x * warps + threadIdx.x / 32, gridDim.x * warps);
 
     if ((int)blockIdx.x < a.G) {
-        gather_role(a, nmb, deadline, s2.n_tiles);
+        gather_role(a, nmb, deadline, s2.n_tiles, smem);
     } else {
         // the tile decode runs at every tile boundary in four roles: keep what it
         // reads in shared memory (the plan was written by the previous launch)
