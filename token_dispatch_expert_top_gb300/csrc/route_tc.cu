@@ -9,8 +9,13 @@
 // activation quantisation folded into the data path.)
 //
 // CTA = 16 warps:  w0 TMA producer, w1 MMA issuer + TMEM owner, w2-3 idle,
-//                  w4-11 x quantisers (MXFP8 only; two threads per token row, one MX
-//                  block each), w12-15 top-k epilogue.
+//                  w4-11 x quantisers (MXFP8 only; one token row per thread, every
+//                  other K-stage), w12-15 top-k epilogue.
+// Split mode (E >= 64, E % 32 == 0): a cluster of two CTAs shares a 128-token tile,
+// each computing the logits of half of the experts (twice the CTAs, half the
+// weight bytes each).  Each CTA quantises half of the K-stages of x.  The second
+// CTA hands its per-token top-k candidates to the first through distributed
+// shared memory; the first merges the two sorted lists and writes idx and gates.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.cuh"
@@ -25,11 +30,12 @@ constexpr int B_MAX = 256 * 128;             // up to 256 experts x 64 BF16
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_BAR = OFF_B + STAGES * B_MAX;
-constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 1) * 8;
+constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;   // full, empty, tfull, cand
 constexpr int OFF_BIAS = OFF_MISC + 16;
+constexpr int OFF_CAND = OFF_BIAS + 256 * 4;                // split mode: partner's candidates
 constexpr int THREADS = 512;
 constexpr int QUANT_WARPS = 8;
-inline size_t smem_bytes() { return 1024 + OFF_BIAS + 256 * sizeof(float); }
+inline size_t smem_bytes(int kmax) { return 1024 + OFF_CAND + (size_t)kmax * BM * 8; }
 }  // namespace rt
 
 struct RouteArgs {
@@ -66,7 +72,7 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], 
     }
 }
 
-template <int KMAX, bool QUANT>
+template <int KMAX, bool QUANT, bool SPLIT>
 __global__ void __launch_bounds__(rt::THREADS, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     RouteArgs args) {
@@ -77,24 +83,36 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = full + 2 * STAGES;
+    uint64_t* cand_bar = full + 2 * STAGES + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    float* cand_v = reinterpret_cast<float*>(smem + OFF_CAND);                 // [BM][KMAX]
+    int* cand_i = reinterpret_cast<int*>(smem + OFF_CAND + BM * KMAX * 4);     // [BM][KMAX]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     float* sbias = reinterpret_cast<float*>(smem + OFF_BIAS);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int row0 = blockIdx.x * BM;
+    const int half = SPLIT ? (int)cluster_ctarank() : 0;      // which half of the experts
+    const int row0 = (SPLIT ? blockIdx.x / 2 : blockIdx.x) * BM;
     const int KB = args.H / 64;
-    const int E = args.E;
+    const int E = SPLIT ? args.E / 2 : args.E;                // experts of this CTA
+    const int e0 = half * E;                                  // first of them
     const uint32_t b_bytes = (uint32_t)E * 128;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS / 2 : 1);   // MMA + the stage's quantiser group
+            // MMA + the quantiser group of the stage (split mode: only the stages of
+            // this CTA's parity are quantised here)
+            const bool quantised = QUANT && (!SPLIT || (s & 1) == half);
+            mbar_init(&empty[s], quantised ? 1 + QUANT_WARPS / 2 : 1);
         }
         mbar_init(tfull, 1);
+        mbar_init(cand_bar, 4);                               // the partner's four epilogue warps
         *abort_flag = 0;
-        fence_mbar_init();
+        if (SPLIT)
+            fence_mbar_init_cluster();
+        else
+            fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
     }
@@ -103,9 +121,10 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         tmem_relinquish();
     }
     if (warp >= 12)
-        for (int e = threadIdx.x - 384; e < E; e += 128) sbias[e] = args.bias ? args.bias[e] : 0.f;
+        for (int e = threadIdx.x - 384; e < E; e += 128) sbias[e] = args.bias ? args.bias[e0 + e] : 0.f;
     tc_fence_before();
     __syncthreads();
+    if constexpr (SPLIT) cluster_sync();   // the first CTA's candidate barrier exists before any arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
@@ -118,7 +137,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) break;
                 mbar_arrive_expect_tx(&full[stage], A_BYTES + b_bytes);
                 tma_load_2d(smem + OFF_A + stage * A_BYTES, &tmX, &full[stage], kb * 64, row0);
-                tma_load_2d(smem + OFF_B + stage * B_MAX, &tmW, &full[stage], kb * 64, 0);
+                tma_load_2d(smem + OFF_B + stage * B_MAX, &tmW, &full[stage], kb * 64, e0);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -158,9 +177,13 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
             // sectors plus one 2-byte scale store
             const int tq = (warp - 4) * 32 + lane;
             const int r = tq & (BM - 1);
-            const int par = tq >> 7;
+            const int grp = tq >> 7;              // quantiser group (warps 4-7, 8-11)
             const int row = row0 + r;
-            for (int kb = par; kb < KB; kb += 2) {
+            // non-split: group g takes the stages of parity g; split: this CTA takes the
+            // stages of parity `half`, and group g every other one of them
+            const int kb_first = SPLIT ? half + 2 * grp : grp;
+            const int kb_step = SPLIT ? 4 : 2;
+            for (int kb = kb_first; kb < KB; kb += kb_step) {
                 const int stage = kb % STAGES;
                 const uint32_t phase = (uint32_t)((kb / STAGES) & 1);
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
@@ -204,16 +227,18 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         }
     } else if (warp >= 12) {
         const int q = warp & 3;
-        const int row = row0 + 32 * q + lane;
-        if (mbar_wait_bounded(tfull, 0, abort_flag, args.ws, deadline)) {
-            tc_fence_after();
-            float tv[KMAX];
-            int ti[KMAX];
+        const int rl = 32 * q + lane;             // token row within the tile
+        const int row = row0 + rl;
+        float tv[KMAX];
+        int ti[KMAX];
 #pragma unroll
-            for (int i = 0; i < KMAX; ++i) {
-                tv[i] = -INFINITY;
-                ti[i] = -1;
-            }
+        for (int i = 0; i < KMAX; ++i) {
+            tv[i] = -INFINITY;
+            ti[i] = -1;
+        }
+        const bool got = mbar_wait_bounded(tfull, 0, abort_flag, args.ws, deadline);
+        if (got) {
+            tc_fence_after();
             const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
             for (int c = 0; c < E / 16; ++c) {
                 uint32_t r[16];
@@ -223,29 +248,56 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + sbias[16 * c + i];
                 if (args.logits_out && row < args.N) {
-                    float* dst = args.logits_out + (int64_t)row * E + 16 * c;
+                    float* dst = args.logits_out + (int64_t)row * args.E + e0 + 16 * c;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         st_v4(dst + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
                                                       __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) topk_insert<KMAX>(tv, ti, v[i], 16 * c + i);
+                for (int i = 0; i < 16; ++i) topk_insert<KMAX>(tv, ti, v[i], e0 + 16 * c + i);
             }
-            if (row < args.N) {
-                float z = 0.f;
-                float p[KMAX];
+        }
+        bool write = row < args.N;
+        if constexpr (SPLIT) {
+            if (half == 1) {
+                // hand this half's candidates to the first CTA of the pair (its
+                // shared memory, through the cluster), then tell it they are there
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
-                    p[j] = (j < args.k) ? expf(tv[j] - tv[0]) : 0.f;
-                    z += p[j];
+                    const uint32_t av = mapa_shared(smem_u32(cand_v + rl * KMAX + j), 0);
+                    const uint32_t ai = mapa_shared(smem_u32(cand_i + rl * KMAX + j), 0);
+                    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(av), "r"(__float_as_uint(tv[j])) : "memory");
+                    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(ai), "r"(ti[j]) : "memory");
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(cand_bar, 0);
+                write = false;
+            } else {
+                // the other half's top-k joins after this half's: its experts have
+                // higher indices, so equal logits keep the lower index first
+                if (mbar_wait_bounded(cand_bar, 0, abort_flag, args.ws, deadline)) {
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    if (j < args.k) {
-                        args.idx[(int64_t)row * args.k + j] = ti[j];
-                        args.gate[(int64_t)row * args.k + j] = p[j] / z;
-                    }
+                    for (int j = 0; j < KMAX; ++j)
+                        topk_insert<KMAX>(tv, ti, cand_v[rl * KMAX + j], cand_i[rl * KMAX + j]);
+                } else {
+                    write = false;
+                }
+            }
+        }
+        if (got && write) {
+            float z = 0.f;
+            float p[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                p[j] = (j < args.k) ? expf(tv[j] - tv[0]) : 0.f;
+                z += p[j];
+            }
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j < args.k) {
+                    args.idx[(int64_t)row * args.k + j] = ti[j];
+                    args.gate[(int64_t)row * args.k + j] = p[j] / z;
                 }
             }
         }
@@ -268,13 +320,31 @@ bool route_tc_supported(int dtype, int H, int E, int k) {
 
 template <int KMAX, bool QUANT>
 static cudaError_t launch_route(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
-                                int grid, cudaStream_t st) {
-    auto kern = route_tc_kernel<KMAX, QUANT>;
-    const size_t smem = rt::smem_bytes();
+                                int tiles, bool split, cudaStream_t st) {
+    const size_t smem = rt::smem_bytes(KMAX);
+    if (!split) {
+        auto kern = route_tc_kernel<KMAX, QUANT, false>;
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        kern<<<tiles, rt::THREADS, smem, st>>>(tx, tw, a);
+        return cudaGetLastError();
+    }
+    auto kern = route_tc_kernel<KMAX, QUANT, true>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, rt::THREADS, smem, st>>>(tx, tw, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * tiles);
+    cfg.blockDim = dim3(rt::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tx, tw, a);
 }
 
 cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias, int N, int H,
@@ -282,6 +352,10 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
                                  uint8_t* xq, uint8_t* xq_sf, WsHeader* ws,
                                  unsigned long long timeout_ns, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
+    // two CTAs per token tile, each with half of the experts, when the halves are
+    // whole MMA widths of at least 32
+    const bool split = E >= 64 && E % 32 == 0;
+    const int EC = split ? E / 2 : E;          // experts per CTA
     CUtensorMap tx, tw;
     {
         uint64_t dims[2] = {(uint64_t)H, (uint64_t)N};
@@ -290,7 +364,7 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
         if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box))
             return cudaErrorInvalidValue;
         uint64_t dw[2] = {(uint64_t)H, (uint64_t)E};
-        uint32_t bw[2] = {64, (uint32_t)E};
+        uint32_t bw[2] = {64, (uint32_t)EC};
         if (!encode_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dw, str, bw))
             return cudaErrorInvalidValue;
     }
@@ -308,15 +382,18 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
     a.ws = ws;
     a.timeout_ns = timeout_ns;
     uint32_t cols = 32;
-    while (cols < (uint32_t)E) cols <<= 1;
+    while (cols < (uint32_t)EC) cols <<= 1;
     a.tmem_cols = cols;
-    const int grid = (N + rt::BM - 1) / rt::BM;
+    const int tiles = (N + rt::BM - 1) / rt::BM;
     const bool quant = xq != nullptr;
     if (k <= 8)
-        return quant ? launch_route<8, true>(tx, tw, a, grid, stream) : launch_route<8, false>(tx, tw, a, grid, stream);
+        return quant ? launch_route<8, true>(tx, tw, a, tiles, split, stream)
+                     : launch_route<8, false>(tx, tw, a, tiles, split, stream);
     if (k <= 16)
-        return quant ? launch_route<16, true>(tx, tw, a, grid, stream) : launch_route<16, false>(tx, tw, a, grid, stream);
-    return quant ? launch_route<32, true>(tx, tw, a, grid, stream) : launch_route<32, false>(tx, tw, a, grid, stream);
+        return quant ? launch_route<16, true>(tx, tw, a, tiles, split, stream)
+                     : launch_route<16, false>(tx, tw, a, tiles, split, stream);
+    return quant ? launch_route<32, true>(tx, tw, a, tiles, split, stream)
+                 : launch_route<32, false>(tx, tw, a, tiles, split, stream);
 }
 
 }  // namespace moe
