@@ -260,3 +260,37 @@ ORC_API void orc_combine(const double* y, const int32_t* inv, const double* gate
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Backward element-wise steps                                                */
+/* ------------------------------------------------------------------------- */
+
+/* SwiGLU backward.  With h = silu(u) * v and s = sigma(u):
+ *   dh/dv = silu(u) = u * s
+ *   dh/du = v * silu'(u),  silu'(u) = s + u * s * (1 - s)
+ * so du = dh * v * silu'(u) and dv = dh * silu(u). */
+ORC_API void orc_swiglu_backward(const double* u, const double* v, const double* dh, int64_t n,
+                                 double* du, double* dv) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double s = 1.0 / (1.0 + exp(-u[i]));
+        du[i] = dh[i] * v[i] * (s + u[i] * s * (1.0 - s));
+        dv[i] = dh[i] * u[i] * s;
+    }
+}
+
+/* Gradient of the renormalised gates with respect to the selected logits.  The
+ * renormalised top-k gates are a softmax over the k selected logits,
+ * g_j = e^{l_j} / sum_i e^{l_i}, so dg_j/dl_m = g_j (delta_jm - g_m) and
+ *   dlogit_m = sum_j dg_j g_j (delta_jm - g_m) = g_m (dg_m - sum_j g_j dg_j).
+ * The unselected logits get no gradient: the selection is piecewise constant. */
+ORC_API void orc_gate_backward(const double* gate, const double* dgate, int64_t n, int k,
+                               double* dlogit_sel) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        double dot = 0.0;
+        for (int j = 0; j < k; ++j) dot += gate[t * k + j] * dgate[t * k + j];
+        for (int j = 0; j < k; ++j)
+            dlogit_sel[t * k + j] = gate[t * k + j] * (dgate[t * k + j] - dot);
+    }
+}

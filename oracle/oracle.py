@@ -20,7 +20,12 @@ dispatch, expert FFN, combine, final weighted merge):
      workload's intermediate format, y = h . W_down rounded to the staging format
   6. combine: out[n] = sum_j g[n,j] * y[slot(n,j)] in j order, rounded once.
 
+The backward (``backward``) is the exact derivative of that forward, taken in FP64
+with every rounding point passed straight through and the top-k choice held fixed;
+its two element-wise steps (SwiGLU derivative, gate Jacobian) are C loops too.
+
 Rounding points per workload dtype:
+  f64   : nothing rounded (the smooth layer the derivative pins perturb)
   f32   : operands FP32 values; h, y and out rounded to FP32
   bf16  : operands BF16 values; h, y and out rounded to BF16
   mxfp8 : x, W_gate/W_up (along H) and W_down (along I) MXFP8-quantised; h
@@ -79,6 +84,8 @@ def lib():
         L.orc_layout.argtypes = [_i32p, _i64, _int, _int, _int, _i32p, _i32p, _i32p, _i32p]
         L.orc_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
         L.orc_combine.argtypes = [_f64p, _i32p, _f64p, _i64, _int, _i64, _f64p]
+        L.orc_swiglu_backward.argtypes = [_f64p, _f64p, _f64p, _i64, _f64p, _f64p]
+        L.orc_gate_backward.argtypes = [_f64p, _f64p, _i64, _int, _f64p]
         _lib = L
     return _lib
 
@@ -147,7 +154,10 @@ def mxfp8_values(a: np.ndarray) -> np.ndarray:
 
 
 def round_to(a: np.ndarray, fmt: str) -> np.ndarray:
-    """Round an FP64 array to the storage format of a tensor: f32, bf16, mxfp8."""
+    """Round an FP64 array to the storage format of a tensor: f64 (kept as is), f32,
+    bf16, mxfp8."""
+    if fmt == "f64":
+        return np.array(a, dtype=np.float64)
     if fmt == "f32":
         return round_f32(a)
     if fmt == "bf16":
@@ -221,6 +231,7 @@ def combine(y: np.ndarray, inv: np.ndarray, gate: np.ndarray) -> np.ndarray:
 # Storage formats of the FFN operands and outputs per workload dtype.
 FORMATS = {
     #          operands  h        y       out
+    "f64":   ("f64",     "f64",   "f64",  "f64"),     # unrounded: smooth, for derivative pins
     "f32":   ("f32",     "f32",   "f32",  "f32"),
     "bf16":  ("bf16",    "bf16",  "bf16", "bf16"),
     "mxfp8": ("mxfp8",   "mxfp8", "bf16", "bf16"),
@@ -295,3 +306,140 @@ def forward(inp: dict, E: int, k: int, S: int, dtype: str, tokens=None, expert_f
     out = round_to(out, fmt_out)
     return dict(logits=logits, idx=idx, gate=gate, gap=topk_gap(logits, k), counts=counts,
                 offsets=offsets, sched=sched, inv=inv, tokens=toks, out=out, y=y)
+
+
+# --------------------------------------------------------------------------- backward
+def swiglu_backward(u: np.ndarray, v: np.ndarray, dh: np.ndarray):
+    """(du, dv) for h = silu(u) * v, given dh."""
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    dh = np.ascontiguousarray(dh, dtype=np.float64)
+    du = np.empty_like(u)
+    dv = np.empty_like(u)
+    lib().orc_swiglu_backward(u.ravel(), v.ravel(), dh.ravel(), u.size, du.ravel(), dv.ravel())
+    return du, dv
+
+
+def gate_backward(gate: np.ndarray, dgate: np.ndarray) -> np.ndarray:
+    """Gradient of the renormalised top-k gates w.r.t. the selected logits, [n, k]."""
+    gate = np.ascontiguousarray(gate, dtype=np.float64)
+    dgate = np.ascontiguousarray(dgate, dtype=np.float64)
+    n, k = gate.shape
+    out = np.empty_like(gate)
+    lib().orc_gate_backward(gate, dgate, n, k, out)
+    return out
+
+
+def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, experts=None,
+             weights=None) -> dict:
+    """Gradients of the forward layer, L = sum(dout * out), on the oracle.
+
+    The backward the pages describe for the layer ([MoK-2.37x] section 01: training
+    adds two exchanges in the opposite direction; section 02: a pulled reverse
+    combine and a pushed reverse dispatch) undoes the combine by bringing dout back
+    to every slot, differentiates the expert FFN, and undoes the dispatch by adding
+    every slot's input gradient back to its token.  Here it is the exact derivative
+    of ``forward`` with two readings the pages leave open:
+      * every rounding point (MXFP8 / BF16 / FP32 storage of x, the weights, h, y
+        and out) is passed straight through: its derivative is taken as 1, and the
+        values after rounding are the ones used wherever the forward used them;
+      * the top-k choice is piecewise constant, so only the k selected logits of a
+        token get a gradient, through the renormalised gates.
+
+    Per (token n, choice j) pair, with slot expert e = idx[n, j], gate g = gate[n, j]:
+      dy     = g * dout[n]                            reverse combine, pulled by slot
+      dgate  = <dout[n], y>                           y as the forward stored it
+      dh     = dy . Wd                                (y = h . Wd^T)
+      du, dv = dh * v * silu'(u), dh * silu(u)       (h = silu(u) * v)
+      da     = du . Wg + dv . Wu                      (u = a . Wg^T, v = a . Wu^T)
+    Per expert: dWg = sum du^T a, dWu = sum dv^T a, dWd = sum dy^T h over its pairs.
+    Per token: dx_ffn = sum_j da (reverse dispatch); dlogit of the selected experts
+    = g_j (dgate_j - sum_i g_i dgate_i); dx_router = dlogit . W_r; dx = both summed.
+    Router: dW_r = sum_n dlogit^T x (x as stored, which is what the logits read),
+    dbias = sum_n dlogit.
+
+    tokens:  optional token subset for dx and the per-pair outputs of those tokens.
+    experts: optional expert subset for dW_gate_up, dW_down, dW_r rows and dbias.
+    Without either, every output covers the whole layer.  The per-pair arrays cover
+    exactly the pairs listed in ``pairs`` (pair id = n*k + j), which are all pairs
+    of ``tokens``, of the tokens routed to ``experts`` (their dlogit needs every
+    choice's dgate) and every pair routed to ``experts``.
+    Returns dict(idx, gate, inv, counts, offsets, pairs, dy, dgate, dh, du, dv, da,
+    tokens, dx_ffn, dx_router, dx, dlogit, experts, dw_router, dbias, dw_gate_up,
+    dw_down).
+    """
+    fmt_a, fmt_h, fmt_y, _ = FORMATS[dtype]
+    x = _f64(inp["x"])
+    wr = _f64(inp["w_router"])
+    dY = _f64(dout)
+    N, H = x.shape
+    logits = router_logits(x, inp["w_router"], inp.get("bias"))
+    idx, gate = route_topk(logits, k)
+    counts, offsets, sched, inv = layout(idx, E, S)
+    pair_e = idx.ravel().astype(np.int64)
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    exps = np.arange(E) if experts is None else np.asarray(experts, dtype=np.int64)
+
+    # the tokens whose dlogit is needed, and every pair whose FFN gradient is needed
+    routed = np.isin(idx, exps).any(axis=1)
+    need_tok = np.union1d(toks, np.nonzero(routed)[0])
+    pairs = np.union1d((need_tok[:, None] * k + np.arange(k)[None, :]).ravel(),
+                       np.nonzero(np.isin(pair_e, exps))[0])
+    pos = {int(p): i for i, p in enumerate(pairs)}
+    ptok = pairs // k
+    P = len(pairs)
+
+    a_rows = x[ptok]
+    if fmt_a == "mxfp8":
+        a_rows = mxfp8_values(a_rows)
+    dy = gate.ravel()[pairs][:, None] * dY[ptok]           # reverse combine
+    dgate_p = np.empty(P)
+    I = _f64(inp["w_down"][0]).shape[1] if weights is None else weights(int(pair_e[0]))[2].shape[1]
+    dh = np.zeros((P, I))
+    du = np.zeros((P, I))
+    dv = np.zeros((P, I))
+    da = np.zeros((P, H))
+    dwgu = np.zeros((len(exps), 2 * I, H))
+    dwd = np.zeros((len(exps), H, I))
+    exp_pos = {int(e): i for i, e in enumerate(exps)}
+    for e in np.unique(pair_e[pairs]):
+        sel = np.nonzero(pair_e[pairs] == e)[0]
+        a = a_rows[sel]
+        wg, wu, wd = weights(int(e)) if weights is not None else expert_operands(
+            inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
+        u = a @ wg.T
+        v = a @ wu.T
+        h = round_to(swiglu(u, v), fmt_h)
+        y = round_to(h @ wd.T, fmt_y)
+        dgate_p[sel] = np.einsum("ph,ph->p", dY[ptok[sel]], y)
+        dh[sel] = dy[sel] @ wd
+        du[sel], dv[sel] = swiglu_backward(u, v, dh[sel])
+        da[sel] = du[sel] @ wg + dv[sel] @ wu
+        if int(e) in exp_pos:
+            i = exp_pos[int(e)]
+            dwgu[i, :I] = du[sel].T @ a
+            dwgu[i, I:] = dv[sel].T @ a
+            dwd[i] = dy[sel].T @ h
+
+    # reverse dispatch: each token adds the input gradients of its k slots, j order
+    tok_pairs = np.array([[pos[int(n * k + j)] for j in range(k)] for n in toks],
+                         dtype=np.int32).reshape(len(toks), k)
+    dx_ffn = combine(da, tok_pairs, np.ones((len(toks), k)))
+
+    # router: dlogit over the tokens that need it (zero for unselected experts)
+    dgate_full = np.zeros((N, k))
+    have = np.zeros((N, k), dtype=bool)
+    dgate_full.ravel()[pairs] = dgate_p
+    have.ravel()[pairs] = True
+    assert have[need_tok].all()
+    dlsel = gate_backward(gate[need_tok], dgate_full[need_tok])
+    dlogit = np.zeros((N, E))
+    rows = np.repeat(need_tok, k)
+    dlogit[rows, idx[need_tok].ravel()] = dlsel.ravel()
+    dx_router = dlogit[toks] @ wr
+    dw_router = dlogit[:, exps].T @ x
+    dbias = dlogit[:, exps].sum(axis=0)
+    return dict(idx=idx, gate=gate, inv=inv, counts=counts, offsets=offsets, pairs=pairs,
+                dy=dy, dgate=dgate_full, dh=dh, du=du, dv=dv, da=da, tokens=toks,
+                dx_ffn=dx_ffn, dx_router=dx_router, dx=dx_ffn + dx_router, dlogit=dlogit,
+                experts=exps, dw_router=dw_router, dbias=dbias, dw_gate_up=dwgu, dw_down=dwd)

@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+import test_oracle_backward as B
 import test_oracle_formats as F
 import test_oracle_layer as L
 
@@ -85,6 +86,33 @@ def _ffn_transposed_down(orig):
     return f
 
 
+def _swiglu_backward_swapped(orig):
+    def f(u, v, dh):
+        du, dv = orig(u, v, dh)
+        return dv, du
+    return f
+
+
+def _silu_derivative_drops_second_term(orig):
+    def f(u, v, dh):
+        du, dv = orig(u, v, dh)
+        s = 1.0 / (1.0 + np.exp(-u))
+        return dh * v * s, dv
+    return f
+
+
+def _gate_backward_drops_mean(orig):
+    return lambda gate, dgate: np.asarray(gate) * np.asarray(dgate)
+
+
+def _autograd_pin():
+    B.test_matches_torch_autograd(16, 32, 24, 8, 2, True)
+
+
+def _fd_pin():
+    B.test_directional_derivatives_match_central_differences(8, 32, 16, 6, 2)
+
+
 CASES = [
     ("route_topk", _topk_ties_to_higher_index, [L.test_topk_matches_numpy_stable_argsort]),
     ("route_topk", _gates_not_renormalised, [L.test_gates_renormalised_softmax]),
@@ -95,6 +123,10 @@ CASES = [
     ("round_bf16", _round_bf16_truncates, [F.test_bf16_rounding_matches_torch_on_ties_and_near_ties]),
     ("expert_ffn", _ffn_transposed_down,
      [lambda: L.test_single_expert_top1_is_a_dense_ffn("bf16", lambda t: t.bfloat16().double(), 1e-2)]),
+    ("swiglu_backward", _swiglu_backward_swapped, [_fd_pin]),
+    ("swiglu_backward", _silu_derivative_drops_second_term, [_autograd_pin]),
+    ("gate_backward", _gate_backward_drops_mean, [_fd_pin]),
+    ("gate_backward", _gate_backward_drops_mean, [lambda: B.test_router_shift_invariances("f64")]),
 ]
 
 
