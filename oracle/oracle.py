@@ -330,6 +330,62 @@ def gate_backward(gate: np.ndarray, dgate: np.ndarray) -> np.ndarray:
     return out
 
 
+# Storage formats of the backward's dgrad operands and intermediates per workload
+# dtype: dy (the first dgrad GEMM's A operand, along H), the kept pre-activations
+# u|v, du|dv (the second dgrad GEMM's A operand, along I) and da.  The dgrad
+# weights are the masters in the GEMM format quantised along the dgrad K
+# (``expert_operands_dgrad``).
+BWD_FORMATS = {
+    #          dy        uv      duv      da
+    "f64":   ("f64",    "f64",  "f64",   "f64"),
+    "f32":   ("f32",    "f32",  "f32",   "f32"),
+    "bf16":  ("bf16",   "bf16", "bf16",  "bf16"),
+    "mxfp8": ("mxfp8",  "bf16", "mxfp8", "bf16"),
+}
+
+
+def expert_operands_dgrad(w_gate_up_e, w_down_e, dtype: str):
+    """FP64 values of one expert's weights as the dgrad GEMMs see them: (Wg [I,H],
+    Wu [I,H], Wd [H,I]) with the reduction running over I (gate/up) and over H
+    (down).  MXFP8 quantises the masters along that reduction axis: W_gate_up
+    down its 2I rows (blocks split at I), W_down down its H rows."""
+    wgu = _f64(w_gate_up_e)
+    wd = _f64(w_down_e)
+    I = wgu.shape[0] // 2
+    if dtype == "mxfp8":
+        wgu = mxfp8_values(wgu.T).T
+        wd = mxfp8_values(wd.T).T
+    return wgu[:I], wgu[I:], wd
+
+
+def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray,
+                        dy: np.ndarray, dtype: str, wb=None) -> dict:
+    """Backward of one expert's SwiGLU FFN over its rows a, given dy = dL/dy.
+
+    Forward as ``expert_ffn``: u = a Wg^T, v = a Wu^T, h = round_h(silu(u) v),
+    y = round_y(h Wd^T).  Each rounding point's derivative is taken as 1, so
+      dh = dy_b Wd_b,  (du, dv) = swiglu_backward(u_s, v_s, dh),
+      da = round_da(du_b Wg_b + dv_b Wu_b),
+      dWg = du^T a,  dWu = dv^T a,  dWd = dy^T h   (h after its rounding),
+    where _b marks a dgrad GEMM operand in its storage format (BWD_FORMATS; the
+    weights ``wb`` = expert_operands_dgrad, default the forward's values) and
+    u_s, v_s the kept pre-activations.  For "f64" nothing is rounded and this is
+    the exact derivative.
+    Returns dict(u, v, h, y, dh, du, dv, da, dwg, dwu, dwd)."""
+    _, fmt_h, fmt_y, _ = FORMATS[dtype]
+    f_dy, f_uv, f_duv, f_da = BWD_FORMATS[dtype]
+    wg_b, wu_b, wd_b = (wg, wu, wd) if wb is None else wb
+    u = a @ wg.T
+    v = a @ wu.T
+    h = round_to(swiglu(u, v), fmt_h)
+    y = round_to(h @ wd.T, fmt_y)
+    dh = round_to(dy, f_dy) @ wd_b
+    du, dv = swiglu_backward(round_to(u, f_uv), round_to(v, f_uv), dh)
+    da = round_to(round_to(du, f_duv) @ wg_b + round_to(dv, f_duv) @ wu_b, f_da)
+    return dict(u=u, v=v, h=h, y=y, dh=dh, du=du, dv=dv, da=da, dwg=du.T @ a, dwu=dv.T @ a,
+                dwd=dy.T @ h)
+
+
 def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, experts=None,
              weights=None) -> dict:
     """Gradients of the forward layer, L = sum(dout * out), on the oracle.
@@ -345,6 +401,11 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
         values after rounding are the ones used wherever the forward used them;
       * the top-k choice is piecewise constant, so only the k selected logits of a
         token get a gradient, through the renormalised gates.
+
+    For the rounded dtypes the dgrad GEMMs also round their operands the way the
+    layer's configuration fixes for every expert GEMM (MXFP8: each operand
+    quantised along that GEMM's reduction axis; BWD_FORMATS, expert_operands_dgrad),
+    the kept pre-activations u, v are BF16, da is BF16 and dx is rounded once.
 
     Per (token n, choice j) pair, with slot expert e = idx[n, j], gate g = gate[n, j]:
       dy     = g * dout[n]                            reverse combine, pulled by slot
@@ -368,7 +429,7 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     tokens, dx_ffn, dx_router, dx, dlogit, experts, dw_router, dbias, dw_gate_up,
     dw_down).
     """
-    fmt_a, fmt_h, fmt_y, _ = FORMATS[dtype]
+    fmt_a = FORMATS[dtype][0]
     x = _f64(inp["x"])
     wr = _f64(inp["w_router"])
     dY = _f64(dout)
@@ -407,24 +468,21 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
         a = a_rows[sel]
         wg, wu, wd = weights(int(e)) if weights is not None else expert_operands(
             inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
-        u = a @ wg.T
-        v = a @ wu.T
-        h = round_to(swiglu(u, v), fmt_h)
-        y = round_to(h @ wd.T, fmt_y)
-        dgate_p[sel] = np.einsum("ph,ph->p", dY[ptok[sel]], y)
-        dh[sel] = dy[sel] @ wd
-        du[sel], dv[sel] = swiglu_backward(u, v, dh[sel])
-        da[sel] = du[sel] @ wg + dv[sel] @ wu
+        wb = expert_operands_dgrad(inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
+        r = expert_ffn_backward(a, wg, wu, wd, dy[sel], dtype, wb)
+        dgate_p[sel] = np.einsum("ph,ph->p", dY[ptok[sel]], r["y"])
+        dh[sel], du[sel], dv[sel], da[sel] = r["dh"], r["du"], r["dv"], r["da"]
         if int(e) in exp_pos:
             i = exp_pos[int(e)]
-            dwgu[i, :I] = du[sel].T @ a
-            dwgu[i, I:] = dv[sel].T @ a
-            dwd[i] = dy[sel].T @ h
+            dwgu[i, :I] = r["dwg"]
+            dwgu[i, I:] = r["dwu"]
+            dwd[i] = r["dwd"]
 
     # reverse dispatch: each token adds the input gradients of its k slots, j order
     tok_pairs = np.array([[pos[int(n * k + j)] for j in range(k)] for n in toks],
                          dtype=np.int32).reshape(len(toks), k)
     dx_ffn = combine(da, tok_pairs, np.ones((len(toks), k)))
+    f_dx = FORMATS[dtype][3]
 
     # router: dlogit over the tokens that need it (zero for unselected experts)
     dgate_full = np.zeros((N, k))
@@ -441,5 +499,6 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     dbias = dlogit[:, exps].sum(axis=0)
     return dict(idx=idx, gate=gate, inv=inv, counts=counts, offsets=offsets, pairs=pairs,
                 dy=dy, dgate=dgate_full, dh=dh, du=du, dv=dv, da=da, tokens=toks,
-                dx_ffn=dx_ffn, dx_router=dx_router, dx=dx_ffn + dx_router, dlogit=dlogit,
+                dx_ffn=dx_ffn, dx_router=dx_router, dx=round_to(dx_ffn + dx_router, f_dx),
+                dlogit=dlogit,
                 experts=exps, dw_router=dw_router, dbias=dbias, dw_gate_up=dwgu, dw_down=dwd)

@@ -223,14 +223,29 @@ def test_identical_experts_make_the_gates_irrelevant():
     np.testing.assert_allclose(b["dw_down"].sum(0), d1["dw_down"][0], rtol=1e-11, atol=1e-12)
 
 
-def test_linear_in_dout_and_zero_for_zero_dout():
+@pytest.mark.parametrize("dtype,c", [("f64", -2.5), ("mxfp8", -4.0), ("bf16", 0.5)])
+def test_linear_in_dout_and_zero_for_zero_dout(dtype, c):
+    """Linear in dout; with rounding points, for power-of-two factors (which every
+    rounding commutes with)."""
     inp, dout = _layer(12, 32, 32, 4, 2, seed=15)
-    b1 = _grads(O.backward(inp, 4, 2, 1, "mxfp8", dout))
-    b2 = _grads(O.backward(inp, 4, 2, 1, "mxfp8", -2.5 * dout))
-    b0 = _grads(O.backward(inp, 4, 2, 1, "mxfp8", np.zeros_like(dout)))
+    b1 = _grads(O.backward(inp, 4, 2, 1, dtype, dout))
+    b2 = _grads(O.backward(inp, 4, 2, 1, dtype, c * dout))
+    b0 = _grads(O.backward(inp, 4, 2, 1, dtype, np.zeros_like(dout)))
     for name in b1:
-        np.testing.assert_allclose(b2[name], -2.5 * b1[name], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(b2[name], c * b1[name], rtol=1e-12, atol=1e-14)
         assert np.all(b0[name] == 0.0)
+
+
+def test_rounded_backward_is_near_the_exact_one():
+    """The rounding points move each gradient by about the formats' precision."""
+    inp, dout = _layer(16, 64, 64, 4, 2, seed=18)
+    b64 = O.backward(inp, 4, 2, 1, "f64", dout)
+    for dtype, tol in (("bf16", 2e-2), ("mxfp8", 0.15)):
+        b = O.backward(inp, 4, 2, 1, dtype, dout)
+        for name in ("dx", "dw_router", "da", "du", "dv"):
+            ref = b64[name]
+            err = np.abs(b[name] - ref).max() / np.abs(ref).max()
+            assert err < tol, (dtype, name, err)
 
 
 def test_subsets_agree_with_the_full_backward():
