@@ -283,6 +283,146 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
 int moe_layout_noalloc(const int32_t* idx, const moe_shape_t* shape, int32_t* counts,
                        int32_t* offsets, int32_t* sched, int32_t* inv, void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* Backward pass ([MoK-2.37x] section 01: training adds two exchanges in the    */
+/* direction opposite to dispatch and combine; section 02: the backward pulls   */
+/* in the reverse combine and pushes in the reverse dispatch).  BF16 and MXFP8  */
+/* layers only (MOE_ERR_UNSUPPORTED for MOE_F32).  The backward is the exact    */
+/* derivative of the forward with every rounding point passed straight through */
+/* and the top-k choice held fixed: only the k selected logits of a token get a */
+/* gradient, through the renormalised gates.                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Activations the forward keeps for the backward (all DEVICE, caller-owned,
+ * written by moe_forward_train):
+ *   idx, gate, inv : [N][k] int32 / FP32 / int32   (as moe_route_topk, moe_layout)
+ *   offsets        : [E+1] int32, sched : [T][2] int32   (as moe_layout)
+ *   y              : [T][H] BF16 expert outputs in slot order (32-byte aligned)
+ *   uv             : [T][2I] BF16 pre-activations of every slot: u = a.W_gate in
+ *                    columns 0..I-1, v = a.W_up in columns I..2I-1 (32-byte aligned) */
+typedef struct {
+    int32_t* idx;
+    float* gate;
+    int32_t* inv;
+    int32_t* offsets;
+    int32_t* sched;
+    void* y;
+    void* uv;
+} moe_saved_t;
+
+/* Bytes of workspace the backward entry points need (dy, du|dv, da, gate and
+ * logit gradients, router-gradient partial sums).  0 for an invalid shape.  The
+ * first 256 bytes are the status header, as for moe_workspace_bytes(). */
+size_t moe_backward_workspace_bytes(const moe_shape_t* shape);
+
+/* One-time packing of the expert weights for the dgrad GEMMs: the transposes of
+ * the forward's weights, quantised (MXFP8) along the forward's OUTPUT dimension,
+ * which is the dgrad GEMMs' reduction dimension, in the tile-image form of
+ * moe_pack_expert_weights.
+ *   w_gate_up : [E][2I][H] BF16 master weights (natural layout, not packed)
+ *   w_down    : [E][H][I]  BF16 master weights
+ *   packed_gate_up_t : [E][H/256][2I/KS][32 KB], tile row = h, K = the 2I rows of
+ *                      w_gate_up (KS = 128 for MXFP8, 64 for BF16)         (out)
+ *   packed_gu_t_scales : [E][H/256][2I/128][1 KB] (MXFP8; NULL for BF16)  (out)
+ *   packed_down_t : [E][Ip/256][H/KS][32 KB], tile row = i, K = h, Ip = I
+ *                   rounded up to a multiple of 256 (padding rows are zero) (out)
+ *   packed_d_t_scales : [E][Ip/256][H/128][1 KB] (MXFP8; NULL for BF16)   (out)
+ * All pointers 16-byte aligned. */
+int moe_pack_expert_weights_dgrad(const moe_shape_t* shape, const void* w_gate_up,
+                                  const void* w_down, void* packed_gate_up_t,
+                                  uint8_t* packed_gu_t_scales, void* packed_down_t,
+                                  uint8_t* packed_d_t_scales, void* stream);
+
+/* moe_expert_ffn that also writes the pre-activations u|v of every slot row
+ * ([T][2I] BF16, as moe_saved_t.uv) for the SwiGLU backward.  BF16/MXFP8 only. */
+int moe_expert_ffn_train(const void* a, const void* a_scales, const int32_t* offsets,
+                         const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                         const void* w_d_scales, const moe_shape_t* shape, void* y, void* uv,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The staged forward (moe_forward) for training: same output, and every
+ * activation the backward needs goes to `saved` (all fields required).  Takes
+ * the forward's workspace (moe_workspace_bytes). */
+int moe_forward_train(const void* x, const void* w_router, const float* bias,
+                      const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                      const void* w_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                      void* out, const moe_saved_t* saved, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Reverse combine (pulled by slot, [MoK-2.37x] section 02).  For every token n
+ * and choice j, slot s = inv[n][j], gate g = gate[n][j]:
+ *   dy[s]          = g * dout[n]   (FP32 product, then MXFP8-quantised along H
+ *                                    with the MX rule of moe_quantize_mxfp8, or
+ *                                    rounded to BF16)
+ *   dgate[n][j]    = <dout[n], y[s]>            (FP32 accumulation)
+ *   dlogit[n][j]   = g * (dgate[n][j] - sum_i gate[n][i] * dgate[n][i])
+ *   slot_gate[s] = g,  slot_dlogit[s] = dlogit[n][j]
+ *   dout : [N][H] BF16;  y : [T][H] BF16 (moe_saved_t.y)
+ *   dy, dy_scales : [T][H] codes + [T][H/32] scales (MXFP8), or [T][H] BF16 with
+ *                   dy_scales NULL                                       (out)
+ *   dgate, dlogit : [N][k] FP32 (out);  slot_gate, slot_dlogit : [T] FP32 (out)
+ * An inverse-map entry outside [0, T) skips its token and records
+ * MOE_ERR_DEVICE_CHECK.  Needs only the status header of the workspace. */
+int moe_reverse_combine(const void* dout, const void* y, const int32_t* inv, const float* gate,
+                        const moe_shape_t* shape, void* dy, uint8_t* dy_scales, float* dgate,
+                        float* dlogit, float* slot_gate, float* slot_dlogit, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Expert dgrad: the two grouped dgrad GEMMs of the SwiGLU FFN on tcgen05, over
+ * the expert segments [offsets[e], offsets[e+1]) of the slot rows:
+ *   dh = dy . W_down,e ;  du = dh * v * silu'(u) ;  dv = dh * silu(u)
+ *   da = du . W_gate,e + dv . W_up,e
+ *   dy, dy_scales : moe_reverse_combine's dy
+ *   uv            : moe_saved_t.uv
+ *   wt_* : moe_pack_expert_weights_dgrad's output
+ *   duv           : [T][2I] BF16, du in columns 0..I-1, dv in I..2I-1     (out)
+ *   duv_codes, duv_scales : MXFP8 copy of duv quantised along 2I ([T][2I] +
+ *                   [T][2I/32]; the operand of the second GEMM), NULL for BF16 (out)
+ *   da            : [T][H] BF16 input gradient of every slot              (out)
+ * FP32 accumulation; the derivative of silu is evaluated in FP32 from the saved
+ * BF16 u and v.  All row buffers 32-byte aligned. */
+int moe_expert_ffn_dgrad(const void* dy, const uint8_t* dy_scales, const void* uv,
+                         const int32_t* offsets, const void* wt_gate_up,
+                         const uint8_t* wt_gu_scales, const void* wt_down,
+                         const uint8_t* wt_d_scales, const moe_shape_t* shape, void* duv,
+                         uint8_t* duv_codes, uint8_t* duv_scales, void* da, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Reverse dispatch (pushed back to each token, [MoK-2.37x] section 02) plus the
+ * router's input gradient:
+ *   dx[n] = sum_j da[inv[n][j]] + sum_j dlogit[n][j] * w_router[idx[n][j]]
+ * each sum in j order in FP32 (slots first), rounded once to BF16.  No atomics:
+ * deterministic.
+ *   da : [T][H] BF16;  inv, idx : [N][k];  dlogit : [N][k] FP32;
+ *   w_router : [E][H] BF16;  dx : [N][H] BF16 (out)
+ * An index out of range skips its terms and records MOE_ERR_DEVICE_CHECK. */
+int moe_reverse_dispatch(const void* da, const int32_t* inv, const int32_t* idx,
+                         const float* dlogit, const void* w_router, const moe_shape_t* shape,
+                         void* dx, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Router weight gradient: dW_r[e] = sum over expert e's slots s (in slot order)
+ * of slot_dlogit[s] * x[token(s)], dbias[e] = sum of slot_dlogit over them;
+ * token(s) = shard * (N/S) + row from sched.  Pieces of 256 slots are summed in
+ * FP32 and then reduced in piece order, so the result is deterministic.
+ *   x : [N][H] BF16;  sched : [T][2];  offsets : [E+1];  slot_dlogit : [T] FP32
+ *   dw_router : [E][H] FP32 (out);  dbias : [E] FP32 (out, may be NULL)
+ * Needs moe_backward_workspace_bytes() of workspace. */
+int moe_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets,
+                     const float* slot_dlogit, const moe_shape_t* shape, float* dw_router,
+                     float* dbias, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The backward of the layer, one kernel per step on `stream`: reverse combine,
+ * expert dgrad, reverse dispatch, router gradient.
+ *   dout : [N][H] BF16;  x, w_router : the forward's inputs;  saved : filled by
+ *   moe_forward_train;  wt_* : moe_pack_expert_weights_dgrad's output
+ *   dx : [N][H] BF16;  dw_router : [E][H] FP32;  dbias : [E] FP32 or NULL  (out)
+ * Needs moe_backward_workspace_bytes() of workspace. */
+int moe_backward(const void* dout, const void* x, const void* w_router, const moe_saved_t* saved,
+                 const void* wt_gate_up, const uint8_t* wt_gu_scales, const void* wt_down,
+                 const uint8_t* wt_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                 void* dx, float* dw_router, float* dbias, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
 /* Smallest minibatch (in slots) that gives `waves` full waves of GEMM1 tiles of
  * tile_m x tile_n over `compute_sms` SMs when GEMM1 has 2*I output columns
  * ([MoK-2.37x] section 02: a minibatch should form at least two full waves; the

@@ -74,3 +74,32 @@ def test_minibatch_wave_rule_golden():
     assert rows
     for waves, sms, bm, bn, I, expect in rows:
         assert M.moe_min_minibatch(int(waves), int(sms), int(bm), int(bn), int(I)) == int(expect)
+
+
+def test_backward_host_checks():
+    lib = M.lib()
+    f32 = M.Shape.of(synth.WORKLOADS["tiny_f32"])
+    mx = M.Shape.of(synth.WORKLOADS["dsv3_mxfp8"])
+    # the backward has no FP32 path
+    assert M.moe_backward_workspace_bytes(f32) == 0
+    assert lib.moe_reverse_combine(1, 1, 1, 1, ctypes.byref(f32), 1, None, 1, 1, 1, 1, 32, 1 << 20,
+                                   None) == M.MOE_ERR_UNSUPPORTED
+    # workspace: dy codes + scales, du|dv in BF16 and MXFP8, da, per-slot floats
+    T, H, I = 8192 * 8, 7168, 2048
+    need = T * (H + H // 32 + 4 * I + 2 * I + 2 * I // 32 + 2 * H + 16)
+    assert M.moe_backward_workspace_bytes(mx) >= need
+    # MXFP8 reverse combine needs dy scales; a null dout is an argument error
+    assert lib.moe_reverse_combine(16, 16, 16, 16, ctypes.byref(mx), 16, None, 16, 16, 16, 16, 32,
+                                   1 << 20, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_reverse_combine(None, 16, 16, 16, ctypes.byref(mx), 16, 16, 16, 16, 16, 16, 32,
+                                   1 << 20, None) == M.MOE_ERR_INVALID_ARG
+    # router wgrad needs the backward workspace
+    assert lib.moe_router_wgrad(16, 16, 16, 16, ctypes.byref(mx), 16, 16, 32, 1 << 20,
+                                None) == M.MOE_ERR_WORKSPACE
+    # the training forward needs every saved buffer
+    sv = M.Saved(16, 16, 16, 16, 16, 32, None)
+    assert lib.moe_forward_train(16, 16, None, 16, 16, 16, 16, ctypes.byref(mx), None, 16,
+                                 ctypes.byref(sv), 32, 1 << 40, None) == M.MOE_ERR_INVALID_ARG
+    # misaligned du|dv output
+    assert lib.moe_expert_ffn_dgrad(16, 16, 32, 16, 16, 16, 16, 16, ctypes.byref(mx), 48, 32, 16, 32,
+                                    32, 1 << 20, None) == M.MOE_ERR_INVALID_ARG

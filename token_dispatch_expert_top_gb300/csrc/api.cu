@@ -128,6 +128,41 @@ T* at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// Workspace regions of the backward entry points, in order.
+struct BwdPlan {
+    size_t header, dy, dy_sf, duv, duv_q, duv_sf, da, dgate, dlogit, slot_gate, slot_dlogit;
+    size_t part, part_b, ppre, total;
+};
+
+BwdPlan make_bwd_plan(const moe_shape_t& s) {
+    const size_t T = (size_t)s.N * s.k;
+    const bool mx = s.dtype == MOE_MXFP8;
+    BwdPlan pl{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    const size_t pmax = (size_t)router_max_pieces((int)T, s.E);
+    pl.header = take(sizeof(WsHeader));
+    pl.dy = take(T * s.H * (mx ? 1 : 2));
+    pl.dy_sf = take(mx ? T * (s.H / 32) : 0);
+    pl.duv = take(T * 2 * s.I * 2);
+    pl.duv_q = take(mx ? T * 2 * s.I : 0);
+    pl.duv_sf = take(mx ? T * (2 * s.I / 32) : 0);
+    pl.da = take(T * s.H * 2);
+    pl.dgate = take(sizeof(float) * T);
+    pl.dlogit = take(sizeof(float) * T);
+    pl.slot_gate = take(sizeof(float) * T);
+    pl.slot_dlogit = take(sizeof(float) * T);
+    pl.part = take(sizeof(float) * pmax * s.H);
+    pl.part_b = take(sizeof(float) * pmax);
+    pl.ppre = take(sizeof(int32_t) * (s.E + 1));
+    pl.total = off;
+    return pl;
+}
+
 int check_shape(const moe_shape_t* s) {
     if (!s) return MOE_ERR_INVALID_ARG;
     if (s->N < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 || s->S <= 0)
@@ -149,6 +184,20 @@ int check_ws(const moe_shape_t* s, const moe_params_t* p, void* ws, size_t bytes
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Shapes the backward supports: the tensor-core layers (BF16, MXFP8).
+int check_bwd_shape(const moe_shape_t* s) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    return s->dtype == MOE_F32 ? MOE_ERR_UNSUPPORTED : MOE_OK;
+}
+
+int check_bwd_ws(const moe_shape_t* s, void* ws, size_t bytes) {
+    if (!ws || ((uintptr_t)ws & 31)) return MOE_ERR_WORKSPACE;
+    return bytes < make_bwd_plan(*s).total ? MOE_ERR_WORKSPACE : MOE_OK;
+}
+
+bool aligned32(const void* p) { return ((uintptr_t)p & 31) == 0; }
+
 unsigned long long timeout_of(const moe_params_t* p) {
     return (p && p->timeout_ns > 0) ? (unsigned long long)p->timeout_ns : kDefaultTimeoutNs;
 }
@@ -161,7 +210,7 @@ __global__ void fill_shard_table_kernel(const uint8_t** tab, const uint8_t* base
 int expert_ffn_impl(const void* a, const void* a_scales, int a_rows, const int32_t* offsets,
                     const void* w_gate_up, const void* w_gu_scales, const void* w_down,
                     const void* w_d_scales, const moe_shape_t& s, void* y, void* ws,
-                    unsigned long long timeout, cudaStream_t st) {
+                    unsigned long long timeout, cudaStream_t st, void* uv = nullptr) {
     const Plan pl = make_plan(s, nullptr);
     const int T = s.N * s.k;
     if (s.dtype == MOE_F32)
@@ -185,6 +234,7 @@ int expert_ffn_impl(const void* a, const void* a_scales, int a_rows, const int32
     c.h = at<void>(ws, pl.h);
     c.h_sf = at<void>(ws, pl.h_sf);
     c.y = y;
+    c.uv = uv;
     c.ws = at<WsHeader>(ws, pl.header);
     c.timeout_ns = timeout;
     c.grid = num_sms_current();
@@ -383,10 +433,14 @@ int moe_combine(const void* y, const int32_t* inv, const float* gate, const moe_
                                       (cudaStream_t)stream));
 }
 
-int moe_forward(const void* x, const void* w_router, const float* bias, const void* w_gate_up,
-                const void* w_gu_scales, const void* w_down, const void* w_d_scales,
-                const moe_shape_t* shape, const moe_params_t* params, void* out, int32_t* idx_out,
-                float* gate_out, void* workspace, size_t workspace_bytes, void* stream) {
+// The staged forward; with `sv`, the routing, layout, y and u|v go to the
+// caller's saved-activation buffers (training).
+static int forward_staged(const void* x, const void* w_router, const float* bias,
+                          const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                          const void* w_d_scales, const moe_shape_t* shape,
+                          const moe_params_t* params, void* out, int32_t* idx_out, float* gate_out,
+                          const moe_saved_t* sv, void* workspace, size_t workspace_bytes,
+                          void* stream) {
     int rc = check_shape(shape);
     if (rc) return rc;
     rc = check_ws(shape, params, workspace, workspace_bytes);
@@ -404,12 +458,12 @@ int moe_forward(const void* x, const void* w_router, const float* bias, const vo
     WsHeader* hdr = at<WsHeader>(ws, pl.header);
     const int T = s.N * s.k;
     const int rows = s.N / s.S;
-    int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, pl.idx);
-    float* gate = gate_out ? gate_out : at<float>(ws, pl.gate);
+    int32_t* idx = sv ? sv->idx : (idx_out ? idx_out : at<int32_t>(ws, pl.idx));
+    float* gate = sv ? sv->gate : (gate_out ? gate_out : at<float>(ws, pl.gate));
     int32_t* counts = at<int32_t>(ws, pl.counts);
-    int32_t* offsets = at<int32_t>(ws, pl.offsets);
-    int32_t* sched = at<int32_t>(ws, pl.sched);
-    int32_t* inv = at<int32_t>(ws, pl.inv);
+    int32_t* offsets = sv ? sv->offsets : at<int32_t>(ws, pl.offsets);
+    int32_t* sched = sv ? sv->sched : at<int32_t>(ws, pl.sched);
+    int32_t* inv = sv ? sv->inv : at<int32_t>(ws, pl.inv);
 
     // 1. router + top-k (+ the MXFP8 copy of x each source shard serves)
     uint8_t* xq = mx ? at<uint8_t>(ws, pl.xq) : nullptr;
@@ -440,13 +494,22 @@ int moe_forward(const void* x, const void* w_router, const float* bias, const vo
                                           timeout_of(params), st));
     if (rc) return rc;
     // 4. grouped SwiGLU expert FFN
-    void* y = at<void>(ws, pl.y);
+    void* y = sv ? sv->y : at<void>(ws, pl.y);
     rc = expert_ffn_impl(ring, ring_sf, pl.ring_slots, offsets, w_gate_up, w_gu_scales, w_down,
-                         w_d_scales, s, y, ws, timeout_of(params), st);
+                         w_d_scales, s, y, ws, timeout_of(params), st, sv ? sv->uv : nullptr);
     if (rc) return rc;
     // 5. combine + weighted merge
-    return cuda_status(launch_combine(y, inv, gate, s.N, s.H, s.k, T, s.dtype, out,
-                                      num_sms_current(), hdr, st));
+    rc = cuda_status(launch_combine(y, inv, gate, s.N, s.H, s.k, T, s.dtype, out,
+                                    num_sms_current(), hdr, st));
+    return rc;
+}
+
+int moe_forward(const void* x, const void* w_router, const float* bias, const void* w_gate_up,
+                const void* w_gu_scales, const void* w_down, const void* w_d_scales,
+                const moe_shape_t* shape, const moe_params_t* params, void* out, int32_t* idx_out,
+                float* gate_out, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_staged(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, shape,
+                          params, out, idx_out, gate_out, nullptr, workspace, workspace_bytes, stream);
 }
 
 int moe_forward_fused(const void* x, const void* w_router, const float* bias,
@@ -551,6 +614,199 @@ int moe_min_minibatch(int waves, int compute_sms, int tile_m, int tile_n, int I)
     const long long num = (long long)waves * compute_sms * tile_m * tile_n;
     const long long den = 2LL * I;
     return (int)((num + den - 1) / den);
+}
+
+// ------------------------------------------------------------------ backward
+size_t moe_backward_workspace_bytes(const moe_shape_t* shape) {
+    if (check_bwd_shape(shape) != MOE_OK) return 0;
+    return make_bwd_plan(*shape).total;
+}
+
+int moe_pack_expert_weights_dgrad(const moe_shape_t* shape, const void* w_gate_up,
+                                  const void* w_down, void* packed_gate_up_t,
+                                  uint8_t* packed_gu_t_scales, void* packed_down_t,
+                                  uint8_t* packed_d_t_scales, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!w_gate_up || !w_down || !packed_gate_up_t || !packed_down_t) return MOE_ERR_INVALID_ARG;
+    if (mx && (!packed_gu_t_scales || !packed_d_t_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(packed_gate_up_t) || !aligned16(packed_down_t)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = cuda_status(launch_pack_transposed(mx, w_gate_up, s.E, 2 * s.I, s.H, packed_gate_up_t,
+                                            packed_gu_t_scales, num_sms_current(), st));
+    if (rc) return rc;
+    return cuda_status(launch_pack_transposed(mx, w_down, s.E, s.H, s.I, packed_down_t,
+                                              packed_d_t_scales, num_sms_current(), st));
+}
+
+int moe_expert_ffn_train(const void* a, const void* a_scales, const int32_t* offsets,
+                         const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                         const void* w_d_scales, const moe_shape_t* shape, void* y, void* uv,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    if (!uv || !aligned32(uv)) return MOE_ERR_INVALID_ARG;
+    rc = check_ws(shape, nullptr, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!a || !offsets || !w_gate_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (mx && (!a_scales || !w_gu_scales || !w_d_scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned32(y))
+        return MOE_ERR_INVALID_ARG;
+    return expert_ffn_impl(a, a_scales, s.N * s.k, offsets, w_gate_up, w_gu_scales, w_down,
+                           w_d_scales, s, y, workspace, kDefaultTimeoutNs, (cudaStream_t)stream, uv);
+}
+
+int moe_forward_train(const void* x, const void* w_router, const float* bias,
+                      const void* w_gate_up, const void* w_gu_scales, const void* w_down,
+                      const void* w_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                      void* out, const moe_saved_t* saved, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    if (!saved || !saved->idx || !saved->gate || !saved->inv || !saved->offsets || !saved->sched ||
+        !saved->y || !saved->uv)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned32(saved->y) || !aligned32(saved->uv)) return MOE_ERR_INVALID_ARG;
+    return forward_staged(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, shape,
+                          params, out, nullptr, nullptr, saved, workspace, workspace_bytes, stream);
+}
+
+int moe_reverse_combine(const void* dout, const void* y, const int32_t* inv, const float* gate,
+                        const moe_shape_t* shape, void* dy, uint8_t* dy_scales, float* dgate,
+                        float* dlogit, float* slot_gate, float* slot_dlogit, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!dout || !y || !inv || !gate || !dy || !dgate || !dlogit || !slot_gate || !slot_dlogit)
+        return MOE_ERR_INVALID_ARG;
+    if (mx != (dy_scales != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dout) || !aligned16(y) || !aligned16(dy)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_reverse_combine(mx, dout, y, inv, gate, s.N, s.H, s.k, s.N * s.k, dy,
+                                              dy_scales, dgate, dlogit, slot_gate, slot_dlogit,
+                                              num_sms_current(), at<WsHeader>(workspace, 0),
+                                              (cudaStream_t)stream));
+}
+
+int moe_expert_ffn_dgrad(const void* dy, const uint8_t* dy_scales, const void* uv,
+                         const int32_t* offsets, const void* wt_gate_up,
+                         const uint8_t* wt_gu_scales, const void* wt_down,
+                         const uint8_t* wt_d_scales, const moe_shape_t* shape, void* duv,
+                         uint8_t* duv_codes, uint8_t* duv_scales, void* da, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    if (!dy || !uv || !offsets || !wt_gate_up || !wt_down || !duv || !da) return MOE_ERR_INVALID_ARG;
+    if (mx && (!dy_scales || !wt_gu_scales || !wt_d_scales || !duv_codes || !duv_scales))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned32(uv) || !aligned16(wt_gate_up) || !aligned16(wt_down) ||
+        !aligned32(duv) || !aligned32(da) || (mx && !aligned32(duv_codes)))
+        return MOE_ERR_INVALID_ARG;
+    if (mx && (((uintptr_t)dy_scales & 15) || ((uintptr_t)duv_scales & 15)))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    TcDgradCall c{};
+    c.mx = mx;
+    c.T = s.N * s.k;
+    c.H = s.H;
+    c.I = s.I;
+    c.E = s.E;
+    c.a_rows = c.T;
+    c.dy = dy;
+    c.dy_sf = dy_scales;
+    c.uv = uv;
+    c.offsets = offsets;
+    c.wt_down = wt_down;
+    c.wt_d_sf = wt_d_scales;
+    c.wt_gate_up = wt_gate_up;
+    c.wt_gu_sf = wt_gu_scales;
+    c.duv = duv;
+    c.duv_q = duv_codes;
+    c.duv_sf = duv_scales;
+    c.da = da;
+    c.ws = at<WsHeader>(workspace, 0);
+    c.timeout_ns = kDefaultTimeoutNs;
+    c.grid = num_sms_current();
+    return cuda_status(launch_ffn_dgrad_tc(c, (cudaStream_t)stream));
+}
+
+int moe_reverse_dispatch(const void* da, const int32_t* inv, const int32_t* idx,
+                         const float* dlogit, const void* w_router, const moe_shape_t* shape,
+                         void* dx, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (s.N == 0) return MOE_OK;
+    if (!da || !inv || !idx || !dlogit || !w_router || !dx) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(da) || !aligned16(w_router) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_reverse_dispatch(da, inv, idx, dlogit, w_router, s.N, s.H, s.k,
+                                               s.N * s.k, s.E, dx, num_sms_current(),
+                                               at<WsHeader>(workspace, 0), (cudaStream_t)stream));
+}
+
+int moe_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets,
+                     const float* slot_dlogit, const moe_shape_t* shape, float* dw_router,
+                     float* dbias, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    rc = check_bwd_ws(shape, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (!offsets || !dw_router || (s.N > 0 && (!x || !sched || !slot_dlogit))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dw_router) || ((uintptr_t)x & 7)) return MOE_ERR_INVALID_ARG;
+    const BwdPlan pl = make_bwd_plan(s);
+    return cuda_status(launch_router_wgrad(x, sched, offsets, slot_dlogit, s.N, s.H, s.E, s.N * s.k,
+                                           s.N / s.S, dw_router, dbias, at<float>(workspace, pl.part),
+                                           at<float>(workspace, pl.part_b),
+                                           at<int32_t>(workspace, pl.ppre),
+                                           at<WsHeader>(workspace, pl.header), (cudaStream_t)stream));
+}
+
+int moe_backward(const void* dout, const void* x, const void* w_router, const moe_saved_t* saved,
+                 const void* wt_gate_up, const uint8_t* wt_gu_scales, const void* wt_down,
+                 const uint8_t* wt_d_scales, const moe_shape_t* shape, const moe_params_t* params,
+                 void* dx, float* dw_router, float* dbias, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    rc = check_bwd_ws(shape, workspace, workspace_bytes);
+    if (rc) return rc;
+    (void)params;
+    const moe_shape_t& s = *shape;
+    if (!saved) return MOE_ERR_INVALID_ARG;
+    if (s.N == 0) return MOE_OK;
+    const bool mx = s.dtype == MOE_MXFP8;
+    const BwdPlan pl = make_bwd_plan(s);
+    void* ws = workspace;
+    uint8_t* dy_sf = mx ? at<uint8_t>(ws, pl.dy_sf) : nullptr;
+    rc = moe_reverse_combine(dout, saved->y, saved->inv, saved->gate, shape, at<void>(ws, pl.dy),
+                             dy_sf, at<float>(ws, pl.dgate), at<float>(ws, pl.dlogit),
+                             at<float>(ws, pl.slot_gate), at<float>(ws, pl.slot_dlogit), ws,
+                             workspace_bytes, stream);
+    if (rc) return rc;
+    rc = moe_expert_ffn_dgrad(at<void>(ws, pl.dy), dy_sf, saved->uv, saved->offsets, wt_gate_up,
+                              wt_gu_scales, wt_down, wt_d_scales, shape, at<void>(ws, pl.duv),
+                              mx ? at<uint8_t>(ws, pl.duv_q) : nullptr,
+                              mx ? at<uint8_t>(ws, pl.duv_sf) : nullptr, at<void>(ws, pl.da), ws,
+                              workspace_bytes, stream);
+    if (rc) return rc;
+    rc = moe_reverse_dispatch(at<void>(ws, pl.da), saved->inv, saved->idx, at<float>(ws, pl.dlogit),
+                              w_router, shape, dx, ws, workspace_bytes, stream);
+    if (rc) return rc;
+    return moe_router_wgrad(x, saved->sched, saved->offsets, at<float>(ws, pl.slot_dlogit), shape,
+                            dw_router, dbias, ws, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -36,11 +36,15 @@ namespace moe {
 
 // Tiles of one grouped GEMM over expert segments: expert-major, then N tile,
 // then M tile, so CTAs working on consecutive tiles share a weight tile in L2.
+template <int KIND, bool SAVE = false>
 struct ExpertTiles {
     static constexpr bool kDeps = false;        // inputs are always ready
+    static constexpr int kKinds = 1 << KIND;    // the one tile kind of this launch
+    static constexpr bool kSaveUV = SAVE;       // GEMM1 also stores u|v (training)
+    static constexpr int kind = KIND;
     const int32_t* offsets;   // [E+1]
     const int32_t* mpre;      // [E+1] prefix of ceil(count_e / 128), in shared memory
-    int E, n_tiles, kind, total;
+    int E, n_tiles, total;
     __device__ int first() const { return blockIdx.x; }
     __device__ int next(int t) const { return t + gridDim.x; }
     __device__ int count() const { return total; }
@@ -70,7 +74,7 @@ struct ExpertTiles {
     __device__ void tile_stored(const TileInfo&, const Pipe&) const {}
 };
 
-template <bool MX, int KIND>
+template <bool MX, int KIND, bool SAVE>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmSFA,
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         if (lane == 31) mpre[E] = incl;
     }
     __syncthreads();
-    ExpertTiles src{offsets, mpre, E, side.n_tiles, KIND, mpre[E] * side.n_tiles};
+    ExpertTiles<KIND, SAVE> src{offsets, mpre, E, side.n_tiles, mpre[E] * side.n_tiles};
     const GemmMaps maps{&tmA, &tmA, &tmSFA, &tmSFA};
     const GemmSides sides{&side, &side};
     run_gemm_pipeline<MX>(smem, maps, sides, src, ws, timeout_ns);
@@ -111,11 +115,11 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 // ------------------------------------------------------------------ host side
 inline size_t gemm_smem_bytes(int E) { return 1024 + tc::OFF_TAIL + sizeof(int32_t) * (E + 1); }
 
-template <bool MX, int KIND>
+template <bool MX, int KIND, bool SAVE = false>
 static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tsa, const GemmSide& side,
                               const int32_t* offsets, int E, WsHeader* ws,
                               unsigned long long timeout_ns, int grid, cudaStream_t stream) {
-    auto kern = tc_grouped_gemm_kernel<MX, KIND>;
+    auto kern = tc_grouped_gemm_kernel<MX, KIND, SAVE>;
     const size_t smem = gemm_smem_bytes(E);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
@@ -164,7 +168,9 @@ bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2)
     s1->out = (uint8_t*)c.h;
     s1->out_sf = (uint8_t*)c.h_sf;
     s1->out_ld = c.I;
+    s1->aux = (uint8_t*)c.uv;
     *s2 = *s1;
+    s2->aux = nullptr;
     s2->K = c.I;
     s2->n_tiles = c.H / tc::BN;
     s2->up_off = 0;
@@ -193,13 +199,81 @@ cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream) {
     if (!encode_ffn_maps(c, &m, &s1, &s2)) return cudaErrorInvalidValue;
     cudaError_t err;
     if (c.mx) {
-        err = launch_one<true, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = c.uv ? launch_one<true, 0, true>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                   : launch_one<true, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
         err = launch_one<true, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     } else {
-        err = launch_one<false, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = c.uv ? launch_one<false, 0, true>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                   : launch_one<false, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
         err = launch_one<false, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+    }
+    return err;
+}
+
+// ------------------------------------------------------------- backward (dgrad)
+// dgrad of GEMM2 (kind 2): dh = dy . W_down over A = dy [rows][H] (K = H) and the
+// transposed-packed W_down (N = I, padded to 256-column tiles), epilogue = SwiGLU
+// backward -> du|dv.  dgrad of GEMM1 (kind 1): da = [du dv] . [W_gate; W_up] over
+// A = du|dv [rows][2I] (K = 2I) and the transposed-packed W_gate_up (N = H).
+cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
+    if (c.T == 0) return cudaSuccess;
+    const bool mx = c.mx;
+    const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t esz = mx ? 1 : 2;
+    const uint32_t bk = mx ? 128 : 64;
+    CUtensorMap m_dy, m_duv, s_dy = CUtensorMap{}, s_duv = CUtensorMap{};
+    {
+        uint64_t dims[2] = {(uint64_t)c.H, (uint64_t)c.a_rows};
+        uint64_t str[1] = {(uint64_t)c.H * esz};
+        uint32_t box[2] = {bk, 128};
+        if (!encode_tmap(&m_dy, dt, 2, c.dy, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    const void* a1 = mx ? c.duv_q : c.duv;
+    {
+        uint64_t dims[2] = {(uint64_t)(2 * c.I), (uint64_t)c.a_rows};
+        uint64_t str[1] = {(uint64_t)(2 * c.I) * esz};
+        uint32_t box[2] = {bk, 128};
+        if (!encode_tmap(&m_duv, dt, 2, a1, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    GemmSide s2{};   // dgrad of GEMM2
+    s2.K = c.H;
+    s2.n_tiles = (c.I + tc::BN - 1) / tc::BN;
+    s2.a_rows = c.a_rows;
+    s2.a_sf = (const uint8_t*)c.dy_sf;
+    s2.b_pk = (const uint8_t*)c.wt_down;
+    s2.sfb_pk = (const uint8_t*)c.wt_d_sf;
+    s2.out = (uint8_t*)c.duv;
+    s2.out_ld = 2 * c.I;
+    s2.aux = (uint8_t*)c.uv;
+    s2.out2 = (uint8_t*)c.duv_q;
+    s2.out2_sf = (uint8_t*)c.duv_sf;
+    s2.n_valid = c.I;
+    GemmSide s1{};   // dgrad of GEMM1
+    s1.K = 2 * c.I;
+    s1.n_tiles = c.H / tc::BN;
+    s1.a_rows = c.a_rows;
+    s1.a_sf = (const uint8_t*)c.duv_sf;
+    s1.b_pk = (const uint8_t*)c.wt_gate_up;
+    s1.sfb_pk = (const uint8_t*)c.wt_gu_sf;
+    s1.out = (uint8_t*)c.da;
+    s1.out_ld = c.H;
+    if (mx) {
+        s2.sf_tma = (c.H % 512) == 0;
+        s1.sf_tma = ((2 * c.I) % 512) == 0;
+        if (s2.sf_tma && !encode_sfa_map(&s_dy, c.dy_sf, c.a_rows, c.H)) return cudaErrorInvalidValue;
+        if (s1.sf_tma && !encode_sfa_map(&s_duv, c.duv_sf, c.a_rows, 2 * c.I)) return cudaErrorInvalidValue;
+    }
+    cudaError_t err;
+    if (mx) {
+        err = launch_one<true, 2>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        if (err != cudaSuccess) return err;
+        err = launch_one<true, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+    } else {
+        err = launch_one<false, 2>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        if (err != cudaSuccess) return err;
+        err = launch_one<false, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     }
     return err;
 }

@@ -60,12 +60,54 @@ struct TcFfnCall {
     void* h;                  // [a_rows][I] scratch
     void* h_sf;               // [a_rows][I/32] scratch (MXFP8)
     void* y;                  // [a_rows][H] BF16
+    void* uv;                 // training: u|v saved as BF16 [a_rows][2I], or null
     WsHeader* ws;
     unsigned long long timeout_ns;
     int grid;                 // persistent CTAs (one per SM)
 };
 
 cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream);
+
+// Backward of the tensor-core expert FFN: the two dgrad GEMMs.
+struct TcDgradCall {
+    bool mx;
+    int T, H, I, E;
+    int a_rows;               // rows of dy / uv / duv / da (>= T)
+    const void* dy;           // [a_rows][H] (codes or BF16)
+    const void* dy_sf;        // [a_rows][H/32] (MXFP8)
+    const void* uv;           // [a_rows][2I] BF16 saved by the forward
+    const int32_t* offsets;   // [E+1]
+    const void* wt_down;      // transposed-packed W_down (N = I padded to 256)
+    const void* wt_d_sf;
+    const void* wt_gate_up;   // transposed-packed W_gate_up (N = H, K = 2I)
+    const void* wt_gu_sf;
+    void* duv;                // [a_rows][2I] BF16 (out)
+    void* duv_q;              // [a_rows][2I] codes (MXFP8, out)
+    void* duv_sf;             // [a_rows][2I/32] (MXFP8, out)
+    void* da;                 // [a_rows][H] BF16 (out)
+    WsHeader* ws;
+    unsigned long long timeout_ns;
+    int grid;
+};
+cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream);
+
+// Backward memory-bound steps (backward.cu).
+constexpr int kRouterPiece = 256;   // slots per router-wgrad piece
+inline int router_max_pieces(int T, int E) { return T / kRouterPiece + E; }
+cudaError_t launch_pack_transposed(bool mx, const void* w, int E, int R, int C, void* dst,
+                                   uint8_t* dst_sf, int num_sms, cudaStream_t stream);
+cudaError_t launch_reverse_combine(bool mx, const void* dout, const void* y, const int32_t* inv,
+                                   const float* gate, int N, int H, int k, int T, void* dy,
+                                   uint8_t* dy_sf, float* dgate, float* dlogit, float* slot_gate,
+                                   float* slot_dlogit, int num_sms, WsHeader* ws, cudaStream_t stream);
+cudaError_t launch_reverse_dispatch(const void* da, const int32_t* inv, const int32_t* idx,
+                                    const float* dlogit, const void* w_router, int N, int H, int k,
+                                    int T, int E, void* dx, int num_sms, WsHeader* ws,
+                                    cudaStream_t stream);
+cudaError_t launch_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets,
+                                const float* slot_dlogit, int N, int H, int E, int T,
+                                int rows_per_shard, float* dw, float* db, float* part, float* part_b,
+                                int32_t* ppre, WsHeader* ws, cudaStream_t stream);
 
 // One-time repacking of natural K-major expert weights into tile images.
 struct PackCall {

@@ -29,9 +29,27 @@ def quantize_mxfp8(t: torch.Tensor):
     return codes, scales
 
 
+def pack_expert_weights_dgrad(shape, wgu: torch.Tensor, wd: torch.Tensor):
+    """Transposed tile-packed copies of the BF16 master weights for the backward's
+    dgrad GEMMs (MXFP8-quantised along their new K for the MXFP8 dtype), made by
+    libmoe.  Returns (gate_up_t, gate_up_t_scales, down_t, down_t_scales)."""
+    mx = shape.dtype == M.MOE_MXFP8
+    E, H, I = shape.E, shape.H, shape.I
+    Ip = (I + 255) // 256 * 256
+    esz = 1 if mx else 2
+    dev = wgu.device
+    p_gu = torch.empty(E * H * 2 * I * esz, dtype=torch.uint8, device=dev)
+    p_d = torch.empty(E * Ip * H * esz, dtype=torch.uint8, device=dev)
+    p_gu_sf = torch.empty(E * H * 2 * I // 32, dtype=torch.uint8, device=dev) if mx else None
+    p_d_sf = torch.empty(E * Ip * H // 32, dtype=torch.uint8, device=dev) if mx else None
+    M.moe_pack_expert_weights_dgrad(shape, wgu.contiguous(), wd.contiguous(), p_gu, p_gu_sf, p_d,
+                                    p_d_sf)
+    return p_gu, p_gu_sf, p_d, p_d_sf
+
+
 class MoeLayer:
     def __init__(self, w: Workload, inputs: dict, params: M.Params | None = None,
-                 device: str = "cuda", keep_master: bool = False):
+                 device: str = "cuda", keep_master: bool = False, train: bool = False):
         self.w = w
         self.shape = M.Shape.of(w)
         self.params = params
@@ -49,6 +67,28 @@ class MoeLayer:
         self.wgu, self.wgu_sf, self.wd, self.wd_sf = pack_expert_weights(
             self.shape, q_gu, q_gu_sf, q_d, q_d_sf)
         del q_gu, q_gu_sf, q_d, q_d_sf
+        self.train = train
+        if train:
+            self.wgu_t, self.wgu_t_sf, self.wd_t, self.wd_t_sf = pack_expert_weights_dgrad(
+                self.shape, wgu, wd)
+            T = w.T
+            i32 = torch.int32
+            self.saved = {
+                "idx": torch.empty((w.N, w.k), dtype=i32, device=dev),
+                "gate": torch.empty((w.N, w.k), dtype=torch.float32, device=dev),
+                "inv": torch.empty((w.N, w.k), dtype=i32, device=dev),
+                "offsets": torch.empty(w.E + 1, dtype=i32, device=dev),
+                "sched": torch.empty((T, 2), dtype=i32, device=dev),
+                "y": torch.empty((T, w.H), dtype=torch.bfloat16, device=dev),
+                "uv": torch.empty((T, 2 * w.I), dtype=torch.bfloat16, device=dev),
+            }
+            self.saved_c = M.Saved.of(self.saved)
+            self.bws = torch.empty(M.moe_backward_workspace_bytes(self.shape), dtype=torch.uint8,
+                                   device=dev)
+            M.moe_workspace_init(self.bws)
+            self.dx = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
+            self.dw_router = torch.empty((w.E, w.H), dtype=torch.float32, device=dev)
+            self.dbias = torch.empty(w.E, dtype=torch.float32, device=dev)
         if keep_master:
             self.master = (wgu, wd)
         else:
@@ -74,3 +114,22 @@ class MoeLayer:
 
     def device_status(self) -> int:
         return M.moe_last_device_status(self.ws)
+
+    def forward_train(self, x: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None):
+        """The staged forward, keeping the activations the backward needs."""
+        M.moe_forward_train(self.x if x is None else x, self.w_router, self.bias, self.wgu,
+                            self.wgu_sf, self.wd, self.wd_sf, self.shape, self.params,
+                            self.out if out is None else out, self.saved_c, self.ws, stream)
+        return self.out if out is None else out
+
+    def backward(self, dout: torch.Tensor, x: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None):
+        """Gradients of the last forward_train: (dx, dW_router, dbias)."""
+        M.moe_backward(dout, self.x if x is None else x, self.w_router, self.saved_c, self.wgu_t,
+                       self.wgu_t_sf, self.wd_t, self.wd_t_sf, self.shape, self.params, self.dx,
+                       self.dw_router, self.dbias, self.bws, stream)
+        return self.dx, self.dw_router, self.dbias
+
+    def backward_status(self) -> int:
+        return M.moe_last_device_status(self.bws)

@@ -27,7 +27,9 @@ ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_last_device_status", "moe_status_string",
     "moe_quantize_mxfp8", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
     "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
-    "moe_pack_expert_weights",
+    "moe_pack_expert_weights", "moe_backward_workspace_bytes", "moe_pack_expert_weights_dgrad",
+    "moe_expert_ffn_train", "moe_forward_train", "moe_reverse_combine", "moe_expert_ffn_dgrad",
+    "moe_reverse_dispatch", "moe_router_wgrad", "moe_backward",
 )
 
 
@@ -53,6 +55,18 @@ class Params(ctypes.Structure):
                 ("timeout_ns", ctypes.c_longlong), ("test_skip_ready", ctypes.c_int)]
 
 
+class Saved(ctypes.Structure):
+    """moe_saved_t: device pointers of the activations the backward reads."""
+    _fields_ = [("idx", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("inv", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("sched", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("uv", ctypes.c_void_p)]
+
+    @classmethod
+    def of(cls, t: dict) -> "Saved":
+        """From a dict of tensors with the field names as keys."""
+        return cls(*(t[f].data_ptr() for f, _ in cls._fields_))
+
+
 def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(f"libmoe.so not built at {path}; run token_dispatch_expert_top_gb300.build")
@@ -61,7 +75,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
 
 _lib = load_library()
 _vp, _i, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
-_shp, _prm = ctypes.POINTER(Shape), ctypes.POINTER(Params)
+_shp, _prm, _svd = ctypes.POINTER(Shape), ctypes.POINTER(Params), ctypes.POINTER(Saved)
 _SIGS = {
     "moe_workspace_bytes": (_sz, [_shp, _prm]),
     "moe_workspace_init": (_i, [_vp, _sz, _vp]),
@@ -79,6 +93,19 @@ _SIGS = {
     "moe_min_minibatch": (_i, [_i, _i, _i, _i, _i]),
     "moe_layout_noalloc": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp]),
     "moe_pack_expert_weights": (_i, [_shp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_backward_workspace_bytes": (_sz, [_shp]),
+    "moe_pack_expert_weights_dgrad": (_i, [_shp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_expert_ffn_train": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_forward_train": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _prm, _vp, _svd, _vp, _sz,
+                               _vp]),
+    "moe_reverse_combine": (_i, [_vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                 _vp]),
+    "moe_expert_ffn_dgrad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _vp,
+                                  _vp, _sz, _vp]),
+    "moe_reverse_dispatch": (_i, [_vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _sz, _vp]),
+    "moe_router_wgrad": (_i, [_vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_backward": (_i, [_vp, _vp, _vp, _svd, _vp, _vp, _vp, _vp, _shp, _prm, _vp, _vp, _vp, _vp,
+                          _sz, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -209,3 +236,69 @@ def moe_layout_noalloc(idx, shape: Shape, counts, offsets, sched, inv, stream=No
     library's fixed device scratch array is used instead (see include/moe.h)."""
     _check("moe_layout_noalloc", _lib.moe_layout_noalloc(
         _p(idx), ctypes.byref(shape), _p(counts), _p(offsets), _p(sched), _p(inv), _stream(stream)))
+
+
+# ------------------------------------------------------------------ backward
+def moe_backward_workspace_bytes(shape: Shape) -> int:
+    return _lib.moe_backward_workspace_bytes(ctypes.byref(shape))
+
+
+def moe_pack_expert_weights_dgrad(shape: Shape, w_gate_up, w_down, packed_gate_up_t,
+                                  packed_gu_t_scales, packed_down_t, packed_d_t_scales,
+                                  stream=None) -> None:
+    _check("moe_pack_expert_weights_dgrad", _lib.moe_pack_expert_weights_dgrad(
+        ctypes.byref(shape), _p(w_gate_up), _p(w_down), _p(packed_gate_up_t),
+        _p(packed_gu_t_scales), _p(packed_down_t), _p(packed_d_t_scales), _stream(stream)))
+
+
+def moe_expert_ffn_train(a, a_scales, offsets, w_gate_up, w_gu_scales, w_down, w_d_scales,
+                         shape: Shape, y, uv, ws, stream=None) -> None:
+    _check("moe_expert_ffn_train", _lib.moe_expert_ffn_train(
+        _p(a), _p(a_scales), _p(offsets), _p(w_gate_up), _p(w_gu_scales), _p(w_down),
+        _p(w_d_scales), ctypes.byref(shape), _p(y), _p(uv), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_forward_train(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales,
+                      shape: Shape, params: Params | None, out, saved: Saved, ws,
+                      stream=None) -> None:
+    _check("moe_forward_train", _lib.moe_forward_train(
+        _p(x), _p(w_router), _p(bias), _p(w_gate_up), _p(w_gu_scales), _p(w_down), _p(w_d_scales),
+        ctypes.byref(shape), ctypes.byref(params) if params else None, _p(out),
+        ctypes.byref(saved), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_reverse_combine(dout, y, inv, gate, shape: Shape, dy, dy_scales, dgate, dlogit,
+                        slot_gate, slot_dlogit, ws, stream=None) -> None:
+    _check("moe_reverse_combine", _lib.moe_reverse_combine(
+        _p(dout), _p(y), _p(inv), _p(gate), ctypes.byref(shape), _p(dy), _p(dy_scales),
+        _p(dgate), _p(dlogit), _p(slot_gate), _p(slot_dlogit), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_expert_ffn_dgrad(dy, dy_scales, uv, offsets, wt_gate_up, wt_gu_scales, wt_down,
+                         wt_d_scales, shape: Shape, duv, duv_codes, duv_scales, da, ws,
+                         stream=None) -> None:
+    _check("moe_expert_ffn_dgrad", _lib.moe_expert_ffn_dgrad(
+        _p(dy), _p(dy_scales), _p(uv), _p(offsets), _p(wt_gate_up), _p(wt_gu_scales),
+        _p(wt_down), _p(wt_d_scales), ctypes.byref(shape), _p(duv), _p(duv_codes),
+        _p(duv_scales), _p(da), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_reverse_dispatch(da, inv, idx, dlogit, w_router, shape: Shape, dx, ws, stream=None) -> None:
+    _check("moe_reverse_dispatch", _lib.moe_reverse_dispatch(
+        _p(da), _p(inv), _p(idx), _p(dlogit), _p(w_router), ctypes.byref(shape), _p(dx), _p(ws),
+        _wsz(ws), _stream(stream)))
+
+
+def moe_router_wgrad(x, sched, offsets, slot_dlogit, shape: Shape, dw_router, dbias, ws,
+                     stream=None) -> None:
+    _check("moe_router_wgrad", _lib.moe_router_wgrad(
+        _p(x), _p(sched), _p(offsets), _p(slot_dlogit), ctypes.byref(shape), _p(dw_router),
+        _p(dbias), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_backward(dout, x, w_router, saved: Saved, wt_gate_up, wt_gu_scales, wt_down, wt_d_scales,
+                 shape: Shape, params: Params | None, dx, dw_router, dbias, ws, stream=None) -> None:
+    _check("moe_backward", _lib.moe_backward(
+        _p(dout), _p(x), _p(w_router), ctypes.byref(saved), _p(wt_gate_up), _p(wt_gu_scales),
+        _p(wt_down), _p(wt_d_scales), ctypes.byref(shape), ctypes.byref(params) if params else None,
+        _p(dx), _p(dw_router), _p(dbias), _p(ws), _wsz(ws), _stream(stream)))
