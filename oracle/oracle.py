@@ -344,6 +344,24 @@ BWD_FORMATS = {
 }
 
 
+# Format of the wgrad GEMM operands (quantised along the expert's slots, which
+# those GEMMs reduce over) and of the weight gradients; None: the exact
+# straight-through formulas on the forward's own values.
+WGRAD_FORMATS = {"f64": None, "f32": None, "bf16": "bf16", "mxfp8": "mxfp8"}
+
+
+def round_along_slots(m: np.ndarray, fmt: str) -> np.ndarray:
+    """Round the rows of one expert's slot segment [slots, C] as a wgrad operand:
+    MXFP8 blocks of 32 consecutive slots from the segment's first slot (the last
+    block zero-padded), or element-wise for the other formats."""
+    if fmt != "mxfp8":
+        return round_to(m, fmt)
+    R = m.shape[0]
+    pad = (-R) % 32
+    mp = np.vstack([m, np.zeros((pad, m.shape[1]))]) if pad else m
+    return np.ascontiguousarray(mxfp8_values(np.ascontiguousarray(mp.T)).T[:R])
+
+
 def expert_operands_dgrad(w_gate_up_e, w_down_e, dtype: str):
     """FP64 values of one expert's weights as the dgrad GEMMs see them: (Wg [I,H],
     Wu [I,H], Wd [H,I]) with the reduction running over I (gate/up) and over H
@@ -359,7 +377,7 @@ def expert_operands_dgrad(w_gate_up_e, w_down_e, dtype: str):
 
 
 def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray,
-                        dy: np.ndarray, dtype: str, wb=None) -> dict:
+                        dy: np.ndarray, dtype: str, wb=None, a_master=None) -> dict:
     """Backward of one expert's SwiGLU FFN over its rows a, given dy = dL/dy.
 
     Forward as ``expert_ffn``: u = a Wg^T, v = a Wu^T, h = round_h(silu(u) v),
@@ -369,7 +387,13 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
       dWg = du^T a,  dWu = dv^T a,  dWd = dy^T h   (h after its rounding),
     where _b marks a dgrad GEMM operand in its storage format (BWD_FORMATS; the
     weights ``wb`` = expert_operands_dgrad, default the forward's values) and
-    u_s, v_s the kept pre-activations.  For "f64" nothing is rounded and this is
+    u_s, v_s the kept pre-activations.  With a wgrad format (WGRAD_FORMATS) the
+    weight gradients are GEMMs over the slots too, each operand rounded along the
+    slots (round_along_slots) and the result rounded to BF16:
+      dWg = (du_s)^T a_w,  dWu = (dv_s)^T a_w,  dWd = (dy)^T h_w
+    with du_s, dv_s the BF16 copies of du, dv, a_w the master rows a_master (x,
+    unquantised), h_w = silu(u_s) v_s recomputed from the kept u|v, every one of
+    them then rounded along the slots.  For "f64" nothing is rounded and this is
     the exact derivative.
     Returns dict(u, v, h, y, dh, du, dv, da, dwg, dwu, dwd)."""
     _, fmt_h, fmt_y, _ = FORMATS[dtype]
@@ -379,11 +403,21 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     v = a @ wu.T
     h = round_to(swiglu(u, v), fmt_h)
     y = round_to(h @ wd.T, fmt_y)
+    u_s, v_s = round_to(u, f_uv), round_to(v, f_uv)
     dh = round_to(dy, f_dy) @ wd_b
-    du, dv = swiglu_backward(round_to(u, f_uv), round_to(v, f_uv), dh)
+    du, dv = swiglu_backward(u_s, v_s, dh)
     da = round_to(round_to(du, f_duv) @ wg_b + round_to(dv, f_duv) @ wu_b, f_da)
-    return dict(u=u, v=v, h=h, y=y, dh=dh, du=du, dv=dv, da=da, dwg=du.T @ a, dwu=dv.T @ a,
-                dwd=dy.T @ h)
+    f_w = WGRAD_FORMATS[dtype]
+    if f_w is None:
+        dwg, dwu, dwd = du.T @ a, dv.T @ a, dy.T @ h
+    else:
+        q = lambda m: round_along_slots(m, f_w)
+        a_w = q(a if a_master is None else a_master)
+        h_w = q(swiglu(u_s, v_s))
+        dwg = round_bf16(q(round_bf16(du)).T @ a_w)
+        dwu = round_bf16(q(round_bf16(dv)).T @ a_w)
+        dwd = round_bf16(q(dy).T @ h_w)
+    return dict(u=u, v=v, h=h, y=y, dh=dh, du=du, dv=dv, da=da, dwg=dwg, dwu=dwu, dwd=dwd)
 
 
 def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, experts=None,
@@ -469,7 +503,7 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
         wg, wu, wd = weights(int(e)) if weights is not None else expert_operands(
             inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
         wb = expert_operands_dgrad(inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
-        r = expert_ffn_backward(a, wg, wu, wd, dy[sel], dtype, wb)
+        r = expert_ffn_backward(a, wg, wu, wd, dy[sel], dtype, wb, x[ptok[sel]])
         dgate_p[sel] = np.einsum("ph,ph->p", dY[ptok[sel]], r["y"])
         dh[sel], du[sel], dv[sel], da[sel] = r["dh"], r["du"], r["dv"], r["da"]
         if int(e) in exp_pos:

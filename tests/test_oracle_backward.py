@@ -173,7 +173,8 @@ def test_euler_identity_for_the_linear_weights(dtype):
                         for e in range(E)])
     s_d = float(np.sum(b["dw_down"] * wd_vals))
     s_u = float(np.sum(b["dw_gate_up"][:, I:] * wu_vals))
-    tol = 1e-10 if dtype == "f64" else (1e-5 if dtype == "f32" else 2e-2)
+    # the wgrad GEMMs round dy and h along the slots (MXFP8 blocks of 32 slots)
+    tol = {"f64": 1e-10, "f32": 1e-5, "bf16": 2e-2, "mxfp8": 6e-2}[dtype]
     assert abs(s_d - L) <= tol * max(1.0, abs(L)), (s_d, L)
     # W_up feeds h, which is rounded before the down GEMM: exact only without rounding
     tol_u = 1e-10 if dtype == "f64" else (1e-5 if dtype == "f32" else 6e-2)
@@ -261,3 +262,20 @@ def test_subsets_agree_with_the_full_backward():
     for i, p in enumerate(part["pairs"]):
         j = int(np.nonzero(full["pairs"] == p)[0][0])
         np.testing.assert_allclose(part["da"][i], full["da"][j], rtol=1e-13, atol=1e-14)
+
+
+def test_round_along_slots_blocks_start_at_the_segment():
+    """MXFP8 wgrad operands: blocks of 32 slots from the segment's first slot; the
+    last, partial block is scaled by its own rows only; other formats round
+    element-wise."""
+    rng = np.random.default_rng(19)
+    m = rng.standard_normal((40, 6)) * np.exp2(rng.integers(-8, 8, size=(40, 1)))
+    q = O.round_along_slots(m, "mxfp8")
+    np.testing.assert_array_equal(q[:32], O.mxfp8_values(m[:32].T).T)
+    tail = np.vstack([m[32:], np.zeros((24, 6))])
+    np.testing.assert_array_equal(q[32:], O.mxfp8_values(tail.T).T[:8])
+    # a power-of-two column is exact; a block's scale follows its own amax
+    m2 = np.zeros((32, 1))
+    m2[5, 0] = 2.0 ** -20
+    np.testing.assert_array_equal(O.round_along_slots(m2, "mxfp8"), m2)
+    np.testing.assert_array_equal(O.round_along_slots(m, "bf16"), O.round_bf16(m))
