@@ -311,7 +311,8 @@ typedef struct {
 } moe_saved_t;
 
 /* Bytes of workspace the backward entry points need (dy, du|dv, da, gate and
- * logit gradients, router-gradient partial sums).  0 for an invalid shape.  The
+ * logit gradients, router-gradient partial sums, the weight-gradient operand
+ * images).  0 for an invalid shape.  The
  * first 256 bytes are the status header, as for moe_workspace_bytes(). */
 size_t moe_backward_workspace_bytes(const moe_shape_t* shape);
 
@@ -411,17 +412,37 @@ int moe_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets
                      const float* slot_dlogit, const moe_shape_t* shape, float* dw_router,
                      float* dbias, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Expert weight gradients: for every expert e, GEMMs that reduce over its slots
+ * [offsets[e], offsets[e+1]) on tcgen05,
+ *   dW_gate_up[e] = [du dv]^T . x[token(s)]     dW_down[e] = (g * dout[token(s)])^T . h
+ * with h = silu(u) * v recomputed from the kept u|v, FP32 accumulation, BF16
+ * results; an expert without slots gets zeros.  Each operand is first transposed
+ * into K-major tile images over the slot axis (each expert's slots padded to 128
+ * with zeros); MXFP8 quantises it along the slots, in blocks of 32 from the
+ * expert's first slot (the block-scaled MMA reduces along its K).
+ *   duv : [T][2I] BF16 (moe_expert_ffn_dgrad);  x, dout : [N][H] BF16;
+ *   uv : moe_saved_t.uv;  sched, offsets : moe_layout;  slot_gate : [T] FP32
+ *   (moe_reverse_combine)
+ *   dw_gate_up : [E][2I][H] BF16 (rows as w_gate_up), dw_down : [E][H][I] BF16,
+ *   both 32-byte aligned                                                    (out)
+ * Needs moe_backward_workspace_bytes() of workspace. */
+int moe_expert_wgrad(const void* duv, const void* x, const void* dout, const void* uv,
+                     const int32_t* sched, const float* slot_gate, const int32_t* offsets,
+                     const moe_shape_t* shape, void* dw_gate_up, void* dw_down, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* The backward of the layer, one kernel per step on `stream`: reverse combine,
- * expert dgrad, reverse dispatch, router gradient.
+ * expert dgrad, reverse dispatch, router gradient, expert weight gradients.
  *   dout : [N][H] BF16;  x, w_router : the forward's inputs;  saved : filled by
  *   moe_forward_train;  wt_* : moe_pack_expert_weights_dgrad's output
- *   dx : [N][H] BF16;  dw_router : [E][H] FP32;  dbias : [E] FP32 or NULL  (out)
+ *   dx : [N][H] BF16;  dw_router : [E][H] FP32;  dbias : [E] FP32 or NULL;
+ *   dw_gate_up, dw_down : as moe_expert_wgrad, or both NULL to skip them  (out)
  * Needs moe_backward_workspace_bytes() of workspace. */
 int moe_backward(const void* dout, const void* x, const void* w_router, const moe_saved_t* saved,
                  const void* wt_gate_up, const uint8_t* wt_gu_scales, const void* wt_down,
                  const uint8_t* wt_d_scales, const moe_shape_t* shape, const moe_params_t* params,
-                 void* dx, float* dw_router, float* dbias, void* workspace, size_t workspace_bytes,
-                 void* stream);
+                 void* dx, float* dw_router, float* dbias, void* dw_gate_up, void* dw_down,
+                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* Smallest minibatch (in slots) that gives `waves` full waves of GEMM1 tiles of
  * tile_m x tile_n over `compute_sms` SMs when GEMM1 has 2*I output columns

@@ -407,17 +407,25 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     dh = round_to(dy, f_dy) @ wd_b
     du, dv = swiglu_backward(u_s, v_s, dh)
     da = round_to(round_to(du, f_duv) @ wg_b + round_to(dv, f_duv) @ wu_b, f_da)
-    f_w = WGRAD_FORMATS[dtype]
-    if f_w is None:
+    if WGRAD_FORMATS[dtype] is None:
         dwg, dwu, dwd = du.T @ a, dv.T @ a, dy.T @ h
     else:
-        q = lambda m: round_along_slots(m, f_w)
-        a_w = q(a if a_master is None else a_master)
-        h_w = q(swiglu(u_s, v_s))
-        dwg = round_bf16(q(round_bf16(du)).T @ a_w)
-        dwu = round_bf16(q(round_bf16(dv)).T @ a_w)
-        dwd = round_bf16(q(dy).T @ h_w)
+        dwg, dwu, dwd = expert_wgrad(a if a_master is None else a_master, round_bf16(du),
+                                     round_bf16(dv), dy, u_s, v_s, dtype)
     return dict(u=u, v=v, h=h, y=y, dh=dh, du=du, dv=dv, da=da, dwg=dwg, dwu=dwu, dwd=dwd)
+
+
+def expert_wgrad(a: np.ndarray, du: np.ndarray, dv: np.ndarray, dy: np.ndarray, u: np.ndarray,
+                 v: np.ndarray, dtype: str):
+    """One expert's weight gradients as GEMMs over its slots (rows in slot order):
+      dWg = du^T a,  dWu = dv^T a,  dWd = dy^T h,  h = silu(u) v,
+    every operand rounded along the slots in the wgrad format (round_along_slots)
+    and each result rounded to BF16.  a: master x rows; du, dv, u, v: the values
+    as stored (BF16 copies); dy: g * dout."""
+    q = lambda m: round_along_slots(m, WGRAD_FORMATS[dtype])
+    a_w = q(a)
+    h_w = q(swiglu(u, v))
+    return (round_bf16(q(du).T @ a_w), round_bf16(q(dv).T @ a_w), round_bf16(q(dy).T @ h_w))
 
 
 def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, experts=None,

@@ -277,7 +277,7 @@ def test_backward_layer_matches_oracle(M, w):
     layer = MoeLayer(w, inp, train=True)
     dout = torch.randn((w.N, w.H), generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
     layer.forward_train()
-    dx, dwr, db = layer.backward(dout.cuda())
+    dx, dwr, db, dwgu, dwd = layer.backward(dout.cuda())
     assert layer.device_status() == 0 and layer.backward_status() == 0
     ref = O.backward(inp, w.E, w.k, w.S, w.dtype, dout)
     np.testing.assert_array_equal(to_np(layer.saved["idx"]), ref["idx"])
@@ -291,8 +291,68 @@ def test_backward_layer_matches_oracle(M, w):
     assert err_wr.max() < tol, err_wr.max()
     assert np.all(to_np(dwr)[~used] == 0.0)
     assert np.abs(to_np(db) - ref["dbias"]).max() < tol * np.abs(ref["dbias"]).max()
+    # expert weight gradients: every row of every expert with slots; zeros otherwise
+    g_gu, g_d = to_np(dwgu), to_np(dwd)
+    err_w = max(row_rel_err(g_gu[used].reshape(-1, w.H), ref["dw_gate_up"][used].reshape(-1, w.H)).max(),
+                row_rel_err(g_d[used].reshape(-1, w.I), ref["dw_down"][used].reshape(-1, w.I)).max())
+    assert err_w < tol, err_w
+    assert np.all(g_gu[~used] == 0.0) and np.all(g_d[~used] == 0.0)
     # deterministic: a second backward is bitwise identical
-    dx1, dwr1, db1 = dx.clone(), dwr.clone(), db.clone()
+    dx1, dwr1, db1, gu1, d1 = dx.clone(), dwr.clone(), db.clone(), dwgu.clone(), dwd.clone()
     layer.backward(dout.cuda())
     assert torch.equal(dx1, layer.dx) and torch.equal(dwr1, layer.dw_router)
     assert torch.equal(db1, layer.dbias)
+    assert torch.equal(gu1, layer.dw_gate_up) and torch.equal(d1, layer.dw_down)
+
+
+# ------------------------------------------------------------------ expert wgrad
+WGRAD_CASES = [
+    # dtype, N, H, I, E, k, hot (an expert every token picks), empty expert
+    ("mxfp8", 300, 512, 256, 6, 2, 1, 4),
+    ("bf16", 200, 512, 384, 4, 2, None, 2),
+    ("mxfp8", 64, 7168, 2048, 4, 2, None, None),
+]
+
+
+@pytest.mark.parametrize("dtype,N,H,I,E,k,hot,empty", WGRAD_CASES,
+                         ids=[f"{c[0]}-H{c[2]}-I{c[3]}-E{c[4]}" for c in WGRAD_CASES])
+def test_expert_wgrad_matches_oracle(M, dtype, N, H, I, E, k, hot, empty):
+    rng = np.random.default_rng(51)
+    S = 2
+    w = synth.Workload("wg", N=N, H=H, I=I, E=E, k=k, S=S, dtype=dtype)
+    shape = M.Shape.of(w)
+    ws = _bws(M, shape)
+    T = N * k
+    idx = np.empty((N, k), dtype=np.int32)
+    pool = [e for e in range(E) if e != empty]
+    for n in range(N):
+        idx[n] = rng.choice(pool, size=k, replace=False)
+        if hot is not None and hot not in idx[n]:
+            idx[n, -1] = hot
+    counts, offsets_np, sched_np, _ = O.layout(idx, E, S)
+    gen = torch.Generator().manual_seed(6)
+    x = torch.randn((N, H), generator=gen).to(torch.bfloat16)
+    dout = torch.randn((N, H), generator=gen).to(torch.bfloat16)
+    uv = (torch.randn((T, 2 * I), generator=gen) * 2).to(torch.bfloat16)
+    duv = (torch.randn((T, 2 * I), generator=gen) * 0.1).to(torch.bfloat16)
+    sg = (rng.random(T) * 0.9 + 0.1).astype(np.float32)
+    dwgu = torch.full((E, 2 * I, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dwd = torch.full((E, H, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.moe_expert_wgrad(duv.cuda(), x.cuda(), dout.cuda(), uv.cuda(), torch.from_numpy(sched_np).cuda(),
+                       torch.from_numpy(sg).cuda(), torch.from_numpy(offsets_np).cuda(), shape, dwgu, dwd,
+                       ws)
+    assert M.moe_last_device_status(ws) == 0
+    tok = sched_np[:, 0] * (N // S) + sched_np[:, 1]
+    x64, d64, uv64, duv64 = O._f64(x), O._f64(dout), O._f64(uv), O._f64(duv)
+    g_gu, g_d = to_np(dwgu), to_np(dwd)
+    for e in range(E):
+        s = slice(offsets_np[e], offsets_np[e + 1])
+        if counts[e] == 0:
+            assert np.all(g_gu[e] == 0.0) and np.all(g_d[e] == 0.0)
+            continue
+        dy = sg[s].astype(np.float64)[:, None] * d64[tok[s]]
+        dwg, dwu, dwdn = O.expert_wgrad(x64[tok[s]], duv64[s, :I], duv64[s, I:], dy, uv64[s, :I],
+                                        uv64[s, I:], dtype)
+        err = max(row_rel_err(g_gu[e, :I], dwg).max(), row_rel_err(g_gu[e, I:], dwu).max(),
+                  row_rel_err(g_d[e], dwdn).max())
+        assert err < 2e-2, (e, counts[e], err)

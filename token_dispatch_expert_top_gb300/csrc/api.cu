@@ -131,7 +131,9 @@ T* at(void* ws, size_t off) {
 // Workspace regions of the backward entry points, in order.
 struct BwdPlan {
     size_t header, dy, dy_sf, duv, duv_q, duv_sf, da, dgate, dlogit, slot_gate, slot_dlogit;
-    size_t part, part_b, ppre, total;
+    size_t part, part_b, ppre;
+    size_t pstage, img_duv, sf_duv, img_x, sf_x, img_dy, sf_dy, img_h, sf_h;
+    size_t total;
 };
 
 BwdPlan make_bwd_plan(const moe_shape_t& s) {
@@ -159,6 +161,19 @@ BwdPlan make_bwd_plan(const moe_shape_t& s) {
     pl.part = take(sizeof(float) * pmax * s.H);
     pl.part_b = take(sizeof(float) * pmax);
     pl.ppre = take(sizeof(int32_t) * (s.E + 1));
+    // wgrad operand images over the padded slot axis
+    const size_t tp = (size_t)wgrad_max_padded_slots((int)T, s.E);
+    const size_t esz = mx ? 1 : 2;
+    const size_t Ip = (size_t)(s.I + 255) / 256 * 256;
+    pl.pstage = take(sizeof(int32_t) * (s.E + 1));
+    pl.img_duv = take(tp * 2 * s.I * esz);
+    pl.sf_duv = take(mx ? tp * 2 * s.I / 32 : 0);
+    pl.img_x = take(tp * s.H * esz);
+    pl.sf_x = take(mx ? tp * s.H / 32 : 0);
+    pl.img_dy = take(tp * s.H * esz);
+    pl.sf_dy = take(mx ? tp * s.H / 32 : 0);
+    pl.img_h = take(tp * Ip * esz);
+    pl.sf_h = take(mx ? tp * Ip / 32 : 0);
     pl.total = off;
     return pl;
 }
@@ -774,11 +789,60 @@ int moe_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets
                                            at<WsHeader>(workspace, pl.header), (cudaStream_t)stream));
 }
 
+int moe_expert_wgrad(const void* duv, const void* x, const void* dout, const void* uv,
+                     const int32_t* sched, const float* slot_gate, const int32_t* offsets,
+                     const moe_shape_t* shape, void* dw_gate_up, void* dw_down, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    int rc = check_bwd_shape(shape);
+    if (rc) return rc;
+    rc = check_bwd_ws(shape, workspace, workspace_bytes);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (!offsets || !dw_gate_up || !dw_down) return MOE_ERR_INVALID_ARG;
+    if (s.N > 0 && (!duv || !x || !dout || !uv || !sched || !slot_gate)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(duv) || !aligned16(x) || !aligned16(dout) || !aligned16(uv) ||
+        !aligned32(dw_gate_up) || !aligned32(dw_down))
+        return MOE_ERR_INVALID_ARG;
+    const BwdPlan pl = make_bwd_plan(s);
+    void* ws = workspace;
+    const bool mx = s.dtype == MOE_MXFP8;
+    WgradCall c{};
+    c.mx = mx;
+    c.N = s.N;
+    c.H = s.H;
+    c.I = s.I;
+    c.E = s.E;
+    c.T = s.N * s.k;
+    c.rows_per_shard = s.N / s.S;
+    c.duv = duv;
+    c.x = x;
+    c.dout = dout;
+    c.uv = uv;
+    c.sched = sched;
+    c.slot_gate = slot_gate;
+    c.offsets = offsets;
+    c.dw_gate_up = dw_gate_up;
+    c.dw_down = dw_down;
+    c.pstage = at<int32_t>(ws, pl.pstage);
+    c.img_duv = at<uint8_t>(ws, pl.img_duv);
+    c.sf_duv = mx ? at<uint8_t>(ws, pl.sf_duv) : nullptr;
+    c.img_x = at<uint8_t>(ws, pl.img_x);
+    c.sf_x = mx ? at<uint8_t>(ws, pl.sf_x) : nullptr;
+    c.img_dy = at<uint8_t>(ws, pl.img_dy);
+    c.sf_dy = mx ? at<uint8_t>(ws, pl.sf_dy) : nullptr;
+    c.img_h = at<uint8_t>(ws, pl.img_h);
+    c.sf_h = mx ? at<uint8_t>(ws, pl.sf_h) : nullptr;
+    c.ws = at<WsHeader>(ws, pl.header);
+    c.timeout_ns = kDefaultTimeoutNs;
+    c.grid = num_sms_current();
+    return cuda_status(launch_wgrad(c, (cudaStream_t)stream));
+}
+
 int moe_backward(const void* dout, const void* x, const void* w_router, const moe_saved_t* saved,
                  const void* wt_gate_up, const uint8_t* wt_gu_scales, const void* wt_down,
                  const uint8_t* wt_d_scales, const moe_shape_t* shape, const moe_params_t* params,
-                 void* dx, float* dw_router, float* dbias, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+                 void* dx, float* dw_router, float* dbias, void* dw_gate_up, void* dw_down,
+                 void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_bwd_shape(shape);
     if (rc) return rc;
     rc = check_bwd_ws(shape, workspace, workspace_bytes);
@@ -805,8 +869,13 @@ int moe_backward(const void* dout, const void* x, const void* w_router, const mo
     rc = moe_reverse_dispatch(at<void>(ws, pl.da), saved->inv, saved->idx, at<float>(ws, pl.dlogit),
                               w_router, shape, dx, ws, workspace_bytes, stream);
     if (rc) return rc;
-    return moe_router_wgrad(x, saved->sched, saved->offsets, at<float>(ws, pl.slot_dlogit), shape,
-                            dw_router, dbias, ws, workspace_bytes, stream);
+    rc = moe_router_wgrad(x, saved->sched, saved->offsets, at<float>(ws, pl.slot_dlogit), shape,
+                          dw_router, dbias, ws, workspace_bytes, stream);
+    if (rc || (!dw_gate_up && !dw_down)) return rc;
+    if (!dw_gate_up || !dw_down) return MOE_ERR_INVALID_ARG;
+    return moe_expert_wgrad(at<void>(ws, pl.duv), x, dout, saved->uv, saved->sched,
+                            at<float>(ws, pl.slot_gate), saved->offsets, shape, dw_gate_up, dw_down,
+                            ws, workspace_bytes, stream);
 }
 
 }  // extern "C"

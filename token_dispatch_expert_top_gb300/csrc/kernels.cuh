@@ -104,6 +104,40 @@ cudaError_t launch_reverse_dispatch(const void* da, const int32_t* inv, const in
                                     const float* dlogit, const void* w_router, int N, int H, int k,
                                     int T, int E, void* dx, int num_sms, WsHeader* ws,
                                     cudaStream_t stream);
+// Expert weight gradients (wgrad.cu).
+inline int wgrad_max_padded_slots(int T, int E) { return 128 * (T / 128 + E); }
+struct WgGemm {
+    const uint8_t* a_img;     // A operand images [K-stages][a_rb][16 KB]
+    const uint8_t* a_sf;      // MXFP8 scale images [K-stages of 128][a_rb][512]
+    int a_rb;
+    const uint8_t* b_img;
+    const uint8_t* b_sf;
+    int b_rb;
+    int m_tiles, n_tiles, n_valid;
+    uint8_t* out;             // BF16 [E][M][N]: out + e*out_estride + (row*out_ld + col)*2
+    int64_t out_estride;      // bytes
+    int out_ld;               // elements
+};
+struct WgradCall {
+    bool mx;
+    int N, H, I, E, T, rows_per_shard;
+    const void* duv;          // [T][2I] BF16
+    const void* x;            // [N][H] BF16
+    const void* dout;         // [N][H] BF16
+    const void* uv;           // [T][2I] BF16
+    const int32_t* sched;
+    const float* slot_gate;
+    const int32_t* offsets;
+    void* dw_gate_up;         // [E][2I][H] BF16 (out)
+    void* dw_down;            // [E][H][I] BF16 (out)
+    int32_t* pstage;          // [E+1] scratch
+    uint8_t *img_duv, *sf_duv, *img_x, *sf_x, *img_dy, *sf_dy, *img_h, *sf_h;   // scratch
+    WsHeader* ws;
+    unsigned long long timeout_ns;
+    int grid;
+};
+cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream);
+
 cudaError_t launch_router_wgrad(const void* x, const int32_t* sched, const int32_t* offsets,
                                 const float* slot_dlogit, int N, int H, int E, int T,
                                 int rows_per_shard, float* dw, float* db, float* part, float* part_b,

@@ -1,0 +1,489 @@
+// wgrad.cu -- the expert weight gradients of the backward pass: grouped GEMMs
+// whose reduction runs over each expert's slots, on the sm_103a tensor cores.
+//
+// For expert e with slots [offsets[e], offsets[e+1]):
+//   dW_gate_up[e] = [du dv]^T . a      ([2I x H]; a = the master x rows)
+//   dW_down[e]    = dy^T . h           ([H x I]; h = silu(u) v from the kept u|v)
+// written as BF16 master gradients (zeros for an expert without slots).
+// ([MoK-2.37x] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72", section 01: the backward's expert computation on Blackwell tensor
+// cores, grouped per expert like the forward's.)
+//
+// Operands.  A tcgen05 operand is K-major, so the slot-major rows (du|dv, x,
+// g*dout, u|v) are first transposed by `wgrad_pack_kernel` into tile images:
+// per operand matrix of R rows (R padded to 256) and the padded slot axis (each
+// expert's slots padded to a multiple of 128, expert e starting at 128 *
+// pstage[e]), image (kb, rb) = rows 128 rb .. +127 x one K-stage (128 MXFP8 or
+// 64 BF16 slots) as the 16 KB shared-memory image the MMA reads (128-byte rows,
+// 16-byte chunk q of row r at chunk q ^ (r % 8)), stored [kb][rb].  MXFP8
+// quantises along the slots (blocks of 32 from the expert's first slot) and packs
+// the scales as the 512-byte [32 lanes][4 words] image tcgen05.cp moves to tensor
+// memory.  A B tile (256 rows) is two adjacent images: one bulk copy.
+//
+// GEMM.  One persistent CTA of 12 warps per SM over tiles (expert, GEMM, n, m):
+//   warp 0   producer: bulk copies of the A and B images (and scale images)
+//   warp 1   TMEM owner + MMA issuer; the last K-stage of an expert issues only
+//            the 32-slot (MXFP8) or 16-slot (BF16) steps that hold slots
+//   warps 4-11 epilogue: accumulator -> BF16 -> dW (zeros when the expert has
+//            no slots)
+// Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT and stops.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace wg {
+constexpr int STAGES = 4;
+constexpr int IMG = 16384;                     // one 128-row x 128-byte image
+constexpr int A_BYTES = IMG, B_BYTES = 2 * IMG;
+constexpr int SFA_BYTES = 512, SFB_BYTES = 1024;
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 3;       // full, empty, tfull, tempty, drain
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM = OFF_MISC + 16;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = (4 + EPI_WARPS) * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int TCOL_SFA = 256;
+constexpr int TCOL_SFB = 256 + 4 * STAGES;
+}  // namespace wg
+
+// ------------------------------------------------------------- slot padding
+// pstage[e] = sum over e' < e of ceil(count_e' / 128): expert e's first padded
+// slot is 128 * pstage[e]; pstage[E] covers all experts.  One warp.
+__global__ void wgrad_pstage_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ pstage) {
+    const int lane = threadIdx.x % 32;
+    const int per = (E + 31) / 32;
+    const int lo = min(lane * per, E), hi = min(lo + per, E);
+    int s = 0;
+    for (int e = lo; e < hi; ++e) s += (offsets[e + 1] - offsets[e] + 127) / 128;
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - s;
+    for (int e = lo; e < hi; ++e) {
+        pstage[e] = run;
+        run += (offsets[e + 1] - offsets[e] + 127) / 128;
+    }
+    if (lane == 31) pstage[E] = incl;
+}
+
+// ------------------------------------------------------------- operand packing
+enum { WG_DUV = 0, WG_X = 1, WG_DY = 2, WG_H = 3 };
+
+struct WgPackArgs {
+    const uint16_t* src;      // DUV: du|dv [T][2I]; X: x [N][H]; DY: dout [N][H]; H: u|v [T][2I]
+    const int32_t* sched;     // [T][2] (X, DY)
+    const float* slot_gate;   // [T] (DY)
+    const int32_t* offsets;   // [E+1]
+    const int32_t* pstage;    // [E+1]
+    int E, C, ld, I, rows_per_shard, N;
+    uint8_t* img;             // [Tp/KS][RB][16 KB]
+    uint8_t* sf;              // MXFP8: [Tp/128][RB][512]
+    int RB;                   // row blocks of 128 (R padded to 256)
+};
+
+// CTA = (32-slot block of the padded slot axis, 256 operand rows).  Phase 1: the
+// 32 slot rows' 256 values are read as contiguous 16-byte vectors into shared
+// memory (zeros past the expert's slots or past C).  Phase 2: thread t takes
+// operand row c0 + t and quantises / rounds its 32 slots into the images.
+template <int SRC, bool MX>
+__global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgPackArgs a, WsHeader* ws) {
+    __shared__ float tile[32][257];
+    __shared__ int s_e;
+    const int P0 = blockIdx.x * 32;
+    if (threadIdx.x == 0) {
+        int e = -1;
+        if (P0 < a.pstage[a.E] * 128) {
+            int lo = 0, hi = a.E;   // last e with 128 * pstage[e] <= P0
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (a.pstage[mid] * 128 <= P0) lo = mid; else hi = mid;
+            }
+            e = lo;
+        }
+        s_e = e;
+    }
+    __syncthreads();
+    const int e = s_e;
+    if (e < 0) return;
+    const int local0 = P0 - a.pstage[e] * 128;
+    const int cnt = a.offsets[e + 1] - a.offsets[e];
+    const int s0 = a.offsets[e] + local0;
+    const int c0 = blockIdx.y * 256;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = warp; i < 32; i += 8) {
+        const int col = c0 + lane * 8;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        if (local0 + i < cnt && col < a.C) {
+            const int64_t s = s0 + i;
+            if constexpr (SRC == WG_DUV) {
+                const uint4 w = ld_nc_v4(a.src + s * a.ld + col);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    v[2 * p] = bf16_to_f32((uint16_t)(ww[p] & 0xFFFF));
+                    v[2 * p + 1] = bf16_to_f32((uint16_t)(ww[p] >> 16));
+                }
+            } else if constexpr (SRC == WG_X || SRC == WG_DY) {
+                const int64_t tok = (int64_t)a.sched[2 * s] * a.rows_per_shard + a.sched[2 * s + 1];
+                if (tok >= 0 && tok < a.N) {
+                    const uint4 w = ld_nc_v4(a.src + tok * a.ld + col);
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                    const float gs = SRC == WG_DY ? a.slot_gate[s] : 1.0f;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const float lo = bf16_to_f32((uint16_t)(ww[p] & 0xFFFF));
+                        const float hi = bf16_to_f32((uint16_t)(ww[p] >> 16));
+                        v[2 * p] = SRC == WG_DY ? gs * lo : lo;
+                        v[2 * p + 1] = SRC == WG_DY ? gs * hi : hi;
+                    }
+                } else if (lane == 0) {
+                    set_status(ws, MOE_ERR_DEVICE_CHECK);
+                }
+            } else {   // WG_H: h = silu(u) * v from the kept u|v
+                const uint4 wu = ld_nc_v4(a.src + s * a.ld + col);
+                const uint4 wv = ld_nc_v4(a.src + s * a.ld + a.I + col);
+                const uint32_t uu[4] = {wu.x, wu.y, wu.z, wu.w};
+                const uint32_t vv[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    v[2 * p] = silu_f32(bf16_to_f32((uint16_t)(uu[p] & 0xFFFF))) *
+                               bf16_to_f32((uint16_t)(vv[p] & 0xFFFF));
+                    v[2 * p + 1] = silu_f32(bf16_to_f32((uint16_t)(uu[p] >> 16))) *
+                                   bf16_to_f32((uint16_t)(vv[p] >> 16));
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) tile[i][lane * 8 + q] = v[q];
+    }
+    __syncthreads();
+    const int c = c0 + threadIdx.x;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = tile[i][threadIdx.x];
+    const int rb = c / 128, r = c % 128;
+    if constexpr (MX) {
+        uint32_t codes[8];
+        const uint8_t sc = mx_quantize32(v, codes);
+        const int kb = P0 / 128, sub = (P0 % 128) / 32;
+        uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int q = sub * 2 + h;
+            st_v4(row + ((q ^ (r & 7)) * 16), make_uint4(codes[4 * h], codes[4 * h + 1], codes[4 * h + 2],
+                                                          codes[4 * h + 3]));
+        }
+        a.sf[((int64_t)kb * a.RB + rb) * 512 + ((r % 32) * 4 + r / 32) * 4 + sub] = sc;
+    } else {
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+        const int kb = P0 / 64, sub = (P0 % 64) / 32;
+        uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int q = sub * 4 + h;
+            st_v4(row + ((q ^ (r & 7)) * 16), make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the GEMMs
+struct WgTile {
+    int e, g, m, n;           // expert, GEMM (0: dW_gate_up, 1: dW_down), M tile, N tile
+    int KB;                   // K-stages holding slots (0: the expert has none)
+    int last_steps;           // MMA K-steps in the last stage
+    int kbase;                // first K-stage of the expert in the images
+};
+
+template <bool MX>
+__device__ __forceinline__ WgTile wg_tile(int t, const WgGemm& g0, const WgGemm& g1,
+                                          const int32_t* offsets, const int32_t* pstage) {
+    constexpr int KS = MX ? 128 : 64, KSTEP = MX ? 32 : 16;
+    const int t0 = g0.m_tiles * g0.n_tiles;
+    const int per = t0 + g1.m_tiles * g1.n_tiles;
+    WgTile w;
+    w.e = t / per;
+    int l = t % per;
+    w.g = l >= t0;
+    if (w.g) l -= t0;
+    const int mt = w.g ? g1.m_tiles : g0.m_tiles;
+    w.n = l / mt;
+    w.m = l % mt;
+    const int cnt = offsets[w.e + 1] - offsets[w.e];
+    w.KB = (cnt + KS - 1) / KS;
+    w.kbase = pstage[w.e] * (128 / KS);
+    w.last_steps = w.KB > 0 ? (cnt - (w.KB - 1) * KS + KSTEP - 1) / KSTEP : 0;
+    return w;
+}
+
+template <bool MX>
+__global__ void __launch_bounds__(wg::THREADS, 1)
+    wgrad_gemm_kernel(const __grid_constant__ WgGemm g0, const __grid_constant__ WgGemm g1,
+                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ pstage, int E,
+                      WsHeader* ws, unsigned long long timeout_ns) {
+    using namespace wg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tfull + 2;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, EPI_WARPS);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(reinterpret_cast<uint32_t*>(smem + OFF_MISC), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    const unsigned long long deadline = globaltimer_ns() + timeout_ns;
+    const int total = E * (g0.m_tiles * g0.n_tiles + g1.m_tiles * g1.n_tiles);
+
+    if (warp == 0) {
+        if (lane == 0) {   // producer
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
+                const WgGemm& G = w.g ? g1 : g0;
+                bool ok = true;
+                for (int kb = 0; kb < w.KB; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, ws, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t gk = w.kbase + kb;
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + (MX ? SFA_BYTES + SFB_BYTES : 0));
+                    bulk_load(smem + OFF_A + stage * A_BYTES, G.a_img + (gk * G.a_rb + w.m) * IMG, A_BYTES,
+                              &full[stage]);
+                    bulk_load(smem + OFF_B + stage * B_BYTES, G.b_img + (gk * G.b_rb + 2 * w.n) * IMG, B_BYTES,
+                              &full[stage]);
+                    if (MX) {
+                        bulk_load(smem + OFF_SFA + stage * SFA_BYTES, G.a_sf + (gk * G.a_rb + w.m) * 512,
+                                  SFA_BYTES, &full[stage]);
+                        bulk_load(smem + OFF_SFB + stage * SFB_BYTES, G.b_sf + (gk * G.b_rb + 2 * w.n) * 512,
+                                  SFB_BYTES, &full[stage]);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // MMA issuer
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
+                if (!mbar_wait_bounded(tempty, acc_phase ^ 1, abort_flag, ws, deadline)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < w.KB; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, abort_flag, ws, deadline)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int steps = kb == w.KB - 1 ? w.last_steps : 4;
+                    const uint32_t sa = smem_u32(smem + OFF_A + stage * A_BYTES);
+                    const uint32_t sb = smem_u32(smem + OFF_B + stage * B_BYTES);
+                    if constexpr (MX) {
+                        const uint32_t sfa_t = tmem_base + TCOL_SFA + stage * 4;
+                        const uint32_t sfb_t = tmem_base + TCOL_SFB + stage * 8;
+                        tmem_cp_32x128b_x4(sfa_t, sdesc_sf_block(smem_u32(smem + OFF_SFA + stage * SFA_BYTES)));
+                        tmem_cp_32x128b_x4(sfb_t, sdesc_sf_block(smem_u32(smem + OFF_SFB + stage * SFB_BYTES)));
+                        tmem_cp_32x128b_x4(sfb_t + 4,
+                                           sdesc_sf_block(smem_u32(smem + OFF_SFB + stage * SFB_BYTES + 512)));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (k < steps)
+                                mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + 32 * k), sdesc_kmajor_sw128(sb + 32 * k),
+                                         idesc_mxf8(128, 256, k, k), sfa_t, sfb_t, (kb | k) != 0);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            if (k < steps)
+                                mma_bf16(tmem_base, sdesc_kmajor_sw128(sa + 32 * k), sdesc_kmajor_sw128(sb + 32 * k),
+                                         idesc_bf16(128, 256), (kb | k) != 0);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) mma_commit(tfull);
+                acc_phase ^= 1;
+            }
+            mma_commit(drain);
+            const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+            while (!mbar_try_wait(drain, 0) && globaltimer_ns() < d2) {
+            }
+        }
+    } else if (warp >= 4) {   // epilogue
+        const int q = warp & 3;
+        const int half = (warp - 4) >> 2;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
+            const WgGemm& G = w.g ? g1 : g0;
+            if (!mbar_wait_bounded(tfull, acc_phase, abort_flag, ws, deadline)) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            if (w.KB > 0) {
+                const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v[c4]);
+                tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[c4][i] = 0u;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+            const int64_t row = (int64_t)w.m * 128 + 32 * q + lane;
+            uint8_t* orow = G.out + (int64_t)w.e * G.out_estride + row * G.out_ld * 2;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int col = w.n * 256 + 32 * (half * 4 + c4);
+                if (col >= G.n_valid) continue;
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(v[c4][2 * i]), __uint_as_float(v[c4][2 * i + 1]));
+                st_v8(orow + col * 2, pk);
+                st_v8(orow + col * 2 + 32, pk + 8);
+            }
+            acc_phase ^= 1;
+        }
+    }
+
+    if (*abort_flag) {
+        const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+        while (globaltimer_ns() < d2) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
+    if (c.T == 0 && c.E == 0) return cudaSuccess;
+    const bool mx = c.mx;
+    const int Ip = (c.I + 255) / 256 * 256;
+    const int tp = wgrad_max_padded_slots(c.T, c.E);
+    wgrad_pstage_kernel<<<1, 32, 0, stream>>>(c.offsets, c.E, c.pstage);
+    WgPackArgs pa{};
+    pa.sched = c.sched;
+    pa.slot_gate = c.slot_gate;
+    pa.offsets = c.offsets;
+    pa.pstage = c.pstage;
+    pa.E = c.E;
+    pa.I = c.I;
+    pa.rows_per_shard = c.rows_per_shard;
+    pa.N = c.N;
+    auto pack = [&](int src, const void* p, int C, int Cp, int ld, uint8_t* img, uint8_t* sf) {
+        WgPackArgs q = pa;
+        q.src = (const uint16_t*)p;
+        q.C = C;
+        q.ld = ld;
+        q.img = img;
+        q.sf = sf;
+        q.RB = Cp / 128;
+        const dim3 grid((unsigned)(tp / 32), (unsigned)(Cp / 256));
+#define MOE_WG_PACK(S)                                                                                \
+    if (mx) wgrad_pack_kernel<S, true><<<grid, 256, 0, stream>>>(q, c.ws);                          \
+    else wgrad_pack_kernel<S, false><<<grid, 256, 0, stream>>>(q, c.ws)
+        switch (src) {
+            case WG_DUV: MOE_WG_PACK(WG_DUV); break;
+            case WG_X: MOE_WG_PACK(WG_X); break;
+            case WG_DY: MOE_WG_PACK(WG_DY); break;
+            default: MOE_WG_PACK(WG_H); break;
+        }
+#undef MOE_WG_PACK
+    };
+    pack(WG_DUV, c.duv, 2 * c.I, 2 * c.I, 2 * c.I, c.img_duv, c.sf_duv);
+    pack(WG_X, c.x, c.H, c.H, c.H, c.img_x, c.sf_x);
+    pack(WG_DY, c.dout, c.H, c.H, c.H, c.img_dy, c.sf_dy);
+    pack(WG_H, c.uv, c.I, Ip, 2 * c.I, c.img_h, c.sf_h);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    WgGemm g0{};   // dW_gate_up[e] = [du dv]^T . x   (M = 2I, N = H)
+    g0.a_img = c.img_duv;
+    g0.a_sf = c.sf_duv;
+    g0.a_rb = 2 * c.I / 128;
+    g0.b_img = c.img_x;
+    g0.b_sf = c.sf_x;
+    g0.b_rb = c.H / 128;
+    g0.m_tiles = 2 * c.I / 128;
+    g0.n_tiles = c.H / 256;
+    g0.n_valid = c.H;
+    g0.out = (uint8_t*)c.dw_gate_up;
+    g0.out_estride = (int64_t)2 * c.I * c.H * 2;
+    g0.out_ld = c.H;
+    WgGemm g1{};   // dW_down[e] = dy^T . h          (M = H, N = I padded to 256)
+    g1.a_img = c.img_dy;
+    g1.a_sf = c.sf_dy;
+    g1.a_rb = c.H / 128;
+    g1.b_img = c.img_h;
+    g1.b_sf = c.sf_h;
+    g1.b_rb = Ip / 128;
+    g1.m_tiles = c.H / 128;
+    g1.n_tiles = Ip / 256;
+    g1.n_valid = c.I;
+    g1.out = (uint8_t*)c.dw_down;
+    g1.out_estride = (int64_t)c.H * c.I * 2;
+    g1.out_ld = c.I;
+    const size_t smem = 1024 + wg::SMEM;
+    if (mx) {
+        err = cudaFuncSetAttribute(wgrad_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        wgrad_gemm_kernel<true><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, c.offsets, c.pstage, c.E, c.ws,
+                                                                       c.timeout_ns);
+    } else {
+        err = cudaFuncSetAttribute(wgrad_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        wgrad_gemm_kernel<false><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, c.offsets, c.pstage, c.E, c.ws,
+                                                                        c.timeout_ns);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

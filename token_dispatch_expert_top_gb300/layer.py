@@ -89,6 +89,8 @@ class MoeLayer:
             self.dx = torch.empty((w.N, w.H), dtype=torch.bfloat16, device=dev)
             self.dw_router = torch.empty((w.E, w.H), dtype=torch.float32, device=dev)
             self.dbias = torch.empty(w.E, dtype=torch.float32, device=dev)
+            self.dw_gate_up = torch.empty((w.E, 2 * w.I, w.H), dtype=torch.bfloat16, device=dev)
+            self.dw_down = torch.empty((w.E, w.H, w.I), dtype=torch.bfloat16, device=dev)
         if keep_master:
             self.master = (wgu, wd)
         else:
@@ -124,12 +126,16 @@ class MoeLayer:
         return self.out if out is None else out
 
     def backward(self, dout: torch.Tensor, x: torch.Tensor | None = None,
-                 stream: torch.cuda.Stream | None = None):
-        """Gradients of the last forward_train: (dx, dW_router, dbias)."""
+                 stream: torch.cuda.Stream | None = None, weights: bool = True):
+        """Gradients of the last forward_train: (dx, dW_router, dbias, dW_gate_up,
+        dW_down); the expert weight gradients are skipped (None) when not `weights`."""
         M.moe_backward(dout, self.x if x is None else x, self.w_router, self.saved_c, self.wgu_t,
                        self.wgu_t_sf, self.wd_t, self.wd_t_sf, self.shape, self.params, self.dx,
-                       self.dw_router, self.dbias, self.bws, stream)
-        return self.dx, self.dw_router, self.dbias
+                       self.dw_router, self.dbias, self.dw_gate_up if weights else None,
+                       self.dw_down if weights else None, self.bws, stream)
+        if not weights:
+            return self.dx, self.dw_router, self.dbias, None, None
+        return self.dx, self.dw_router, self.dbias, self.dw_gate_up, self.dw_down
 
     def backward_status(self) -> int:
         return M.moe_last_device_status(self.bws)

@@ -29,7 +29,7 @@ ENTRY_POINTS = (
     "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
     "moe_pack_expert_weights", "moe_backward_workspace_bytes", "moe_pack_expert_weights_dgrad",
     "moe_expert_ffn_train", "moe_forward_train", "moe_reverse_combine", "moe_expert_ffn_dgrad",
-    "moe_reverse_dispatch", "moe_router_wgrad", "moe_backward",
+    "moe_reverse_dispatch", "moe_router_wgrad", "moe_backward", "moe_expert_wgrad",
 )
 
 
@@ -105,7 +105,8 @@ _SIGS = {
     "moe_reverse_dispatch": (_i, [_vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _sz, _vp]),
     "moe_router_wgrad": (_i, [_vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _sz, _vp]),
     "moe_backward": (_i, [_vp, _vp, _vp, _svd, _vp, _vp, _vp, _vp, _shp, _prm, _vp, _vp, _vp, _vp,
-                          _sz, _vp]),
+                          _vp, _vp, _sz, _vp]),
+    "moe_expert_wgrad": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _vp, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -296,9 +297,18 @@ def moe_router_wgrad(x, sched, offsets, slot_dlogit, shape: Shape, dw_router, db
         _p(dbias), _p(ws), _wsz(ws), _stream(stream)))
 
 
+def moe_expert_wgrad(duv, x, dout, uv, sched, slot_gate, offsets, shape: Shape, dw_gate_up, dw_down,
+                     ws, stream=None) -> None:
+    _check("moe_expert_wgrad", _lib.moe_expert_wgrad(
+        _p(duv), _p(x), _p(dout), _p(uv), _p(sched), _p(slot_gate), _p(offsets),
+        ctypes.byref(shape), _p(dw_gate_up), _p(dw_down), _p(ws), _wsz(ws), _stream(stream)))
+
+
 def moe_backward(dout, x, w_router, saved: Saved, wt_gate_up, wt_gu_scales, wt_down, wt_d_scales,
-                 shape: Shape, params: Params | None, dx, dw_router, dbias, ws, stream=None) -> None:
+                 shape: Shape, params: Params | None, dx, dw_router, dbias, dw_gate_up, dw_down, ws,
+                 stream=None) -> None:
     _check("moe_backward", _lib.moe_backward(
         _p(dout), _p(x), _p(w_router), ctypes.byref(saved), _p(wt_gate_up), _p(wt_gu_scales),
         _p(wt_down), _p(wt_d_scales), ctypes.byref(shape), ctypes.byref(params) if params else None,
-        _p(dx), _p(dw_router), _p(dbias), _p(ws), _wsz(ws), _stream(stream)))
+        _p(dx), _p(dw_router), _p(dbias), _p(dw_gate_up), _p(dw_down), _p(ws), _wsz(ws),
+        _stream(stream)))
