@@ -28,6 +28,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from token_dispatch_expert_top_gb300 import synth  # noqa: E402
@@ -374,6 +375,187 @@ def gpu_arm(args, rank, world):
     return res, layer
 
 
+# ------------------------------------------------------------- training step
+class BackwardStages:
+    """The kernels of moe_backward, issued entry point by entry point so that CUDA
+    events can bracket each stage on the launching stream."""
+
+    names = ["reverse_combine", "expert_dgrad", "reverse_dispatch", "router_wgrad", "expert_wgrad"]
+
+    def __init__(self, layer):
+        from token_dispatch_expert_top_gb300 import moe as M
+        self.M, self.L = M, layer
+        w, dev = layer.w, layer.x.device
+        mx = w.dtype == "mxfp8"
+        T = w.T
+        f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)
+        bf = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
+        u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device=dev)
+        self.dy = u8(T, w.H) if mx else bf(T, w.H)
+        self.dy_sf = u8(T, w.H // 32) if mx else None
+        self.dgate, self.dlogit, self.sgate, self.sdl = f32(w.N, w.k), f32(w.N, w.k), f32(T), f32(T)
+        self.duv = bf(T, 2 * w.I)
+        self.duv_c = u8(T, 2 * w.I) if mx else None
+        self.duv_s = u8(T, 2 * w.I // 32) if mx else None
+        self.da = bf(T, w.H)
+
+    def run(self, dout, events=None):
+        M, L, sv = self.M, self.L, self.L.saved
+        ev = events or [None] * 6
+        rec = lambda i: ev[i].record() if ev[i] else None
+        rec(0)
+        M.moe_reverse_combine(dout, sv["y"], sv["inv"], sv["gate"], L.shape, self.dy, self.dy_sf,
+                              self.dgate, self.dlogit, self.sgate, self.sdl, L.bws)
+        rec(1)
+        M.moe_expert_ffn_dgrad(self.dy, self.dy_sf, sv["uv"], sv["offsets"], L.wgu_t, L.wgu_t_sf,
+                               L.wd_t, L.wd_t_sf, L.shape, self.duv, self.duv_c, self.duv_s, self.da,
+                               L.bws)
+        rec(2)
+        M.moe_reverse_dispatch(self.da, sv["inv"], sv["idx"], self.dlogit, L.w_router, L.shape, L.dx,
+                               L.bws)
+        rec(3)
+        M.moe_router_wgrad(L.x, sv["sched"], sv["offsets"], self.sdl, L.shape, L.dw_router, L.dbias,
+                           L.bws)
+        rec(4)
+        M.moe_expert_wgrad(self.duv, L.x, dout, sv["uv"], sv["sched"], self.sgate, sv["offsets"],
+                           L.shape, L.dw_gate_up, L.dw_down, L.bws)
+        rec(5)
+
+
+def train_launches_per_step(w) -> int:
+    """libmoe kernels one forward_train + backward launch."""
+    fwd = kernel_launches_per_step(w, False)
+    bwd = 1 + 2 + 1 + 2 + (1 + 4 + 1)   # rev. combine, dgrad x2, rev. dispatch, router wgrad x2,
+    return fwd + bwd                     # wgrad: slot padding, 4 operand packs, GEMM
+
+
+def train_arm(args, rank, world):
+    from token_dispatch_expert_top_gb300 import moe as M
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(w, device=dev)
+    layer = MoeLayer(w, inp, device=str(dev), train=True)
+    del inp
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    dout = torch.randn((w.N, w.H), generator=gen, device=dev).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def step(x=None, g=None):
+        layer.forward_train(x=x)
+        layer.backward(dout if g is None else g, x=x)
+
+    for _ in range(args.warmup):
+        step()
+    for st in (layer.device_status(), layer.backward_status()):
+        if st != 0:
+            raise RuntimeError(f"device status {M.status_name(st)} after warm-up")
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    assert layer.device_status() == 0 and layer.backward_status() == 0
+    ms_per_step = t_ms / args.steps
+
+    # forward time alone (same kernels as forward_train) and the backward stages
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_train()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = f0.elapsed_time(f1) / args.steps
+    bs = BackwardStages(layer)
+    bs.run(dout)
+    torch.cuda.synchronize()
+    sums = [0.0] * 5
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        bs.run(dout, evs)
+        torch.cuda.synchronize()
+        for i in range(5):
+            sums[i] += evs[i].elapsed_time(evs[i + 1])
+    stage_ms = {n: s / args.steps for n, s in zip(bs.names, sums)}
+    assert layer.backward_status() == 0
+
+    # e2e: x and dout from pinned host memory, dx back, every step, inside the region
+    x_host = layer.x.cpu().pin_memory()
+    g_host = dout.cpu().pin_memory()
+    dx_host = torch.empty(layer.dx.shape, dtype=layer.dx.dtype).pin_memory()
+    x_dev, g_dev = torch.empty_like(layer.x), torch.empty_like(dout)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        g_dev.copy_(g_host, non_blocking=True)
+        step(x_dev, g_dev)
+        dx_host.copy_(layer.dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_rate(w.N, args.steps, e2e_ms, world), "unit": "tokens/s",
+           "h2d_bytes_per_step": 2 * x_host.numel() * x_host.element_size(),
+           "d2h_bytes_per_step": dx_host.numel() * dx_host.element_size(),
+           "overlap": "none (copies and the step on one stream)"}
+
+    peaks, peak_src = load_peaks()
+    tensor_peak = peaks["bf16_tflops_sustained"] * (FP8_PER_BF16 if w.dtype == "mxfp8" else 1)
+    flops = w.ffn_flops                      # each of dgrad and wgrad: 6*H*I per slot
+    dgrad_tf = flops / (stage_ms["expert_dgrad"] / 1e3) / 1e12
+    wgrad_tf = flops / (stage_ms["expert_wgrad"] / 1e3) / 1e12
+    dom = "expert_wgrad" if stage_ms["expert_wgrad"] >= stage_ms["expert_dgrad"] else "expert_dgrad"
+    dom_tf = wgrad_tf if dom == "expert_wgrad" else dgrad_tf
+    roofline = {
+        "kernel": ("expert wgrad (slot padding, four operand packs, grouped GEMM)" if dom == "expert_wgrad"
+                   else "expert dgrad grouped GEMMs (two launches)"),
+        "bound": "tensor", "achieved": round(dom_tf, 2), "peak": round(tensor_peak, 1),
+        "unit": "TFLOP/s", "frac": round(dom_tf / tensor_peak, 4), "traffic": None,
+        "peak_source": f"{peak_src} sustained BF16" + (f" x {FP8_PER_BF16:g}" if w.dtype == "mxfp8" else ""),
+        "algorithmic": f"{flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
+    }
+    counts = np.bincount(layer.saved["idx"].cpu().numpy().ravel(), minlength=w.E)
+    res = {
+        "metric": "MoE layer training step (forward + backward) tokens/s", "value":
+            round(job_rate(w.N, args.steps, t_ms, world), 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; x, dout ~N(0,1), W~N(0,1/fan_in), drawn on the device)",
+        "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "S": w.S,
+                   "skew": w.skew, "path": "forward_train + backward", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: ~23 GB of packed MXFP8 weights read per step",
+                   "load_max_over_mean": round(float(counts.max() / counts.mean()), 2),
+                   "empty_experts": int((counts == 0).sum())},
+        "forward_ms": round(fwd_ms, 4),
+        "backward_stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "dgrad_tflops": round(dgrad_tf, 2), "wgrad_tflops": round(wgrad_tf, 2),
+        "roofline": roofline,
+        "gpu_launches": train_launches_per_step(w) * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    return res, layer
+
+
 # ------------------------------------------------------------- the oracle (CPU)
 def oracle_sample(w, inp, n_tokens: int, seed: int):
     """One bounded sample of the layer on the oracle: routing and layout of all N
@@ -390,6 +572,28 @@ def oracle_sample(w, inp, n_tokens: int, seed: int):
     t0 = time.perf_counter()
     O.forward({"x": inp["x"], "w_router": inp["w_router"], "bias": inp["bias"]}, w.E, w.k, w.S,
               w.dtype, tokens=toks, weights=weights)
+    return time.perf_counter() - t0
+
+
+def oracle_train_sample(w, inp, n_tokens: int, seed: int):
+    """One bounded sample of the training step on the oracle: the forward of
+    n_tokens sampled tokens (routing and layout of all N) and the backward of
+    those tokens' input gradients (their k slots' FFN backward, the gate and
+    router terms).  Returns seconds."""
+    sys.path.insert(0, os.path.join(ROOT, "oracle"))
+    import oracle as O
+
+    toks = np.random.default_rng(seed).choice(w.N, size=n_tokens, replace=False)
+    dout = torch.randn((w.N, w.H), generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+
+    def weights(e):
+        return O.expert_operands(inp["w_gate_up"][e].cpu(), inp["w_down"][e].cpu(), w.dtype)
+
+    t0 = time.perf_counter()
+    O.forward({"x": inp["x"], "w_router": inp["w_router"], "bias": inp["bias"]}, w.E, w.k, w.S,
+              w.dtype, tokens=toks, weights=weights)
+    O.backward({k: inp[k] for k in ("x", "w_router", "bias", "w_gate_up", "w_down")}, w.E, w.k, w.S,
+               w.dtype, dout, tokens=toks, experts=[], weights=weights)
     return time.perf_counter() - t0
 
 
@@ -441,6 +645,8 @@ def main():
     ap.add_argument("--sample-tokens", type=int, default=2,
                     help="tokens per oracle sample (CPU baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time the training step (forward_train + backward) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -459,7 +665,7 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
-    res, layer = gpu_arm(args, rank, world)
+    res, layer = (train_arm if args.train else gpu_arm)(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             w = layer.w
@@ -467,12 +673,16 @@ def main():
             torch.cuda.empty_cache()
             inp = synth.make_inputs(w, device="cuda" if w.name in synth.DEVICE_DRAWN else "cpu")
             n_tok = args.sample_tokens
-            dt = oracle_sample(w, inp, n_tok, seed=12345)
-            res["cpu_baseline"] = {
-                "value": round(n_tok / dt, 4), "unit": "tokens/s", "cores": cpu_cores(),
-                "kind": "oracle",
-                "sample": f"routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
-                          f"random tokens, FP64 oracle, {dt:.1f} s"}
+            if args.train:
+                dt = oracle_train_sample(w, inp, n_tok, seed=12345)
+                what = (f"forward and input-gradient backward of {n_tok} random tokens (routing and "
+                        f"layout of all {w.N}), FP64 oracle, {dt:.1f} s")
+            else:
+                dt = oracle_sample(w, inp, n_tok, seed=12345)
+                what = (f"routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
+                        f"random tokens, FP64 oracle, {dt:.1f} s")
+            res["cpu_baseline"] = {"value": round(n_tok / dt, 4), "unit": "tokens/s",
+                                   "cores": cpu_cores(), "kind": "oracle", "sample": what}
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -332,15 +332,16 @@ def gate_backward(gate: np.ndarray, dgate: np.ndarray) -> np.ndarray:
 
 # Storage formats of the backward's dgrad operands and intermediates per workload
 # dtype: dy (the first dgrad GEMM's A operand, along H), the kept pre-activations
-# u|v, du|dv (the second dgrad GEMM's A operand, along I) and da.  The dgrad
+# u|v, du|dv (the second dgrad GEMM's A operand, along I), da, and dh as it is
+# kept between the first dgrad GEMM and the SwiGLU derivative.  The dgrad
 # weights are the masters in the GEMM format quantised along the dgrad K
 # (``expert_operands_dgrad``).
 BWD_FORMATS = {
-    #          dy        uv      duv      da
-    "f64":   ("f64",    "f64",  "f64",   "f64"),
-    "f32":   ("f32",    "f32",  "f32",   "f32"),
-    "bf16":  ("bf16",   "bf16", "bf16",  "bf16"),
-    "mxfp8": ("mxfp8",  "bf16", "mxfp8", "bf16"),
+    #          dy        uv      duv      da      dh
+    "f64":   ("f64",    "f64",  "f64",   "f64",  "f64"),
+    "f32":   ("f32",    "f32",  "f32",   "f32",  "f32"),
+    "bf16":  ("bf16",   "bf16", "bf16",  "bf16", "bf16"),
+    "mxfp8": ("mxfp8",  "bf16", "mxfp8", "bf16", "bf16"),
 }
 
 
@@ -382,7 +383,7 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
 
     Forward as ``expert_ffn``: u = a Wg^T, v = a Wu^T, h = round_h(silu(u) v),
     y = round_y(h Wd^T).  Each rounding point's derivative is taken as 1, so
-      dh = dy_b Wd_b,  (du, dv) = swiglu_backward(u_s, v_s, dh),
+      dh = round_dh(dy_b Wd_b),  (du, dv) = swiglu_backward(u_s, v_s, dh),
       da = round_da(du_b Wg_b + dv_b Wu_b),
       dWg = du^T a,  dWu = dv^T a,  dWd = dy^T h   (h after its rounding),
     where _b marks a dgrad GEMM operand in its storage format (BWD_FORMATS; the
@@ -397,14 +398,14 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     the exact derivative.
     Returns dict(u, v, h, y, dh, du, dv, da, dwg, dwu, dwd)."""
     _, fmt_h, fmt_y, _ = FORMATS[dtype]
-    f_dy, f_uv, f_duv, f_da = BWD_FORMATS[dtype]
+    f_dy, f_uv, f_duv, f_da, f_dh = BWD_FORMATS[dtype]
     wg_b, wu_b, wd_b = (wg, wu, wd) if wb is None else wb
     u = a @ wg.T
     v = a @ wu.T
     h = round_to(swiglu(u, v), fmt_h)
     y = round_to(h @ wd.T, fmt_y)
     u_s, v_s = round_to(u, f_uv), round_to(v, f_uv)
-    dh = round_to(dy, f_dy) @ wd_b
+    dh = round_to(round_to(dy, f_dy) @ wd_b, f_dh)
     du, dv = swiglu_backward(u_s, v_s, dh)
     da = round_to(round_to(du, f_duv) @ wg_b + round_to(dv, f_duv) @ wu_b, f_da)
     if WGRAD_FORMATS[dtype] is None:

@@ -89,3 +89,46 @@ def test_fullsize_skew_ring_sweep_bitwise(ring):
     fused = layer.forward(fused=True)
     assert layer.device_status() == 0
     assert torch.equal(fused, staged)
+
+
+def test_fullsize_backward_sampled_parity():
+    """The 16384-token skewed layer, forward + backward: dx of sampled tokens, and
+    the weight gradients (dW_gate_up, dW_down, the router row and bias entry) of
+    two sampled lightly loaded experts, against the oracle's backward restricted to
+    those tokens and experts.  Tokens and experts are drawn among those whose
+    routing is away from top-k near-ties."""
+    need_cuda()
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+    w = synth.WORKLOADS["dsv3_mxfp8_skew_16k"]
+    inp = synth.make_inputs(w)
+    layer = MoeLayer(w, inp, train=True)
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    dout = torch.randn((w.N, w.H), generator=gen, device="cuda").to(torch.bfloat16)
+    layer.forward_train()
+    dx, dwr, db, dwgu, dwd = layer.backward(dout)
+    assert layer.device_status() == 0 and layer.backward_status() == 0
+    lg = O.router_logits(inp["x"], inp["w_router"], inp["bias"])
+    gap = O.topk_gap(lg, w.k)
+    ridx, _ = O.route_topk(lg, w.k)
+    assert check_routing(to_np(layer.saved["idx"]), ridx, lg, gap) > 0.97
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(np.nonzero(gap >= TIE_TAU)[0], 8, replace=False))
+    counts = np.bincount(ridx.ravel(), minlength=w.E)
+    cand = [int(e) for e in np.argsort(counts, kind="stable")
+            if 0 < counts[e] <= 64 and np.all(gap[(ridx == e).any(axis=1)] >= TIE_TAU)]
+    exps = np.array(sorted(cand[:2]))
+    assert len(exps) == 2
+    ref = O.backward(inp, w.E, w.k, w.S, w.dtype, dout, tokens=toks, experts=exps,
+                     weights=_oracle_weights(inp, w.dtype))
+    tol = TOL[w.dtype]
+    err = row_rel_err(to_np(dx)[toks], ref["dx"])
+    assert err.max() < tol, ("dx", err.max())
+    g_gu, g_d, g_r, g_b = to_np(dwgu), to_np(dwd), to_np(dwr), to_np(db)
+    for i, e in enumerate(exps):
+        e_gu = row_rel_err(g_gu[e], ref["dw_gate_up"][i]).max()
+        e_d = row_rel_err(g_d[e], ref["dw_down"][i]).max()
+        e_r = row_rel_err(g_r[e:e + 1], ref["dw_router"][i:i + 1]).max()
+        assert max(e_gu, e_d, e_r) < tol, (int(e), int(counts[e]), e_gu, e_d, e_r)
+        scale = np.abs(ref["dlogit"][:, e]).sum()
+        assert abs(g_b[e] - ref["dbias"][i]) <= tol * scale, (int(e), g_b[e], ref["dbias"][i])
+    print(f"backward 16k: dx err {err.max():.4f}, experts {exps.tolist()} with {counts[exps].tolist()} slots")

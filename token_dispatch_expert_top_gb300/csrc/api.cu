@@ -130,9 +130,9 @@ T* at(void* ws, size_t off) {
 
 // Workspace regions of the backward entry points, in order.
 struct BwdPlan {
-    size_t header, dy, dy_sf, duv, duv_q, duv_sf, da, dgate, dlogit, slot_gate, slot_dlogit;
+    size_t header, dy, dy_sf, dh, duv, duv_q, duv_sf, da, dgate, dlogit, slot_gate, slot_dlogit;
     size_t part, part_b, ppre;
-    size_t pstage, img_duv, sf_duv, img_x, sf_x, img_dy, sf_dy, img_h, sf_h;
+    size_t pstage, blk_e, img_duv, sf_duv, img_x, sf_x, img_dy, sf_dy, img_h, sf_h;
     size_t total;
 };
 
@@ -150,6 +150,7 @@ BwdPlan make_bwd_plan(const moe_shape_t& s) {
     pl.header = take(sizeof(WsHeader));
     pl.dy = take(T * s.H * (mx ? 1 : 2));
     pl.dy_sf = take(mx ? T * (s.H / 32) : 0);
+    pl.dh = take(T * s.I * 2);
     pl.duv = take(T * 2 * s.I * 2);
     pl.duv_q = take(mx ? T * 2 * s.I : 0);
     pl.duv_sf = take(mx ? T * (2 * s.I / 32) : 0);
@@ -166,6 +167,7 @@ BwdPlan make_bwd_plan(const moe_shape_t& s) {
     const size_t esz = mx ? 1 : 2;
     const size_t Ip = (size_t)(s.I + 255) / 256 * 256;
     pl.pstage = take(sizeof(int32_t) * (s.E + 1));
+    pl.blk_e = take(sizeof(int32_t) * (tp / 32));
     pl.img_duv = take(tp * 2 * s.I * esz);
     pl.sf_duv = take(mx ? tp * 2 * s.I / 32 : 0);
     pl.img_x = take(tp * s.H * esz);
@@ -730,7 +732,9 @@ int moe_expert_ffn_dgrad(const void* dy, const uint8_t* dy_scales, const void* u
         return MOE_ERR_INVALID_ARG;
     if (mx && (((uintptr_t)dy_scales & 15) || ((uintptr_t)duv_scales & 15)))
         return MOE_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
+    rc = check_bwd_ws(shape, workspace, workspace_bytes);
+    if (rc) return rc;
+    const BwdPlan pl = make_bwd_plan(s);
     TcDgradCall c{};
     c.mx = mx;
     c.T = s.N * s.k;
@@ -746,13 +750,15 @@ int moe_expert_ffn_dgrad(const void* dy, const uint8_t* dy_scales, const void* u
     c.wt_d_sf = wt_d_scales;
     c.wt_gate_up = wt_gate_up;
     c.wt_gu_sf = wt_gu_scales;
+    c.dh = at<void>(workspace, pl.dh);
     c.duv = duv;
     c.duv_q = duv_codes;
     c.duv_sf = duv_scales;
     c.da = da;
-    c.ws = at<WsHeader>(workspace, 0);
+    c.ws = at<WsHeader>(workspace, pl.header);
     c.timeout_ns = kDefaultTimeoutNs;
     c.grid = num_sms_current();
+    c.num_sms = num_sms_current();
     return cuda_status(launch_ffn_dgrad_tc(c, (cudaStream_t)stream));
 }
 
@@ -824,6 +830,7 @@ int moe_expert_wgrad(const void* duv, const void* x, const void* dout, const voi
     c.dw_gate_up = dw_gate_up;
     c.dw_down = dw_down;
     c.pstage = at<int32_t>(ws, pl.pstage);
+    c.blk_e = at<int32_t>(ws, pl.blk_e);
     c.img_duv = at<uint8_t>(ws, pl.img_duv);
     c.sf_duv = mx ? at<uint8_t>(ws, pl.sf_duv) : nullptr;
     c.img_x = at<uint8_t>(ws, pl.img_x);

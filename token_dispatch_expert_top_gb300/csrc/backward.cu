@@ -237,13 +237,79 @@ cudaError_t launch_reverse_combine(bool mx, const void* dout, const void* y, con
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------- SwiGLU backward
+// One thread per (slot row t, 32-column block of I), consecutive threads on
+// consecutive blocks of a row: with s = sigma(u),
+//   du = dh * v * (s + u s (1 - s)),   dv = dh * u * s
+// from BF16 dh and the kept BF16 u|v, in FP32; du|dv stored as BF16 (du in
+// columns 0..I-1, dv in I..2I-1) and, MXFP8, quantised along I per 32-block.
+template <bool MX>
+__global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t* __restrict__ dh,
+                                                              const uint16_t* __restrict__ uv, int T, int I,
+                                                              uint16_t* __restrict__ duv,
+                                                              uint8_t* __restrict__ duv_q,
+                                                              uint8_t* __restrict__ duv_sf) {
+    const int nb = I / 32;
+    const int64_t total = (int64_t)T * nb;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = b / nb;
+        const int col = (int)(b % nb) * 32;
+        float d[32], u[32], v[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            unpack_bf16x8(ld_nc_v4(dh + r * I + col + 8 * i), d + 8 * i);
+            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + col + 8 * i), u + 8 * i);
+            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + I + col + 8 * i), v + 8 * i);
+        }
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            float o[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float s = 1.0f / (1.0f + expf(-u[i]));
+                o[i] = part == 0 ? d[i] * v[i] * (s + u[i] * s * (1.0f - s)) : d[i] * u[i] * s;
+            }
+            const int64_t c = col + (part ? I : 0);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+            uint16_t* dst = duv + r * 2 * I + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) st_v4(dst + 8 * i, make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
+            if constexpr (MX) {
+                const uint8_t sc = mx_quantize32(o, pk);
+                uint8_t* q = duv_q + r * 2 * I + c;
+                st_v4(q, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                st_v4(q + 16, make_uint4(pk[4], pk[5], pk[6], pk[7]));
+                duv_sf[r * (2 * I / 32) + c / 32] = sc;
+            }
+        }
+    }
+}
+
+cudaError_t launch_swiglu_backward(bool mx, const void* dh, const void* uv, int T, int I, void* duv,
+                                   uint8_t* duv_q, uint8_t* duv_sf, int num_sms, cudaStream_t stream) {
+    const int64_t total = (int64_t)T * (I / 32);
+    if (total == 0) return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
+    if (mx)
+        swiglu_backward_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(
+            (const uint16_t*)dh, (const uint16_t*)uv, T, I, (uint16_t*)duv, duv_q, duv_sf);
+    else
+        swiglu_backward_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(
+            (const uint16_t*)dh, (const uint16_t*)uv, T, I, (uint16_t*)duv, nullptr, nullptr);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- reverse dispatch
 // Work item = (token n, 256-column chunk); one warp per item, 8 columns per lane.
 //   dx[n] = sum_j da[inv[n][j]]  +  sum_j dlogit[n][j] * W_r[idx[n][j]]
-// both sums in j order in FP32 (the slot part first), rounded once to BF16.  All
-// 2k row loads of an item are issued before the first add.  A slot or expert
-// index out of range skips that term and records MOE_ERR_DEVICE_CHECK.
-template <int KMAX>
+// both sums in j order in FP32 (the slot part first), rounded once to BF16.  Few
+// registers per thread, so many warps per SM keep the row loads in flight (the
+// forward combine's pattern).  A slot or expert index out of range skips that
+// term and records MOE_ERR_DEVICE_CHECK.
 __global__ void __launch_bounds__(kBwdWarps * 32) reverse_dispatch_kernel(
     const uint16_t* __restrict__ da, const int32_t* __restrict__ inv, const int32_t* __restrict__ idx,
     const float* __restrict__ dlogit, const uint16_t* __restrict__ w_router, int N, int H, int k,
@@ -257,44 +323,32 @@ __global__ void __launch_bounds__(kBwdWarps * 32) reverse_dispatch_kernel(
         const int64_t n = it / chunks;
         const int col = (int)(it % chunks) * 256 + lane * 8;
         int my_slot = lane < k ? inv[n * k + lane] : 0;
-        int my_e = lane < k ? idx[n * k + lane] : 0;
+        const int my_e = lane < k ? idx[n * k + lane] : 0;
         const float my_dl = lane < k ? dlogit[n * k + lane] : 0.f;
-        const bool bad = lane < k && (my_slot < 0 || my_slot >= T || my_e < 0 || my_e >= E);
-        if (bad) {
+        if (lane < k && (my_slot < 0 || my_slot >= T || my_e < 0 || my_e >= E)) {
             set_status(ws, MOE_ERR_DEVICE_CHECK);
             my_slot = -1;
-        }
-        uint4 a[KMAX], w[KMAX];
-        int slot[KMAX], e[KMAX];
-        float dl[KMAX];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            slot[j] = __shfl_sync(0xffffffffu, my_slot, j);
-            e[j] = __shfl_sync(0xffffffffu, my_e, j);
-            dl[j] = __shfl_sync(0xffffffffu, my_dl, j);
-            if (j < k && slot[j] >= 0) {
-                a[j] = ld_nc_v4(da + (int64_t)slot[j] * H + col);
-                w[j] = ld_nc_v4(w_router + (int64_t)e[j] * H + col);
-            }
         }
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k || slot[j] < 0) continue;
+        for (int j = 0; j < k; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            if (slot < 0) continue;
             float f[8];
-            unpack_bf16x8(a[j], f);
+            unpack_bf16x8(ld_nc_v4(da + (int64_t)slot * H + col), f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] += f[q];
         }
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k || slot[j] < 0) continue;
+        for (int j = 0; j < k; ++j) {
+            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
+            const int e = __shfl_sync(0xffffffffu, my_e, j);
+            const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+            if (slot < 0) continue;
             float f[8];
-            unpack_bf16x8(w[j], f);
+            unpack_bf16x8(ld_nc_v4(w_router + (int64_t)e * H + col), f);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = fmaf(dl[j], f[q], acc[q]);
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(dl, f[q], acc[q]);
         }
         st_v4(dx + n * H + col, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
@@ -309,14 +363,8 @@ cudaError_t launch_reverse_dispatch(const void* da, const int32_t* inv, const in
     if (items == 0) return cudaSuccess;
     int64_t blocks = (items + kBwdWarps - 1) / kBwdWarps;
     if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
-#define MOE_RD_LAUNCH(KM)                                                                          \
-    reverse_dispatch_kernel<KM><<<(unsigned)blocks, kBwdWarps * 32, 0, stream>>>(                  \
-        (const uint16_t*)da, inv, idx, dlogit, (const uint16_t*)w_router, N, H, k, T, E,           \
-        (uint16_t*)dx, ws)
-    if (k <= 8) MOE_RD_LAUNCH(8);
-    else if (k <= 16) MOE_RD_LAUNCH(16);
-    else MOE_RD_LAUNCH(32);
-#undef MOE_RD_LAUNCH
+    reverse_dispatch_kernel<<<(unsigned)blocks, kBwdWarps * 32, 0, stream>>>(
+        (const uint16_t*)da, inv, idx, dlogit, (const uint16_t*)w_router, N, H, k, T, E, (uint16_t*)dx, ws);
     return cudaGetLastError();
 }
 

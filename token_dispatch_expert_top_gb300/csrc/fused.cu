@@ -238,7 +238,6 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
 // the weight stream evicts it from L2 in between.)
 struct MinibatchTiles {
     static constexpr bool kDeps = true;         // tiles wait for other CTAs (a dependency thread checks)
-    static constexpr int kKinds = 3;            // GEMM1 and GEMM2 tiles
     static constexpr bool kSaveUV = false;
     const FusedArgs* a;
     const int32_t* off;       // offsets in shared memory

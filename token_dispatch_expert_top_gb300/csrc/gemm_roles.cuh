@@ -22,9 +22,8 @@
 //               half the columns, drain the FP32 accumulator into registers,
 //               release it, then apply SwiGLU (+ MXFP8 quantisation of h along I)
 //               or BF16 conversion and store.
-// A tile is GEMM1 (+SwiGLU; kind 0), GEMM2 (kind 1; also the backward's dgrad of
-// GEMM1, which has the same form) or the backward's dgrad of GEMM2 with the
-// SwiGLU derivative in its epilogue (kind 2; sources whose kKinds has bit 2).  The source (first / next
+// A tile is GEMM1 (+SwiGLU; kind 0) or GEMM2 (kind 1; also the form of the
+// backward's two dgrad GEMMs).  The source (first / next
 // / count / kind_of / tile / wait_inputs / tile_stored) decides the
 // order, where each tile's A rows come from, where its output goes, and what a
 // tile waits for before its A operand (or its A scales) may be loaded -- nothing
@@ -76,15 +75,12 @@ struct GemmSide {
     const uint8_t* a_sf;      // MXFP8: [a_rows][K/32]
     const uint8_t* b_pk;      // tile-packed weights [E][n_tiles][K-stages][32 KB]
     const uint8_t* sfb_pk;    // MXFP8: tile-packed scales [E][n_tiles][K-stages][1 KB]
-    uint8_t* out;             // GEMM1: h [rows][I] (codes or BF16); GEMM2: y BF16 [rows][H];
-                              // dgrad of GEMM2: du|dv BF16 [rows][2I]
+    uint8_t* out;             // GEMM1: h [rows][I] (codes or BF16); GEMM2: y BF16 [rows][H]
+                              // (the backward's dgrad GEMMs: dh [rows][I], da [rows][H])
     uint8_t* out_sf;          // GEMM1 MXFP8: h scales [rows][I/32]
     int out_ld;               // row length of out in elements
-    uint8_t* aux;             // GEMM1: where to save u|v (BF16 [rows][2I]), or null;
-                              // dgrad of GEMM2: the saved u|v it reads
-    uint8_t* out2;            // dgrad of GEMM2, MXFP8: du|dv codes [rows][2I]
-    uint8_t* out2_sf;         // dgrad of GEMM2, MXFP8: du|dv scales [rows][2I/32]
-    int n_valid;              // dgrad of GEMM2: I (tile columns past it are padding)
+    uint8_t* aux;             // GEMM1 in training: where to save u|v (BF16 [rows][2I])
+    int n_valid;              // GEMM2 form: output columns (tile columns past it are padding)
 };
 
 // The tensor maps of both GEMMs, picked by tile kind with a select (no indexed
@@ -104,8 +100,8 @@ struct GemmSides {
 };
 
 struct TileInfo {
-    int kind;                 // 0: GEMM1 + SwiGLU, 1: GEMM2 (or the dgrad of GEMM1, the
-                              // same form), 2: dgrad of GEMM2 + SwiGLU backward
+    int kind;                 // 0: GEMM1 + SwiGLU, 1: GEMM2 (or either dgrad GEMM of the
+                              // backward, which have the same form)
     int e, n;                 // expert, N tile
     int a_row0;               // first row of the A tile in its tensor
     int out_row0;             // first output row
@@ -122,15 +118,6 @@ struct Pipe {
     WsHeader* ws;
     unsigned long long deadline;
 };
-
-__device__ __forceinline__ void unpack_bf16x8_g(const uint4& q, float* f) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        f[2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
-        f[2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
-    }
-}
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
     return q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w));
@@ -443,79 +430,6 @@ __device__ void epilogue_role(const Pipe& p, const GemmSides& sides, Src& src) {
                     }
                 }
             }
-        } else if ((Src::kKinds & 4) && tl.kind == 2) {
-            // dgrad of GEMM2: the accumulator holds dh = dy . W_down for 256 h
-            // columns; this warp's 128 of them, in four 32-column blocks, become
-            //   du = dh * v * silu'(u),  dv = dh * silu(u)
-            // from the saved BF16 u|v, stored as BF16 (for the weight gradients)
-            // and, MXFP8, quantised along I (the operand of the dgrad of GEMM1).
-            // Two passes of two 32-column blocks keep the registers in bounds; the
-            // accumulator is released once the second pass has read it.
-            const int I = sd.n_valid;
-            const int64_t ld2 = 2 * (int64_t)I;
-#pragma unroll 1
-            for (int ph = 0; ph < 2; ++ph) {
-            uint32_t v[2][32];
-            tmem_ld_32x32b_x32(tq + 32 * (half * 4 + 2 * ph), v[0]);
-            tmem_ld_32x32b_x32(tq + 32 * (half * 4 + 2 * ph + 1), v[1]);
-            tmem_ld_wait();
-            if (ph == 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p.tempty);
-            }
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                const int col = tl.n * BN + 32 * (half * 4 + 2 * ph + c2);
-                if (col >= I) continue;                     // padding columns of the last tile
-                uint4 uw[4], vw[4];
-                if (valid) {
-                    const uint8_t* su = sd.aux + (row * ld2 + col) * 2;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uw[i] = ld_nc_v4(su + 16 * i);
-                        vw[i] = ld_nc_v4(su + (int64_t)I * 2 + 16 * i);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) uw[i] = vw[i] = make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    // part 0: du (columns col..), part 1: dv (columns I + col..)
-                    float d[32];
-#pragma unroll
-                    for (int i8 = 0; i8 < 4; ++i8) {
-                        float uu[8], vv[8];
-                        unpack_bf16x8_g(uw[i8], uu);
-                        unpack_bf16x8_g(vw[i8], vv);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int i = 8 * i8 + q;
-                            const float dh = __uint_as_float(v[c2][i]);
-                            const float sg = 1.0f / (1.0f + expf(-uu[q]));
-                            d[i] = part == 0 ? dh * vv[q] * (sg + uu[q] * sg * (1.0f - sg)) : dh * uu[q] * sg;
-                        }
-                    }
-                    const int64_t c = col + (part ? I : 0);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(d[2 * i], d[2 * i + 1]);
-                    if (valid) {
-                        uint8_t* dst = sd.out + (row * ld2 + c) * 2;
-                        st_v8(dst, pk);
-                        st_v8(dst + 32, pk + 8);
-                    }
-                    if constexpr (MX) {
-                        const uint8_t sc = mx_quantize32(d, pk);
-                        if (valid) {
-                            st_v8(sd.out2 + row * ld2 + c, pk);
-                            sd.out2_sf[row * (ld2 / 32) + c / 32] = sc;
-                        }
-                    }
-                }
-            }
-            }
         } else {
             // GEMM2: y tile in BF16, this warp's 128 of the 256 columns (one wait,
             // release, then convert and store)
@@ -532,8 +446,9 @@ __device__ void epilogue_role(const Pipe& p, const GemmSides& sides, Src& src) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(__uint_as_float(v[c4][2 * i]), __uint_as_float(v[c4][2 * i + 1]));
-                if (valid) {
-                    uint8_t* dst = sd.out + (row * sd.out_ld + tl.n * BN + 32 * (half * 4 + c4)) * 2;
+                const int col = tl.n * BN + 32 * (half * 4 + c4);
+                if (valid && col < sd.n_valid) {
+                    uint8_t* dst = sd.out + (row * sd.out_ld + col) * 2;
                     st_v8(dst, pk);
                     st_v8(dst + 32, pk + 8);
                 }

@@ -39,7 +39,6 @@ namespace moe {
 template <int KIND, bool SAVE = false>
 struct ExpertTiles {
     static constexpr bool kDeps = false;        // inputs are always ready
-    static constexpr int kKinds = 1 << KIND;    // the one tile kind of this launch
     static constexpr bool kSaveUV = SAVE;       // GEMM1 also stores u|v (training)
     static constexpr int kind = KIND;
     const int32_t* offsets;   // [E+1]
@@ -181,6 +180,7 @@ bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2)
     s2->out = (uint8_t*)c.y;
     s2->out_sf = nullptr;
     s2->out_ld = c.H;
+    s2->n_valid = c.H;
     m->s1a = CUtensorMap{};
     m->s2a = CUtensorMap{};
     if (mx) {
@@ -213,10 +213,11 @@ cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------- backward (dgrad)
-// dgrad of GEMM2 (kind 2): dh = dy . W_down over A = dy [rows][H] (K = H) and the
-// transposed-packed W_down (N = I, padded to 256-column tiles), epilogue = SwiGLU
-// backward -> du|dv.  dgrad of GEMM1 (kind 1): da = [du dv] . [W_gate; W_up] over
-// A = du|dv [rows][2I] (K = 2I) and the transposed-packed W_gate_up (N = H).
+// dgrad of GEMM2: dh = dy . W_down over A = dy [rows][H] (K = H) and the
+// transposed-packed W_down (N = I, padded to 256-column tiles), stored as BF16;
+// the SwiGLU derivative (backward.cu) then makes du|dv; dgrad of GEMM1:
+// da = [du dv] . [W_gate; W_up] over A = du|dv [rows][2I] (K = 2I) and the
+// transposed-packed W_gate_up (N = H).  Both run the GEMM2 form of the kernel.
 cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
     if (c.T == 0) return cudaSuccess;
     const bool mx = c.mx;
@@ -237,20 +238,17 @@ cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
         uint32_t box[2] = {bk, 128};
         if (!encode_tmap(&m_duv, dt, 2, a1, dims, str, box)) return cudaErrorInvalidValue;
     }
-    GemmSide s2{};   // dgrad of GEMM2
+    GemmSide s2{};   // dgrad of GEMM2 -> dh
     s2.K = c.H;
     s2.n_tiles = (c.I + tc::BN - 1) / tc::BN;
     s2.a_rows = c.a_rows;
     s2.a_sf = (const uint8_t*)c.dy_sf;
     s2.b_pk = (const uint8_t*)c.wt_down;
     s2.sfb_pk = (const uint8_t*)c.wt_d_sf;
-    s2.out = (uint8_t*)c.duv;
-    s2.out_ld = 2 * c.I;
-    s2.aux = (uint8_t*)c.uv;
-    s2.out2 = (uint8_t*)c.duv_q;
-    s2.out2_sf = (uint8_t*)c.duv_sf;
+    s2.out = (uint8_t*)c.dh;
+    s2.out_ld = c.I;
     s2.n_valid = c.I;
-    GemmSide s1{};   // dgrad of GEMM1
+    GemmSide s1{};   // dgrad of GEMM1 -> da
     s1.K = 2 * c.I;
     s1.n_tiles = c.H / tc::BN;
     s1.a_rows = c.a_rows;
@@ -259,23 +257,21 @@ cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
     s1.sfb_pk = (const uint8_t*)c.wt_gu_sf;
     s1.out = (uint8_t*)c.da;
     s1.out_ld = c.H;
+    s1.n_valid = c.H;
     if (mx) {
         s2.sf_tma = (c.H % 512) == 0;
         s1.sf_tma = ((2 * c.I) % 512) == 0;
         if (s2.sf_tma && !encode_sfa_map(&s_dy, c.dy_sf, c.a_rows, c.H)) return cudaErrorInvalidValue;
         if (s1.sf_tma && !encode_sfa_map(&s_duv, c.duv_sf, c.a_rows, 2 * c.I)) return cudaErrorInvalidValue;
     }
-    cudaError_t err;
-    if (mx) {
-        err = launch_one<true, 2>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
-        if (err != cudaSuccess) return err;
-        err = launch_one<true, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
-    } else {
-        err = launch_one<false, 2>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
-        if (err != cudaSuccess) return err;
-        err = launch_one<false, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
-    }
-    return err;
+    cudaError_t err = mx ? launch_one<true, 1>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                         : launch_one<false, 1>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+    if (err != cudaSuccess) return err;
+    err = launch_swiglu_backward(mx, c.dh, c.uv, c.T, c.I, c.duv, (uint8_t*)c.duv_q, (uint8_t*)c.duv_sf,
+                                 c.num_sms, stream);
+    if (err != cudaSuccess) return err;
+    return mx ? launch_one<true, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+              : launch_one<false, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
 }
 
 }  // namespace moe

@@ -81,6 +81,7 @@ struct TcDgradCall {
     const void* wt_d_sf;
     const void* wt_gate_up;   // transposed-packed W_gate_up (N = H, K = 2I)
     const void* wt_gu_sf;
+    void* dh;                 // [a_rows][I] BF16 scratch
     void* duv;                // [a_rows][2I] BF16 (out)
     void* duv_q;              // [a_rows][2I] codes (MXFP8, out)
     void* duv_sf;             // [a_rows][2I/32] (MXFP8, out)
@@ -88,8 +89,13 @@ struct TcDgradCall {
     WsHeader* ws;
     unsigned long long timeout_ns;
     int grid;
+    int num_sms;
 };
 cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream);
+// du = dh * v * silu'(u), dv = dh * silu(u) from BF16 dh [T][I] and u|v [T][2I] ->
+// du|dv BF16 [T][2I] and, MXFP8, codes [T][2I] + scales [T][2I/32] along I.
+cudaError_t launch_swiglu_backward(bool mx, const void* dh, const void* uv, int T, int I, void* duv,
+                                   uint8_t* duv_q, uint8_t* duv_sf, int num_sms, cudaStream_t stream);
 
 // Backward memory-bound steps (backward.cu).
 constexpr int kRouterPiece = 256;   // slots per router-wgrad piece
@@ -131,6 +137,7 @@ struct WgradCall {
     void* dw_gate_up;         // [E][2I][H] BF16 (out)
     void* dw_down;            // [E][H][I] BF16 (out)
     int32_t* pstage;          // [E+1] scratch
+    int32_t* blk_e;           // [wgrad_max_padded_slots / 32] scratch
     uint8_t *img_duv, *sf_duv, *img_x, *sf_x, *img_dy, *sf_dy, *img_h, *sf_h;   // scratch
     WsHeader* ws;
     unsigned long long timeout_ns;

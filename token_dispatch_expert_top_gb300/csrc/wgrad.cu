@@ -21,30 +21,41 @@
 // memory.  A B tile (256 rows) is two adjacent images: one bulk copy.
 //
 // GEMM.  One persistent CTA of 12 warps per SM over tiles (expert, GEMM, n, m):
-//   warp 0   producer: bulk copies of the A and B images (and scale images)
+//   warp 0   producer: bulk copies of the A and B images (and scale images) into
+//            a 3-stage ring
 //   warp 1   TMEM owner + MMA issuer; the last K-stage of an expert issues only
 //            the 32-slot (MXFP8) or 16-slot (BF16) steps that hold slots
-//   warps 4-11 epilogue: accumulator -> BF16 -> dW (zeros when the expert has
-//            no slots)
+//   warp 3   (prologue) lists the experts with and without slots
+//   warps 4-11 epilogue: accumulator -> BF16 -> a 64 KB staging tile in shared
+//            memory -> TMA tensor stores into dW (zeros when the expert has no
+//            slots); the stores run asynchronously while the next tile computes
+// Each CTA interleaves its share of MMA-bound tiles with its share of the
+// store-bound zero tiles of idle experts (WgSchedule).
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT and stops.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 
 namespace wg {
-constexpr int STAGES = 4;
+constexpr int STAGES = 3;
 constexpr int IMG = 16384;                     // one 128-row x 128-byte image
 constexpr int A_BYTES = IMG, B_BYTES = 2 * IMG;
 constexpr int SFA_BYTES = 512, SFB_BYTES = 1024;
+constexpr int C_BYTES = 128 * 256 * 2;         // output tile staging (BF16)
+constexpr int BOX = 32 * 128;                  // one TMA store box: 32 rows x 64 BF16
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+constexpr int OFF_SFA = OFF_C + C_BYTES;
 constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 3;       // full, empty, tfull, tempty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM = OFF_MISC + 16;
+constexpr int OFF_LIST = OFF_MISC + 16;        // experts with / without slots (2 x 1024 ints)
+constexpr int MAX_E = 1024;
+constexpr int SMEM = OFF_LIST + 2 * MAX_E * 4 + 16;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (4 + EPI_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
@@ -54,8 +65,10 @@ constexpr int TCOL_SFB = 256 + 4 * STAGES;
 
 // ------------------------------------------------------------- slot padding
 // pstage[e] = sum over e' < e of ceil(count_e' / 128): expert e's first padded
-// slot is 128 * pstage[e]; pstage[E] covers all experts.  One warp.
-__global__ void wgrad_pstage_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ pstage) {
+// slot is 128 * pstage[e]; pstage[E] covers all experts.  blk_e[b] = the expert
+// of 32-slot block b of the padded slot axis.  One warp.
+__global__ void wgrad_pstage_kernel(const int32_t* __restrict__ offsets, int E, int32_t* __restrict__ pstage,
+                                    int32_t* __restrict__ blk_e) {
     const int lane = threadIdx.x % 32;
     const int per = (E + 31) / 32;
     const int lo = min(lane * per, E), hi = min(lo + per, E);
@@ -70,7 +83,9 @@ __global__ void wgrad_pstage_kernel(const int32_t* __restrict__ offsets, int E, 
     int run = incl - s;
     for (int e = lo; e < hi; ++e) {
         pstage[e] = run;
-        run += (offsets[e + 1] - offsets[e] + 127) / 128;
+        const int n = (offsets[e + 1] - offsets[e] + 127) / 128;
+        for (int b = 4 * run; b < 4 * (run + n); ++b) blk_e[b] = e;
+        run += n;
     }
     if (lane == 31) pstage[E] = incl;
 }
@@ -78,123 +93,122 @@ __global__ void wgrad_pstage_kernel(const int32_t* __restrict__ offsets, int E, 
 // ------------------------------------------------------------- operand packing
 enum { WG_DUV = 0, WG_X = 1, WG_DY = 2, WG_H = 3 };
 
+__device__ __forceinline__ void unpack_bf16x8_w(const uint4& q, float* f) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        f[2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
+        f[2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
+    }
+}
+
 struct WgPackArgs {
     const uint16_t* src;      // DUV: du|dv [T][2I]; X: x [N][H]; DY: dout [N][H]; H: u|v [T][2I]
     const int32_t* sched;     // [T][2] (X, DY)
     const float* slot_gate;   // [T] (DY)
     const int32_t* offsets;   // [E+1]
     const int32_t* pstage;    // [E+1]
-    int E, C, ld, I, rows_per_shard, N;
+    const int32_t* blk_e;     // [padded slots / 32]
+    int E, C, Cp, ld, I, rows_per_shard, N;
     uint8_t* img;             // [Tp/KS][RB][16 KB]
     uint8_t* sf;              // MXFP8: [Tp/128][RB][512]
     int RB;                   // row blocks of 128 (R padded to 256)
 };
 
-// CTA = (32-slot block of the padded slot axis, 256 operand rows).  Phase 1: the
-// 32 slot rows' 256 values are read as contiguous 16-byte vectors into shared
+// CTA = (32-slot block of the padded slot axis, 512 operand rows).  Phase 1: the
+// 32 slot rows' 512 values are read as contiguous 16-byte vectors into shared
 // memory (zeros past the expert's slots or past C).  Phase 2: thread t takes
-// operand row c0 + t and quantises / rounds its 32 slots into the images.
+// operand rows c0 + t and c0 + 256 + t and quantises / rounds their 32 slots into
+// the images.
+constexpr int kPackCols = 512;
+constexpr int kPackPitch = kPackCols + 4;       // floats per shared row (16-byte stores spread)
+
 template <int SRC, bool MX>
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgPackArgs a, WsHeader* ws) {
-    __shared__ float tile[32][257];
-    __shared__ int s_e;
+    extern __shared__ float tile[];             // [32][kPackPitch]
     const int P0 = blockIdx.x * 32;
-    if (threadIdx.x == 0) {
-        int e = -1;
-        if (P0 < a.pstage[a.E] * 128) {
-            int lo = 0, hi = a.E;   // last e with 128 * pstage[e] <= P0
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (a.pstage[mid] * 128 <= P0) lo = mid; else hi = mid;
-            }
-            e = lo;
-        }
-        s_e = e;
-    }
-    __syncthreads();
-    const int e = s_e;
-    if (e < 0) return;
+    if (P0 >= a.pstage[a.E] * 128) return;
+    const int e = a.blk_e[blockIdx.x];
     const int local0 = P0 - a.pstage[e] * 128;
     const int cnt = a.offsets[e + 1] - a.offsets[e];
     const int s0 = a.offsets[e] + local0;
-    const int c0 = blockIdx.y * 256;
+    const int c0 = blockIdx.y * kPackCols;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int i = warp; i < 32; i += 8) {
-        const int col = c0 + lane * 8;
-        float v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = 0.f;
-        if (local0 + i < cnt && col < a.C) {
-            const int64_t s = s0 + i;
-            if constexpr (SRC == WG_DUV) {
-                const uint4 w = ld_nc_v4(a.src + s * a.ld + col);
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    v[2 * p] = bf16_to_f32((uint16_t)(ww[p] & 0xFFFF));
-                    v[2 * p + 1] = bf16_to_f32((uint16_t)(ww[p] >> 16));
-                }
-            } else if constexpr (SRC == WG_X || SRC == WG_DY) {
-                const int64_t tok = (int64_t)a.sched[2 * s] * a.rows_per_shard + a.sched[2 * s + 1];
-                if (tok >= 0 && tok < a.N) {
-                    const uint4 w = ld_nc_v4(a.src + tok * a.ld + col);
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-                    const float gs = SRC == WG_DY ? a.slot_gate[s] : 1.0f;
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float lo = bf16_to_f32((uint16_t)(ww[p] & 0xFFFF));
-                        const float hi = bf16_to_f32((uint16_t)(ww[p] >> 16));
-                        v[2 * p] = SRC == WG_DY ? gs * lo : lo;
-                        v[2 * p + 1] = SRC == WG_DY ? gs * hi : hi;
-                    }
-                } else if (lane == 0) {
-                    set_status(ws, MOE_ERR_DEVICE_CHECK);
-                }
-            } else {   // WG_H: h = silu(u) * v from the kept u|v
-                const uint4 wu = ld_nc_v4(a.src + s * a.ld + col);
-                const uint4 wv = ld_nc_v4(a.src + s * a.ld + a.I + col);
-                const uint32_t uu[4] = {wu.x, wu.y, wu.z, wu.w};
-                const uint32_t vv[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    v[2 * p] = silu_f32(bf16_to_f32((uint16_t)(uu[p] & 0xFFFF))) *
-                               bf16_to_f32((uint16_t)(vv[p] & 0xFFFF));
-                    v[2 * p + 1] = silu_f32(bf16_to_f32((uint16_t)(uu[p] >> 16))) *
-                                   bf16_to_f32((uint16_t)(vv[p] >> 16));
-                }
+        const int64_t s = s0 + i;
+        const bool live = local0 + i < cnt;
+        int64_t tok = 0;
+        float gs = 1.0f;
+        if constexpr (SRC == WG_X || SRC == WG_DY) {
+            if (live) {
+                tok = (int64_t)a.sched[2 * s] * a.rows_per_shard + a.sched[2 * s + 1];
+                if (SRC == WG_DY) gs = a.slot_gate[s];
             }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) tile[i][lane * 8 + q] = v[q];
+        for (int hv = 0; hv < 2; ++hv) {
+            const int col = c0 + hv * 256 + lane * 8;
+            float v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+            if (live && col < a.C) {
+                if constexpr (SRC == WG_DUV) {
+                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + col), v);
+                } else if constexpr (SRC == WG_X || SRC == WG_DY) {
+                    if (tok >= 0 && tok < a.N) {
+                        unpack_bf16x8_w(ld_nc_v4(a.src + tok * a.ld + col), v);
+                        if (SRC == WG_DY) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) v[q] = gs * v[q];
+                        }
+                    } else if (lane == 0) {
+                        set_status(ws, MOE_ERR_DEVICE_CHECK);
+                    }
+                } else {   // WG_H: h = silu(u) * v from the kept u|v
+                    float u[8], w[8];
+                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + col), u);
+                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + a.I + col), w);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = silu_f32(u[q]) * w[q];
+                }
+            }
+            float4* dst = reinterpret_cast<float4*>(tile + i * kPackPitch + hv * 256 + lane * 8);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
     }
     __syncthreads();
-    const int c = c0 + threadIdx.x;
-    float v[32];
+#pragma unroll 1
+    for (int hv = 0; hv < 2; ++hv) {
+        const int c = c0 + hv * 256 + threadIdx.x;
+        if (c >= a.Cp) break;
+        float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = tile[i][threadIdx.x];
-    const int rb = c / 128, r = c % 128;
-    if constexpr (MX) {
-        uint32_t codes[8];
-        const uint8_t sc = mx_quantize32(v, codes);
-        const int kb = P0 / 128, sub = (P0 % 128) / 32;
-        uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
+        for (int i = 0; i < 32; ++i) v[i] = tile[i * kPackPitch + hv * 256 + threadIdx.x];
+        const int rb = c / 128, r = c % 128;
+        if constexpr (MX) {
+            uint32_t codes[8];
+            const uint8_t sc = mx_quantize32(v, codes);
+            const int kb = P0 / 128, sub = (P0 % 128) / 32;
+            uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int q = sub * 2 + h;
-            st_v4(row + ((q ^ (r & 7)) * 16), make_uint4(codes[4 * h], codes[4 * h + 1], codes[4 * h + 2],
-                                                          codes[4 * h + 3]));
-        }
-        a.sf[((int64_t)kb * a.RB + rb) * 512 + ((r % 32) * 4 + r / 32) * 4 + sub] = sc;
-    } else {
-        uint32_t pk[16];
+            for (int h = 0; h < 2; ++h) {
+                const int q = sub * 2 + h;
+                st_v4(row + ((q ^ (r & 7)) * 16),
+                      make_uint4(codes[4 * h], codes[4 * h + 1], codes[4 * h + 2], codes[4 * h + 3]));
+            }
+            a.sf[((int64_t)kb * a.RB + rb) * 512 + ((r % 32) * 4 + r / 32) * 4 + sub] = sc;
+        } else {
+            uint32_t pk[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
-        const int kb = P0 / 64, sub = (P0 % 64) / 32;
-        uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
+            for (int q = 0; q < 16; ++q) pk[q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+            const int kb = P0 / 64, sub = (P0 % 64) / 32;
+            uint8_t* row = a.img + ((int64_t)kb * a.RB + rb) * wg::IMG + r * 128;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int q = sub * 4 + h;
-            st_v4(row + ((q ^ (r & 7)) * 16), make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]));
+            for (int h = 0; h < 4; ++h) {
+                const int q = sub * 4 + h;
+                st_v4(row + ((q ^ (r & 7)) * 16), make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]));
+            }
         }
     }
 }
@@ -207,15 +221,45 @@ struct WgTile {
     int kbase;                // first K-stage of the expert in the images
 };
 
+// The tile order of one CTA.  Tiles of experts with slots ("work", MMA-bound) and
+// of experts without ("zero", store-bound) form two lists, each expert-major then
+// N tile then M tile, and each dealt round-robin over the CTAs.  A CTA walks its
+// two shares interleaved in proportion, so the zero tiles' stores overlap the
+// work tiles' MMAs; CTAs at the same step work on the same expert, so weight-
+// gradient operands are shared through L2.
+struct WgSchedule {
+    const int32_t* work;      // experts with slots, in order (shared memory)
+    const int32_t* zero;      // experts without slots
+    int per, wc, zc, n;       // tiles per expert; this CTA's work / zero / total tile counts
+
+    __device__ void init(const int32_t* w_list, const int32_t* z_list, int nw, int nz, int per_) {
+        work = w_list;
+        zero = z_list;
+        per = per_;
+        const int G = gridDim.x, c = blockIdx.x;
+        const long long W = (long long)nw * per, Z = (long long)nz * per;
+        wc = W > c ? (int)((W - c - 1) / G + 1) : 0;
+        zc = Z > c ? (int)((Z - c - 1) / G + 1) : 0;
+        n = wc + zc;
+    }
+    // (expert, tile within the expert) of step s of this CTA
+    __device__ void at(int s, int& e, int& l) const {
+        const long long zs = n ? (long long)s * zc / n : 0, zs1 = n ? (long long)(s + 1) * zc / n : 0;
+        const long long t = zs1 > zs ? blockIdx.x + zs * (long long)gridDim.x
+                                     : blockIdx.x + (s - zs) * (long long)gridDim.x;
+        e = zs1 > zs ? zero[t / per] : work[t / per];
+        l = (int)(t % per);
+    }
+};
+
 template <bool MX>
-__device__ __forceinline__ WgTile wg_tile(int t, const WgGemm& g0, const WgGemm& g1,
+__device__ __forceinline__ WgTile wg_tile(const WgSchedule& sc, int s, const WgGemm& g0, const WgGemm& g1,
                                           const int32_t* offsets, const int32_t* pstage) {
     constexpr int KS = MX ? 128 : 64, KSTEP = MX ? 32 : 16;
     const int t0 = g0.m_tiles * g0.n_tiles;
-    const int per = t0 + g1.m_tiles * g1.n_tiles;
     WgTile w;
-    w.e = t / per;
-    int l = t % per;
+    int l;
+    sc.at(s, w.e, l);
     w.g = l >= t0;
     if (w.g) l -= t0;
     const int mt = w.g ? g1.m_tiles : g0.m_tiles;
@@ -231,6 +275,7 @@ __device__ __forceinline__ WgTile wg_tile(int t, const WgGemm& g0, const WgGemm&
 template <bool MX>
 __global__ void __launch_bounds__(wg::THREADS, 1)
     wgrad_gemm_kernel(const __grid_constant__ WgGemm g0, const __grid_constant__ WgGemm g1,
+                      const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ pstage, int E,
                       WsHeader* ws, unsigned long long timeout_ns) {
     using namespace wg;
@@ -243,6 +288,9 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
     uint64_t* tempty = tfull + 1;
     uint64_t* drain = tfull + 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    int32_t* w_list = reinterpret_cast<int32_t*>(smem + OFF_LIST);
+    int32_t* z_list = w_list + MAX_E;
+    int32_t* n_lists = reinterpret_cast<int32_t*>(smem + OFF_MISC + 8);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -259,19 +307,38 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         tmem_alloc(reinterpret_cast<uint32_t*>(smem + OFF_MISC), TMEM_COLS);
         tmem_relinquish();
     }
+    if (warp == 3) {   // the two expert lists, in expert order
+        int nw = 0, nz = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const bool has = e < E && offsets[e + 1] > offsets[e];
+            const bool none = e < E && !has;
+            const unsigned bw = __ballot_sync(0xffffffffu, has), bz = __ballot_sync(0xffffffffu, none);
+            const unsigned below = (1u << lane) - 1u;
+            if (has) w_list[nw + __popc(bw & below)] = e;
+            if (none) z_list[nz + __popc(bz & below)] = e;
+            nw += __popc(bw);
+            nz += __popc(bz);
+        }
+        if (lane == 0) {
+            n_lists[0] = nw;
+            n_lists[1] = nz;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     const unsigned long long deadline = globaltimer_ns() + timeout_ns;
-    const int total = E * (g0.m_tiles * g0.n_tiles + g1.m_tiles * g1.n_tiles);
+    WgSchedule sc;
+    sc.init(w_list, z_list, n_lists[0], n_lists[1], g0.m_tiles * g0.n_tiles + g1.m_tiles * g1.n_tiles);
 
     if (warp == 0) {
         if (lane == 0) {   // producer
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
+            for (int s = 0; s < sc.n; ++s) {
+                const WgTile w = wg_tile<MX>(sc, s, g0, g1, offsets, pstage);
                 const WgGemm& G = w.g ? g1 : g0;
                 bool ok = true;
                 for (int kb = 0; kb < w.KB; ++kb) {
@@ -304,8 +371,9 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
+            for (int s = 0; ok && s < sc.n; ++s) {
+                const WgTile w = wg_tile<MX>(sc, s, g0, g1, offsets, pstage);
+                if (w.KB == 0) continue;            // zero tiles never touch the accumulator
                 if (!mbar_wait_bounded(tempty, acc_phase ^ 1, abort_flag, ws, deadline)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < w.KB; ++kb) {
@@ -351,44 +419,64 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             }
         }
     } else if (warp >= 4) {   // epilogue
+        // Warp (q, half) owns rows 32q..32q+31 and columns 128 half..+127 of the
+        // tile: two TMA store boxes of 32 rows x 64 BF16 (128-byte swizzle) in
+        // shared memory, written from registers, then stored by lane 0.
         const int q = warp & 3;
         const int half = (warp - 4) >> 2;
+        uint8_t* box0 = smem + OFF_C + (q * 2 + half) * 2 * BOX;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const WgTile w = wg_tile<MX>(t, g0, g1, offsets, pstage);
-            const WgGemm& G = w.g ? g1 : g0;
-            if (!mbar_wait_bounded(tfull, acc_phase, abort_flag, ws, deadline)) break;
-            tc_fence_after();
+        for (int s = 0; s < sc.n; ++s) {
+            const WgTile w = wg_tile<MX>(sc, s, g0, g1, offsets, pstage);
             uint32_t v[4][32];
             if (w.KB > 0) {
+                if (!mbar_wait_bounded(tfull, acc_phase, abort_flag, ws, deadline)) break;
+                tc_fence_after();
                 const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v[c4]);
                 tmem_ld_wait();
-            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+                acc_phase ^= 1;
+            } else {   // an expert without slots: zeros, without waiting for the MMA
+                if (*abort_flag) break;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[c4][i] = 0u;
             }
-            tc_fence_before();
+            if (lane == 0) bulk_wait_group_read<0>();   // the previous tile's stores have left the boxes
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty);
-            const int64_t row = (int64_t)w.m * 128 + 32 * q + lane;
-            uint8_t* orow = G.out + (int64_t)w.e * G.out_estride + row * G.out_ld * 2;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                const int col = w.n * 256 + 32 * (half * 4 + c4);
-                if (col >= G.n_valid) continue;
-                uint32_t pk[16];
+                uint8_t* rowp = box0 + (c4 >> 1) * BOX + lane * 128;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(v[c4][2 * i]), __uint_as_float(v[c4][2 * i + 1]));
-                st_v8(orow + col * 2, pk);
-                st_v8(orow + col * 2 + 32, pk + 8);
+                for (int h = 0; h < 4; ++h) {
+                    const int qc = (c4 & 1) * 4 + h;   // 16-byte chunk of the 128-byte box row
+                    const uint32_t* f = v[c4] + 8 * h;
+                    *reinterpret_cast<uint4*>(rowp + ((qc ^ (lane & 7)) * 16)) =
+                        make_uint4(pack_bf16x2(__uint_as_float(f[0]), __uint_as_float(f[1])),
+                                   pack_bf16x2(__uint_as_float(f[2]), __uint_as_float(f[3])),
+                                   pack_bf16x2(__uint_as_float(f[4]), __uint_as_float(f[5])),
+                                   pack_bf16x2(__uint_as_float(f[6]), __uint_as_float(f[7])));
+                }
             }
-            acc_phase ^= 1;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const CUtensorMap* tm = w.g ? &tm1 : &tm0;
+                const int M = w.g ? g1.m_tiles * 128 : g0.m_tiles * 128;
+                const int y = w.e * M + w.m * 128 + 32 * q;
+                const int x = w.n * 256 + half * 128;
+                const int nv = w.g ? g1.n_valid : g0.n_valid;   // boxes wholly past it are skipped
+                if (x < nv) tma_store_2d(tm, box0, x, y);
+                if (x + 64 < nv) tma_store_2d(tm, box0 + BOX, x + 64, y);
+                bulk_commit_group();
+            }
         }
+        if (lane == 0) bulk_wait_group_all();
     }
 
     if (*abort_flag) {
@@ -408,12 +496,13 @@ cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
     const bool mx = c.mx;
     const int Ip = (c.I + 255) / 256 * 256;
     const int tp = wgrad_max_padded_slots(c.T, c.E);
-    wgrad_pstage_kernel<<<1, 32, 0, stream>>>(c.offsets, c.E, c.pstage);
+    wgrad_pstage_kernel<<<1, 32, 0, stream>>>(c.offsets, c.E, c.pstage, c.blk_e);
     WgPackArgs pa{};
     pa.sched = c.sched;
     pa.slot_gate = c.slot_gate;
     pa.offsets = c.offsets;
     pa.pstage = c.pstage;
+    pa.blk_e = c.blk_e;
     pa.E = c.E;
     pa.I = c.I;
     pa.rows_per_shard = c.rows_per_shard;
@@ -422,14 +511,23 @@ cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
         WgPackArgs q = pa;
         q.src = (const uint16_t*)p;
         q.C = C;
+        q.Cp = Cp;
         q.ld = ld;
         q.img = img;
         q.sf = sf;
         q.RB = Cp / 128;
-        const dim3 grid((unsigned)(tp / 32), (unsigned)(Cp / 256));
+        const dim3 grid((unsigned)(tp / 32), (unsigned)((Cp + kPackCols - 1) / kPackCols));
+        const size_t sm = sizeof(float) * 32 * kPackPitch;
 #define MOE_WG_PACK(S)                                                                                \
-    if (mx) wgrad_pack_kernel<S, true><<<grid, 256, 0, stream>>>(q, c.ws);                          \
-    else wgrad_pack_kernel<S, false><<<grid, 256, 0, stream>>>(q, c.ws)
+    if (mx) {                                                                                         \
+        cudaFuncSetAttribute(wgrad_pack_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             (int)sm);                                                                \
+        wgrad_pack_kernel<S, true><<<grid, 256, sm, stream>>>(q, c.ws);                               \
+    } else {                                                                                          \
+        cudaFuncSetAttribute(wgrad_pack_kernel<S, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,\
+                             (int)sm);                                                                \
+        wgrad_pack_kernel<S, false><<<grid, 256, sm, stream>>>(q, c.ws);                              \
+    }
         switch (src) {
             case WG_DUV: MOE_WG_PACK(WG_DUV); break;
             case WG_X: MOE_WG_PACK(WG_X); break;
@@ -471,17 +569,34 @@ cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
     g1.out = (uint8_t*)c.dw_down;
     g1.out_estride = (int64_t)c.H * c.I * 2;
     g1.out_ld = c.I;
+    // TMA store maps over the two gradients: [E*2I][H] and [E*H][I] BF16, boxes of
+    // 32 rows x 64 columns with 128-byte swizzle; columns past I are clipped.
+    CUtensorMap tm0, tm1;
+    {
+        uint64_t dims[2] = {(uint64_t)c.H, (uint64_t)c.E * 2 * c.I};
+        uint64_t str[1] = {(uint64_t)c.H * 2};
+        uint32_t box[2] = {64, 32};
+        if (!encode_tmap(&tm0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.dw_gate_up, dims, str, box))
+            return cudaErrorInvalidValue;
+    }
+    {
+        uint64_t dims[2] = {(uint64_t)c.I, (uint64_t)c.E * c.H};
+        uint64_t str[1] = {(uint64_t)c.I * 2};
+        uint32_t box[2] = {64, 32};
+        if (!encode_tmap(&tm1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c.dw_down, dims, str, box))
+            return cudaErrorInvalidValue;
+    }
     const size_t smem = 1024 + wg::SMEM;
     if (mx) {
         err = cudaFuncSetAttribute(wgrad_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        wgrad_gemm_kernel<true><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, c.offsets, c.pstage, c.E, c.ws,
-                                                                       c.timeout_ns);
+        wgrad_gemm_kernel<true><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, tm0, tm1, c.offsets, c.pstage,
+                                                                       c.E, c.ws, c.timeout_ns);
     } else {
         err = cudaFuncSetAttribute(wgrad_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        wgrad_gemm_kernel<false><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, c.offsets, c.pstage, c.E, c.ws,
-                                                                        c.timeout_ns);
+        wgrad_gemm_kernel<false><<<c.grid, wg::THREADS, smem, stream>>>(g0, g1, tm0, tm1, c.offsets, c.pstage,
+                                                                        c.E, c.ws, c.timeout_ns);
     }
     return cudaGetLastError();
 }
