@@ -134,49 +134,63 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
     const int s0 = a.offsets[e] + local0;
     const int c0 = blockIdx.y * kPackCols;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    for (int i = warp; i < 32; i += 8) {
-        const int64_t s = s0 + i;
-        const bool live = local0 + i < cnt;
-        int64_t tok = 0;
-        float gs = 1.0f;
+    // Each warp takes slot rows warp, warp+8, warp+16, warp+24: their indices
+    // first, then all their row loads, so the dependent chain (schedule entry,
+    // token, row) is waited on once per warp, not once per row.
+    bool live[4];
+    int64_t src_row[4];
+    float gs[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = warp + 8 * j;
+        const int64_t sl = s0 + i;
+        live[j] = local0 + i < cnt;
+        src_row[j] = sl;
+        gs[j] = 1.0f;
         if constexpr (SRC == WG_X || SRC == WG_DY) {
-            if (live) {
-                tok = (int64_t)a.sched[2 * s] * a.rows_per_shard + a.sched[2 * s + 1];
-                if (SRC == WG_DY) gs = a.slot_gate[s];
+            if (live[j]) {
+                const int64_t tok = (int64_t)a.sched[2 * sl] * a.rows_per_shard + a.sched[2 * sl + 1];
+                if (SRC == WG_DY) gs[j] = a.slot_gate[sl];
+                if (tok < 0 || tok >= a.N) {
+                    if (lane == 0) set_status(ws, MOE_ERR_DEVICE_CHECK);
+                    live[j] = false;
+                }
+                src_row[j] = tok;
             }
         }
+    }
+    constexpr int NV = SRC == WG_H ? 2 : 1;     // vectors per column group (u and v for h)
+    uint4 raw[4][2][NV];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int hv = 0; hv < 2; ++hv) {
             const int col = c0 + hv * 256 + lane * 8;
+            const bool ok = live[j] && col < a.C;
+#pragma unroll
+            for (int t = 0; t < NV; ++t)
+                raw[j][hv][t] = ok ? ld_nc_v4(a.src + src_row[j] * a.ld + (t ? a.I : 0) + col)
+                                   : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
             float v[8];
+            unpack_bf16x8_w(raw[j][hv][0], v);
+            if constexpr (SRC == WG_DY) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) v[q] = 0.f;
-            if (live && col < a.C) {
-                if constexpr (SRC == WG_DUV) {
-                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + col), v);
-                } else if constexpr (SRC == WG_X || SRC == WG_DY) {
-                    if (tok >= 0 && tok < a.N) {
-                        unpack_bf16x8_w(ld_nc_v4(a.src + tok * a.ld + col), v);
-                        if (SRC == WG_DY) {
+                for (int q = 0; q < 8; ++q) v[q] = gs[j] * v[q];
+            } else if constexpr (SRC == WG_H) {   // h = silu(u) * v from the kept u|v
+                float w2[8];
+                unpack_bf16x8_w(raw[j][hv][1], w2);
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) v[q] = gs * v[q];
-                        }
-                    } else if (lane == 0) {
-                        set_status(ws, MOE_ERR_DEVICE_CHECK);
-                    }
-                } else {   // WG_H: h = silu(u) * v from the kept u|v
-                    float u[8], w[8];
-                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + col), u);
-                    unpack_bf16x8_w(ld_nc_v4(a.src + s * a.ld + a.I + col), w);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = silu_f32(u[q]) * w[q];
-                }
+                for (int q = 0; q < 8; ++q) v[q] = silu_f32(v[q]) * w2[q];
             }
-            float4* dst = reinterpret_cast<float4*>(tile + i * kPackPitch + hv * 256 + lane * 8);
+            float4* dst = reinterpret_cast<float4*>(tile + (warp + 8 * j) * kPackPitch + hv * 256 + lane * 8);
             dst[0] = make_float4(v[0], v[1], v[2], v[3]);
             dst[1] = make_float4(v[4], v[5], v[6], v[7]);
         }
-    }
     __syncthreads();
 #pragma unroll 1
     for (int hv = 0; hv < 2; ++hv) {
