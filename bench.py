@@ -523,16 +523,31 @@ def train_arm(args, rank, world):
     flops = w.ffn_flops                      # each of dgrad and wgrad: 6*H*I per slot
     dgrad_tf = flops / (stage_ms["expert_dgrad"] / 1e3) / 1e12
     wgrad_tf = flops / (stage_ms["expert_wgrad"] / 1e3) / 1e12
+    # wgrad writes every expert's BF16 gradients (zeros for idle experts) and reads its
+    # inputs once: du|dv (4I B), the x and g*dY rows (2H B each) and u|v (4I B) per slot
+    wgrad_bytes = w.E * 3 * w.I * w.H * 2 + w.T * (4 * w.I + 2 * w.H + 2 * w.H + 4 * w.I)
+    hbm = peaks["hbm_gbs"]
     dom = "expert_wgrad" if stage_ms["expert_wgrad"] >= stage_ms["expert_dgrad"] else "expert_dgrad"
-    dom_tf = wgrad_tf if dom == "expert_wgrad" else dgrad_tf
-    roofline = {
-        "kernel": ("expert wgrad (slot padding, four operand packs, grouped GEMM)" if dom == "expert_wgrad"
-                   else "expert dgrad grouped GEMMs (two launches)"),
-        "bound": "tensor", "achieved": round(dom_tf, 2), "peak": round(tensor_peak, 1),
-        "unit": "TFLOP/s", "frac": round(dom_tf / tensor_peak, 4), "traffic": None,
-        "peak_source": f"{peak_src} sustained BF16" + (f" x {FP8_PER_BF16:g}" if w.dtype == "mxfp8" else ""),
-        "algorithmic": f"{flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
-    }
+    if dom == "expert_wgrad" and wgrad_bytes / (hbm * 1e9) > flops / (tensor_peak * 1e12):
+        gbs = wgrad_bytes / (stage_ms["expert_wgrad"] / 1e3) / 1e9
+        roofline = {
+            "kernel": "expert wgrad (slot padding, four operand packs, grouped GEMM)",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(gbs / hbm, 4), "traffic": None, "peak_source": f"{peak_src} copy",
+            "algorithmic": (f"{wgrad_bytes / 1e9:.2f} GB per call: BF16 gradients of {w.E} experts "
+                            f"(6*I*H B each) + du|dv, x, g*dY and u|v rows read once per slot; "
+                            f"the compute floor {flops / (tensor_peak * 1e12) * 1e3:.2f} ms is lower"),
+        }
+    else:
+        dom_tf = wgrad_tf if dom == "expert_wgrad" else dgrad_tf
+        roofline = {
+            "kernel": ("expert wgrad (slot padding, four operand packs, grouped GEMM)" if dom == "expert_wgrad"
+                       else "expert dgrad (two grouped GEMMs and the SwiGLU derivative)"),
+            "bound": "tensor", "achieved": round(dom_tf, 2), "peak": round(tensor_peak, 1),
+            "unit": "TFLOP/s", "frac": round(dom_tf / tensor_peak, 4), "traffic": None,
+            "peak_source": f"{peak_src} sustained BF16" + (f" x {FP8_PER_BF16:g}" if w.dtype == "mxfp8" else ""),
+            "algorithmic": f"{flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
+        }
     counts = np.bincount(layer.saved["idx"].cpu().numpy().ravel(), minlength=w.E)
     res = {
         "metric": "MoE layer training step (forward + backward) tokens/s", "value":
@@ -547,7 +562,8 @@ def train_arm(args, rank, world):
                    "empty_experts": int((counts == 0).sum())},
         "forward_ms": round(fwd_ms, 4),
         "backward_stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "dgrad_tflops": round(dgrad_tf, 2), "wgrad_tflops": round(wgrad_tf, 2),
+        "dgrad_tflops": round(dgrad_tf, 2), "dgrad_frac_tensor": round(dgrad_tf / tensor_peak, 4),
+        "wgrad_tflops": round(wgrad_tf, 2),
         "roofline": roofline,
         "gpu_launches": train_launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
