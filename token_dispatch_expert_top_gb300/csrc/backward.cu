@@ -238,51 +238,66 @@ cudaError_t launch_reverse_combine(bool mx, const void* dout, const void* y, con
 }
 
 // ------------------------------------------------------------- SwiGLU backward
-// One thread per (slot row t, 32-column block of I), consecutive threads on
-// consecutive blocks of a row: with s = sigma(u),
+// One thread per (slot row t, 8 consecutive columns of I); four consecutive lanes
+// hold one 32-column MX block (I/8 is a multiple of 4, so blocks never straddle a
+// row).  With s = sigma(u):
 //   du = dh * v * (s + u s (1 - s)),   dv = dh * u * s
 // from BF16 dh and the kept BF16 u|v, in FP32; du|dv stored as BF16 (du in
-// columns 0..I-1, dv in I..2I-1) and, MXFP8, quantised along I per 32-block.
+// columns 0..I-1, dv in I..2I-1) and, MXFP8, quantised along I per 32-block (the
+// block amax combined over the four lanes, then the row quantiser's rule).
 template <bool MX>
 __global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t* __restrict__ dh,
                                                               const uint16_t* __restrict__ uv, int T, int I,
                                                               uint16_t* __restrict__ duv,
                                                               uint8_t* __restrict__ duv_q,
                                                               uint8_t* __restrict__ duv_sf) {
-    const int nb = I / 32;
-    const int64_t total = (int64_t)T * nb;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
-         b += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = b / nb;
-        const int col = (int)(b % nb) * 32;
-        float d[32], u[32], v[32];
+    const int ng = I / 8;
+    const int64_t total = (int64_t)T * ng;
+    const int lane = threadIdx.x % 32;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // every lane of a warp runs the same number of iterations (the shuffles need all 32)
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x - lane); base < total; base += stride) {
+        const int64_t b = base + lane;
+        const bool ok = b < total;
+        const int64_t r = ok ? b / ng : 0;
+        const int col = ok ? (int)(b % ng) * 8 : 0;
+        float d[8], u[8], v[8];
+        if (ok) {
+            unpack_bf16x8(ld_nc_v4(dh + r * I + col), d);
+            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + col), u);
+            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + I + col), v);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            unpack_bf16x8(ld_nc_v4(dh + r * I + col + 8 * i), d + 8 * i);
-            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + col + 8 * i), u + 8 * i);
-            unpack_bf16x8(ld_nc_v4(uv + r * 2 * I + I + col + 8 * i), v + 8 * i);
+            for (int q = 0; q < 8; ++q) d[q] = u[q] = v[q] = 0.f;
         }
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-            float o[32];
+            float o[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float s = 1.0f / (1.0f + expf(-u[i]));
-                o[i] = part == 0 ? d[i] * v[i] * (s + u[i] * s * (1.0f - s)) : d[i] * u[i] * s;
+            for (int q = 0; q < 8; ++q) {
+                const float s = 1.0f / (1.0f + expf(-u[q]));
+                o[q] = part == 0 ? d[q] * v[q] * (s + u[q] * s * (1.0f - s)) : d[q] * u[q] * s;
             }
             const int64_t c = col + (part ? I : 0);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
-            uint16_t* dst = duv + r * 2 * I + c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) st_v4(dst + 8 * i, make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
+            if (ok)
+                st_v4(duv + r * 2 * I + c, make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                                      pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7])));
             if constexpr (MX) {
-                const uint8_t sc = mx_quantize32(o, pk);
-                uint8_t* q = duv_q + r * 2 * I + c;
-                st_v4(q, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-                st_v4(q + 16, make_uint4(pk[4], pk[5], pk[6], pk[7]));
-                duv_sf[r * (2 * I / 32) + c / 32] = sc;
+                float amax = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(o[q]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const int se = mx_scale_exponent(amax);
+                const float is = mx_inv_scale(se);
+                const uint32_t lo = (uint32_t)cvt_e4m3x2(o[0] * is, o[1] * is) |
+                                    ((uint32_t)cvt_e4m3x2(o[2] * is, o[3] * is) << 16);
+                const uint32_t hi = (uint32_t)cvt_e4m3x2(o[4] * is, o[5] * is) |
+                                    ((uint32_t)cvt_e4m3x2(o[6] * is, o[7] * is) << 16);
+                if (ok) {
+                    *reinterpret_cast<uint2*>(duv_q + r * 2 * I + c) = make_uint2(lo, hi);
+                    if ((lane & 3) == 0) duv_sf[r * (2 * I / 32) + c / 32] = (uint8_t)(se + 127);
+                }
             }
         }
     }
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t* __
 
 cudaError_t launch_swiglu_backward(bool mx, const void* dh, const void* uv, int T, int I, void* duv,
                                    uint8_t* duv_q, uint8_t* duv_sf, int num_sms, cudaStream_t stream) {
-    const int64_t total = (int64_t)T * (I / 32);
+    const int64_t total = (int64_t)T * (I / 8);
     if (total == 0) return cudaSuccess;
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
