@@ -122,10 +122,16 @@ struct WgPackArgs {
 // the images.
 constexpr int kPackCols = 512;
 constexpr int kPackPitch = kPackCols + 4;       // floats per shared row (16-byte stores spread)
+constexpr int kPackPitch16 = kPackCols + 8;     // BF16 elements per shared row
 
 template <int SRC, bool MX>
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgPackArgs a, WsHeader* ws) {
-    extern __shared__ float tile[];             // [32][kPackPitch]
+    // BF16 sources (du|dv, x) are staged as their raw BF16 bits, which is exact and
+    // halves the shared memory (more CTAs per SM); computed ones (g*dY, h) as FP32.
+    constexpr bool RAW = SRC == WG_DUV || SRC == WG_X;
+    extern __shared__ uint4 smem_pack[];
+    float* tile = reinterpret_cast<float*>(smem_pack);        // [32][kPackPitch] FP32
+    uint16_t* tile16 = reinterpret_cast<uint16_t*>(smem_pack); // [32][kPackPitch16] BF16
     const int P0 = blockIdx.x * 32;
     if (P0 >= a.pstage[a.E] * 128) return;
     const int e = a.blk_e[blockIdx.x];
@@ -176,6 +182,11 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
     for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int hv = 0; hv < 2; ++hv) {
+            if constexpr (RAW) {
+                *reinterpret_cast<uint4*>(tile16 + (warp + 8 * j) * kPackPitch16 + hv * 256 + lane * 8) =
+                    raw[j][hv][0];
+                continue;
+            }
             float v[8];
             unpack_bf16x8_w(raw[j][hv][0], v);
             if constexpr (SRC == WG_DY) {
@@ -198,7 +209,9 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
         if (c >= a.Cp) break;
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = tile[i * kPackPitch + hv * 256 + threadIdx.x];
+        for (int i = 0; i < 32; ++i)
+            v[i] = RAW ? bf16_to_f32(tile16[i * kPackPitch16 + hv * 256 + threadIdx.x])
+                       : tile[i * kPackPitch + hv * 256 + threadIdx.x];
         const int rb = c / 128, r = c % 128;
         if constexpr (MX) {
             uint32_t codes[8];
@@ -531,7 +544,8 @@ cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
         q.sf = sf;
         q.RB = Cp / 128;
         const dim3 grid((unsigned)(tp / 32), (unsigned)((Cp + kPackCols - 1) / kPackCols));
-        const size_t sm = sizeof(float) * 32 * kPackPitch;
+        const size_t sm = (src == WG_DUV || src == WG_X) ? sizeof(uint16_t) * 32 * kPackPitch16
+                                                         : sizeof(float) * 32 * kPackPitch;
 #define MOE_WG_PACK(S)                                                                                \
     if (mx) {                                                                                         \
         cudaFuncSetAttribute(wgrad_pack_kernel<S, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
