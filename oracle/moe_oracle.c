@@ -97,6 +97,78 @@ ORC_API uint8_t orc_e4m3_encode(double v) {
     return sign | code;
 }
 
+/* NVFP4 (a reading of NVIDIA's published format: the pages only name it): E2M1
+ * elements -- sign, 2 exponent bits (bias 1), 1 mantissa bit, magnitudes
+ * {0, 0.5, 1, 1.5, 2, 3, 4, 6}, no infinities or NaN -- with one E4M3 scale per 16
+ * consecutive elements along K and one FP32 scale per tensor. */
+ORC_API double orc_e2m1_decode(uint8_t code) {
+    int s = (code >> 3) & 1, ex = (code >> 1) & 3, m = code & 1;
+    double mag = (ex == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, ex - 1);
+    return s ? -mag : mag;
+}
+
+/* Round to nearest-even E2M1, saturating magnitudes above 6 to 6; the sign of
+ * zero is kept.  Returns the 4-bit code. */
+ORC_API uint8_t orc_e2m1_encode(double v) {
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = round_to_format(fabs(v), 1, 0);
+    if (a > 6.0) a = 6.0;
+    if (a == 0.0) return sign;
+    if (a < 1.0) return sign | 1;                                /* subnormal 0.5 */
+    int E;
+    frexp(a, &E);
+    int e = E - 1;                                               /* a = (1 + m/2) 2^e */
+    int m = (int)(a / ldexp(1.0, e) * 2.0) - 2;
+    return sign | (uint8_t)(((e + 1) << 1) | m);
+}
+
+/* Per-tensor scale: amax / (6 * 448) in FP32 (1 for an all-zero tensor), so the
+ * largest block scale lands at the top of E4M3's range. */
+ORC_API double orc_nvfp4_tensor_scale(const double* in, int64_t n) {
+    double amax = 0.0;
+    for (int64_t i = 0; i < n; ++i) amax = fmax(amax, fabs(in[i]));
+    return amax > 0.0 ? orc_round_f32(amax / 2688.0) : 1.0;
+}
+
+/* NVFP4 quantisation along K of a [rows][K] matrix of FP32 values with tensor
+ * scale st.  Per block of 16: t = fp32(fp32(amax / 6) / st), its E4M3 code is the
+ * block scale sb; d = fp32(sb * st); every element is the E2M1 code of
+ * fp32(x / d) (code 0 when d is 0).  Codes are packed two per byte, the lower
+ * element in the low nibble: codes [rows][K/2], scales [rows][K/16].  Every FP32
+ * step is one correctly rounded operation (an FP64 result rounded once is the
+ * FP32 result for these operations). */
+ORC_API void orc_quantize_nvfp4(const double* in, int64_t rows, int64_t K, double st,
+                                uint8_t* codes, uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            const double* v = in + r * K + b * 16;
+            double amax = 0.0;
+            for (int t = 0; t < 16; ++t) amax = fmax(amax, fabs(v[t]));
+            double t6 = orc_round_f32(orc_round_f32(amax / 6.0) / st);
+            uint8_t sb = orc_e4m3_encode(t6);
+            double d = orc_round_f32(orc_e4m3_decode(sb) * st);
+            scales[r * (K / 16) + b] = sb;
+            for (int t = 0; t < 16; t += 2) {
+                uint8_t lo = d == 0.0 ? 0 : orc_e2m1_encode(orc_round_f32(v[t] / d));
+                uint8_t hi = d == 0.0 ? 0 : orc_e2m1_encode(orc_round_f32(v[t + 1] / d));
+                codes[r * (K / 2) + b * 8 + t / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    }
+}
+
+ORC_API void orc_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows,
+                                  int64_t K, double st, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < K; ++c) {
+            uint8_t byte = codes[r * (K / 2) + c / 2];
+            uint8_t q = (c & 1) ? (byte >> 4) : (byte & 15);
+            out[r * K + c] = orc_e2m1_decode(q) * orc_e4m3_decode(scales[r * (K / 16) + c / 16]) * st;
+        }
+}
+
 ORC_API void orc_round_bf16_array(const double* in, int64_t n, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_round_bf16(in[i]);
 }

@@ -84,6 +84,14 @@ def lib():
         L.orc_layout.argtypes = [_i32p, _i64, _int, _int, _int, _i32p, _i32p, _i32p, _i32p]
         L.orc_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
         L.orc_combine.argtypes = [_f64p, _i32p, _f64p, _i64, _int, _i64, _f64p]
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e2m1_encode.restype = ctypes.c_uint8
+        L.orc_e2m1_encode.argtypes = [ctypes.c_double]
+        L.orc_nvfp4_tensor_scale.restype = ctypes.c_double
+        L.orc_nvfp4_tensor_scale.argtypes = [_f64p, _i64]
+        L.orc_quantize_nvfp4.argtypes = [_f64p, _i64, _i64, ctypes.c_double, _u8p, _u8p]
+        L.orc_dequantize_nvfp4.argtypes = [_u8p, _u8p, _i64, _i64, ctypes.c_double, _f64p]
         L.orc_swiglu_backward.argtypes = [_f64p, _f64p, _f64p, _i64, _f64p, _f64p]
         L.orc_gate_backward.argtypes = [_f64p, _f64p, _i64, _int, _f64p]
         _lib = L
@@ -151,6 +159,40 @@ def dequantize_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
 def mxfp8_values(a: np.ndarray) -> np.ndarray:
     """The values an MXFP8 operand holds after quantising a along its last axis."""
     return dequantize_mxfp8(*quantize_mxfp8(a))
+
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    f = lib().orc_e2m1_decode
+    table = np.array([f(c) for c in range(16)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8) & 15]
+
+
+def e2m1_encode(a) -> np.ndarray:
+    f = lib().orc_e2m1_encode
+    a = np.asarray(a, dtype=np.float64)
+    return np.array([f(float(v)) for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
+
+
+def quantize_nvfp4(a: np.ndarray):
+    """[rows, K] FP32 values -> (codes [rows, K/2] u8 (two E2M1 per byte, lower
+    element in the low nibble), scales [rows, K/16] E4M3 u8, tensor scale float)."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    rows, K = a.shape
+    assert K % 16 == 0
+    st = lib().orc_nvfp4_tensor_scale(a.ravel(), a.size)
+    codes = np.empty((rows, K // 2), dtype=np.uint8)
+    scales = np.empty((rows, K // 16), dtype=np.uint8)
+    lib().orc_quantize_nvfp4(a, rows, K, st, codes, scales)
+    return codes, scales, st
+
+
+def dequantize_nvfp4(codes: np.ndarray, scales: np.ndarray, st: float) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, K = codes.shape[0], codes.shape[1] * 2
+    out = np.empty((rows, K), dtype=np.float64)
+    lib().orc_dequantize_nvfp4(codes, scales, rows, K, float(st), out)
+    return out
 
 
 def round_to(a: np.ndarray, fmt: str) -> np.ndarray:

@@ -10,6 +10,7 @@ import oracle as O
 import test_oracle_backward as B
 import test_oracle_formats as F
 import test_oracle_layer as L
+import test_oracle_nvfp4 as N
 
 
 def _fails(fn, *args):
@@ -105,6 +106,34 @@ def _gate_backward_drops_mean(orig):
     return lambda gate, dgate: np.asarray(gate) * np.asarray(dgate)
 
 
+def _nvfp4_nibbles_swapped(orig):
+    def f(a):
+        q, s, st = orig(a)
+        return ((q >> 4) | (q << 4)).astype(np.uint8), s, st
+    return f
+
+
+def _nvfp4_scale_without_tensor_scale(orig):
+    def f(a):
+        q, s, st = orig(a)              # block scales taken on amax/6 alone, st dropped
+        e4 = O.lib().orc_e4m3_encode
+        amax = np.abs(np.asarray(a, dtype=np.float64)).reshape(a.shape[0], -1, 16).max(axis=2)
+        s2 = np.vectorize(lambda t: e4(float(np.float32(t))))(amax / 6.0).astype(np.uint8)
+        return q, s2, 1.0
+    return f
+
+
+def _e2m1_ties_away(orig):
+    def f(v):
+        v = np.asarray(v, dtype=np.float64)
+        a = np.minimum(np.abs(v), 6.0)
+        mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+        d = np.abs(a[..., None] - mags)
+        code = (d.shape[-1] - 1 - np.argmin(d[..., ::-1], axis=-1)).astype(np.uint8)
+        return code | np.where(np.signbit(v), 8, 0).astype(np.uint8)
+    return f
+
+
 def _autograd_pin():
     B.test_matches_torch_autograd(16, 32, 24, 8, 2, True)
 
@@ -127,6 +156,10 @@ CASES = [
     ("swiglu_backward", _silu_derivative_drops_second_term, [_autograd_pin]),
     ("gate_backward", _gate_backward_drops_mean, [_fd_pin]),
     ("gate_backward", _gate_backward_drops_mean, [lambda: B.test_router_shift_invariances("f64")]),
+    ("quantize_nvfp4", _nvfp4_nibbles_swapped, [lambda: N.test_nvfp4_reproduces_exactly_representable_blocks(0)]),
+    ("quantize_nvfp4", _nvfp4_scale_without_tensor_scale,
+     [lambda: N.test_nvfp4_reproduces_exactly_representable_blocks(5)]),
+    ("e2m1_encode", _e2m1_ties_away, [N.test_e2m1_encode_is_round_to_nearest_even_with_saturation]),
 ]
 
 
