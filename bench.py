@@ -203,6 +203,34 @@ def kernel_launches_per_step(w, fused: bool) -> int:
     return n
 
 
+def nvfp4_quant_figures(M, x: torch.Tensor, steps: int, hbm: float) -> dict:
+    """Time moe_quantize_nvfp4 on the layer's token matrix, L2 flushed before each
+    call.  Algorithmic bytes per call: the input read twice (the tensor amax, then
+    the blocks) plus the E2M1 codes and E4M3 scales written."""
+    rows, K = x.shape
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, K // 16), dtype=torch.uint8, device=x.device)
+    st = torch.empty(2, dtype=torch.float32, device=x.device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=x.device)
+    for _ in range(3):
+        M.moe_quantize_nvfp4(x, codes, scales, st)
+    total = 0.0
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        M.moe_quantize_nvfp4(x, codes, scales, st)
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    ms = total / steps
+    nbytes = 2 * x.numel() * x.element_size() + codes.numel() + scales.numel()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"what": f"x [{rows}][{K}] {str(x.dtype).replace('torch.', '')} -> NVFP4 (2 launches)",
+            "ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+            "algorithmic_bytes": nbytes, "l2": "flushed (256 MB write) before each call"}
+
+
 def gpu_arm(args, rank, world):
     from token_dispatch_expert_top_gb300 import moe as M
     from token_dispatch_expert_top_gb300.layer import MoeLayer
@@ -368,6 +396,7 @@ def gpu_arm(args, rank, world):
         "combine_gbs": round(comb_gbs, 1), "combine_frac_hbm": round(comb_gbs / hbm, 4),
         "hbm_peak_gbs": hbm, "hbm_peak_source": peak_src,
         "roofline": roofline,
+        "nvfp4_quantize": nvfp4_quant_figures(M, layer.x, args.steps, hbm) if w.dtype != "f32" else None,
         "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps,
         "clocks": clk.summary(),
         "e2e": e2e,

@@ -121,6 +121,27 @@ const char* moe_status_string(int status);
 int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
                        uint8_t* codes, uint8_t* scales, void* stream);
 
+/* NVFP4 quantisation along K of a row-major [rows][K] matrix.  [Kittens] names
+ * NVFP4, beside MXFP8, as a format of the team's earlier training kernels without
+ * defining it (paragraph on the year of compute-only kernels); the format taken is the OCP MX v1.0 FP4 E2M1 element
+ * with NVIDIA's published two-level scaling: one E4M3 scale per 16 consecutive
+ * elements and one FP32 scale per tensor.  With every step one correctly rounded
+ * FP32 operation:
+ *   s_t  = amax / 2688 over the whole tensor (1 if it is all zero),
+ *   s_b  = E4M3(amax_block / 6 / s_t)        (round to nearest even, saturating),
+ *   d    = value(s_b) * s_t,
+ *   code = E2M1(x / d) (nearest even, saturating at 6; 0 for every element if d = 0).
+ *   in           : [rows][K], in_dtype MOE_F32 or MOE_BF16, finite, 16-byte aligned
+ *   codes        : [rows][K/2] bytes, two E2M1 codes per byte, element 2i in the low
+ *                  nibble of byte i (out; 8-byte aligned)
+ *   scales       : [rows][K/16] E4M3 bytes (out)
+ *   tensor_scale : device float[2] (out): [0] = s_t, [1] = the tensor amax
+ * K must be a multiple of 16.  Two passes over the input (the amax, then the blocks)
+ * on `stream`.  Bit-exact with the oracle on identical input.  The grouped GEMMs do
+ * not take this format. */
+int moe_quantize_nvfp4(const void* in, int in_dtype, int64_t rows, int64_t K,
+                       uint8_t* codes, uint8_t* scales, float* tensor_scale, void* stream);
+
 /* One-time repacking of the expert weights into the layout the grouped GEMMs
  * read (pull dispatch lets the receiver choose its own placement, [MoK-2.37x]
  * section 02; the same holds for the static weights).  Input is the natural

@@ -63,6 +63,8 @@ def test_argument_errors_return_before_any_launch():
     assert lib.moe_expert_ffn(None, None, None, None, None, None, None, ctypes.byref(ok), None, 32,
                               1 << 40, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_quantize_mxfp8(None, 1, 4, 33, None, None, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_nvfp4(None, 1, 4, 24, None, None, None, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_nvfp4(None, 1, 4, 32, None, None, None, None) == M.MOE_ERR_INVALID_ARG
     assert lib.moe_dispatch_pull(1, None, ctypes.byref(ok), 1, None, 100, 100, 1, None, 8, 16, 256,
                                  None) == M.MOE_ERR_INVALID_ARG   # slots past T
 

@@ -310,6 +310,17 @@ int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K, ui
                                              num_sms_current(), (cudaStream_t)stream));
 }
 
+int moe_quantize_nvfp4(const void* in, int in_dtype, int64_t rows, int64_t K, uint8_t* codes,
+                       uint8_t* scales, float* tensor_scale, void* stream) {
+    if (rows < 0 || K <= 0 || K % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (in_dtype != MOE_F32 && in_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (!tensor_scale || ((uintptr_t)tensor_scale & 7)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!in || !codes || !scales || !aligned16(in) || ((uintptr_t)codes & 7)))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_quantize_nvfp4(in, in_dtype, rows, K, codes, scales, tensor_scale,
+                                             num_sms_current(), (cudaStream_t)stream));
+}
+
 int moe_pack_expert_weights(const moe_shape_t* shape, const void* w_gate_up,
                             const uint8_t* w_gu_scales, const void* w_down,
                             const uint8_t* w_d_scales, void* packed_gate_up,

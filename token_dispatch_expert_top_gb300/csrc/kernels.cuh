@@ -12,6 +12,9 @@ inline int layout_chunks(int T) { return (T + kLayoutChunk - 1) / kLayoutChunk; 
 cudaError_t launch_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
                                   uint8_t* codes, uint8_t* scales, int num_sms,
                                   cudaStream_t stream);
+cudaError_t launch_quantize_nvfp4(const void* in, int in_dtype, int64_t rows, int64_t K,
+                                  uint8_t* codes, uint8_t* scales, float* st_amax, int num_sms,
+                                  cudaStream_t stream);
 
 cudaError_t launch_route_topk_simt(const void* x, const void* w, const float* bias, int N, int H,
                                    int E, int k, int dtype, int32_t* idx, float* gate,

@@ -25,7 +25,7 @@ DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8}
 
 ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_last_device_status", "moe_status_string",
-    "moe_quantize_mxfp8", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
+    "moe_quantize_mxfp8", "moe_quantize_nvfp4", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
     "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
     "moe_pack_expert_weights", "moe_backward_workspace_bytes", "moe_pack_expert_weights_dgrad",
     "moe_expert_ffn_train", "moe_forward_train", "moe_reverse_combine", "moe_expert_ffn_dgrad",
@@ -82,6 +82,7 @@ _SIGS = {
     "moe_last_device_status": (_i, [_vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i]),
     "moe_quantize_mxfp8": (_i, [_vp, _i, _i64, _i64, _vp, _vp, _vp]),
+    "moe_quantize_nvfp4": (_i, [_vp, _i, _i64, _i64, _vp, _vp, _vp, _vp]),
     "moe_route_topk": (_i, [_vp, _vp, _vp, _shp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_layout": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_dispatch_pull": (_i, [_vp, _vp, _shp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
@@ -164,6 +165,15 @@ def moe_quantize_mxfp8(inp: torch.Tensor, codes: torch.Tensor, scales: torch.Ten
     rows = inp.numel() // K
     _check("moe_quantize_mxfp8", _lib.moe_quantize_mxfp8(_p(inp), dt, rows, K, _p(codes), _p(scales),
                                                          _stream(stream)))
+
+
+def moe_quantize_nvfp4(inp: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                       tensor_scale: torch.Tensor, stream=None) -> None:
+    dt = MOE_BF16 if inp.dtype == torch.bfloat16 else MOE_F32
+    K = inp.shape[-1]
+    rows = inp.numel() // K
+    _check("moe_quantize_nvfp4", _lib.moe_quantize_nvfp4(_p(inp), dt, rows, K, _p(codes), _p(scales),
+                                                         _p(tensor_scale), _stream(stream)))
 
 
 def moe_pack_expert_weights(shape: Shape, w_gate_up, w_gu_scales, w_down, w_d_scales,
