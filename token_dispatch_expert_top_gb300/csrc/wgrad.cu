@@ -25,12 +25,12 @@
 //            a 3-stage ring
 //   warp 1   TMEM owner + MMA issuer; the last K-stage of an expert issues only
 //            the 32-slot (MXFP8) or 16-slot (BF16) steps that hold slots
-//   warp 3   (prologue) lists the experts with and without slots
+//   warps 2-3 zero the gradients of the experts without slots with streaming
+//            vector stores, alongside the MMA-bound tiles (warp 3 first lists
+//            the experts with and without slots)
 //   warps 4-11 epilogue: accumulator -> BF16 -> a 64 KB staging tile in shared
-//            memory -> TMA tensor stores into dW (zeros when the expert has no
-//            slots); the stores run asynchronously while the next tile computes
-// Each CTA interleaves its share of MMA-bound tiles with its share of the
-// store-bound zero tiles of idle experts (WgSchedule).
+//            memory -> TMA tensor stores into dW; the stores run asynchronously
+//            while the next tile computes
 // Every wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT and stops.
 #include "common.cuh"
 #include "kernels.cuh"
@@ -248,33 +248,25 @@ struct WgTile {
     int kbase;                // first K-stage of the expert in the images
 };
 
-// The tile order of one CTA.  Tiles of experts with slots ("work", MMA-bound) and
-// of experts without ("zero", store-bound) form two lists, each expert-major then
-// N tile then M tile, and each dealt round-robin over the CTAs.  A CTA walks its
-// two shares interleaved in proportion, so the zero tiles' stores overlap the
-// work tiles' MMAs; CTAs at the same step work on the same expert, so weight-
-// gradient operands are shared through L2.
+// The tile order of one CTA: the tiles of the experts with slots, expert-major
+// then N tile then M tile, dealt round-robin over the CTAs, so CTAs at the same
+// step work on the same expert and share its operands through L2.  Experts
+// without slots get no tiles (their gradients are zero-filled separately).
 struct WgSchedule {
     const int32_t* work;      // experts with slots, in order (shared memory)
-    const int32_t* zero;      // experts without slots
-    int per, wc, zc, n;       // tiles per expert; this CTA's work / zero / total tile counts
+    int per, n;               // tiles per expert; this CTA's tile count
 
-    __device__ void init(const int32_t* w_list, const int32_t* z_list, int nw, int nz, int per_) {
+    __device__ void init(const int32_t* w_list, int nw, int per_) {
         work = w_list;
-        zero = z_list;
         per = per_;
         const int G = gridDim.x, c = blockIdx.x;
-        const long long W = (long long)nw * per, Z = (long long)nz * per;
-        wc = W > c ? (int)((W - c - 1) / G + 1) : 0;
-        zc = Z > c ? (int)((Z - c - 1) / G + 1) : 0;
-        n = wc + zc;
+        const long long W = (long long)nw * per;
+        n = W > c ? (int)((W - c - 1) / G + 1) : 0;
     }
     // (expert, tile within the expert) of step s of this CTA
     __device__ void at(int s, int& e, int& l) const {
-        const long long zs = n ? (long long)s * zc / n : 0, zs1 = n ? (long long)(s + 1) * zc / n : 0;
-        const long long t = zs1 > zs ? blockIdx.x + zs * (long long)gridDim.x
-                                     : blockIdx.x + (s - zs) * (long long)gridDim.x;
-        e = zs1 > zs ? zero[t / per] : work[t / per];
+        const long long t = blockIdx.x + (long long)s * gridDim.x;
+        e = work[t / per];
         l = (int)(t % per);
     }
 };
@@ -358,7 +350,7 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
     const uint32_t tmem_base = *reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     const unsigned long long deadline = globaltimer_ns() + timeout_ns;
     WgSchedule sc;
-    sc.init(w_list, z_list, n_lists[0], n_lists[1], g0.m_tiles * g0.n_tiles + g1.m_tiles * g1.n_tiles);
+    sc.init(w_list, n_lists[0], g0.m_tiles * g0.n_tiles + g1.m_tiles * g1.n_tiles);
 
     if (warp == 0) {
         if (lane == 0) {   // producer
@@ -400,7 +392,6 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             bool ok = true;
             for (int s = 0; ok && s < sc.n; ++s) {
                 const WgTile w = wg_tile<MX>(sc, s, g0, g1, offsets, pstage);
-                if (w.KB == 0) continue;            // zero tiles never touch the accumulator
                 if (!mbar_wait_bounded(tempty, acc_phase ^ 1, abort_flag, ws, deadline)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < w.KB; ++kb) {
@@ -445,6 +436,29 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             while (!mbar_try_wait(drain, 0) && globaltimer_ns() < d2) {
             }
         }
+    } else if (warp == 2 || warp == 3) {
+        // Zero fill: dW_gate_up[e] and dW_down[e] of an expert without slots are
+        // contiguous byte ranges (out_estride bytes each, a multiple of 16).  They
+        // are cut into 64 KB chunks dealt over (CTA, warp); a warp's 32 lanes write
+        // 512 contiguous bytes per store.  Streaming stores keep the zeros from
+        // evicting the working tiles' operands from L2.
+        constexpr int64_t CH = 65536;
+        const int64_t b0 = g0.out_estride, b1 = g1.out_estride;
+        const int64_t c0 = (b0 + CH - 1) / CH, c1 = (b1 + CH - 1) / CH;
+        const int64_t total = (int64_t)n_lists[1] * (c0 + c1);
+        const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+        for (int64_t t = 2 * (int64_t)blockIdx.x + (warp - 2); t < total; t += 2 * (int64_t)gridDim.x) {
+            if (*abort_flag) break;
+            const int e = z_list[t / (c0 + c1)];
+            int64_t r = t % (c0 + c1);
+            const bool second = r >= c0;
+            if (second) r -= c0;
+            const int64_t bytes = second ? b1 : b0;
+            uint8_t* dst = (second ? g1.out : g0.out) + (int64_t)e * bytes + r * CH;
+            const int64_t len = bytes - r * CH < CH ? bytes - r * CH : CH;
+            for (int64_t off = (int64_t)lane * 16; off < len; off += 512)
+                __stcs(reinterpret_cast<uint4*>(dst + off), zero4);
+        }
     } else if (warp >= 4) {   // epilogue
         // Warp (q, half) owns rows 32q..32q+31 and columns 128 half..+127 of the
         // tile: two TMA store boxes of 32 rows x 64 BF16 (128-byte swizzle) in
@@ -456,24 +470,16 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         for (int s = 0; s < sc.n; ++s) {
             const WgTile w = wg_tile<MX>(sc, s, g0, g1, offsets, pstage);
             uint32_t v[4][32];
-            if (w.KB > 0) {
-                if (!mbar_wait_bounded(tfull, acc_phase, abort_flag, ws, deadline)) break;
-                tc_fence_after();
-                const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+            if (!mbar_wait_bounded(tfull, acc_phase, abort_flag, ws, deadline)) break;
+            tc_fence_after();
+            const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v[c4]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty);
-                acc_phase ^= 1;
-            } else {   // an expert without slots: zeros, without waiting for the MMA
-                if (*abort_flag) break;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[c4][i] = 0u;
-            }
+            for (int c4 = 0; c4 < 4; ++c4) tmem_ld_32x32b_x32(tq + 32 * (half * 4 + c4), v[c4]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);
+            acc_phase ^= 1;
             if (lane == 0) bulk_wait_group_read<0>();   // the previous tile's stores have left the boxes
             __syncwarp();
 #pragma unroll
