@@ -55,7 +55,8 @@ constexpr int NUM_BARS = 2 * STAGES + 3;       // full, empty, tfull, tempty, dr
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_LIST = OFF_MISC + 16;        // experts with / without slots (2 x 1024 ints)
 constexpr int MAX_E = 1024;
-constexpr int SMEM = OFF_LIST + 2 * MAX_E * 4 + 16;
+constexpr int OFF_PROG = OFF_LIST + 2 * MAX_E * 4;   // K-stages whose tiles are stored
+constexpr int SMEM = OFF_PROG + 16;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (4 + EPI_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
     int32_t* w_list = reinterpret_cast<int32_t*>(smem + OFF_LIST);
     int32_t* z_list = w_list + MAX_E;
     int32_t* n_lists = reinterpret_cast<int32_t*>(smem + OFF_MISC + 8);
+    volatile int* progress = reinterpret_cast<volatile int*>(smem + OFF_PROG);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         mbar_init(tempty, EPI_WARPS);
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *progress = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -441,13 +444,31 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         // contiguous byte ranges (out_estride bytes each, a multiple of 16).  They
         // are cut into 64 KB chunks dealt over (CTA, warp); a warp's 32 lanes write
         // 512 contiguous bytes per store.  Streaming stores keep the zeros from
-        // evicting the working tiles' operands from L2.
+        // evicting the working tiles' operands from L2.  The stores are paced by
+        // the CTA's own MMA work (K-stages of tiles already stored): written in one
+        // burst they saturate HBM with writes and stall the operand loads of the
+        // tiles, which then run after them instead of beside them.
         constexpr int64_t CH = 65536;
         const int64_t b0 = g0.out_estride, b1 = g1.out_estride;
         const int64_t c0 = (b0 + CH - 1) / CH, c1 = (b1 + CH - 1) / CH;
         const int64_t total = (int64_t)n_lists[1] * (c0 + c1);
+        const int64_t first = 2 * (int64_t)blockIdx.x + (warp - 2), stride = 2 * (int64_t)gridDim.x;
+        const int64_t mine = total > first ? (total - first - 1) / stride + 1 : 0;
+        int64_t work = 0;
+        if (mine > 0)
+            for (int s = 0; s < sc.n; ++s) work += wg_tile<MX>(sc, s, g0, g1, offsets, pstage).KB;
         const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-        for (int64_t t = 2 * (int64_t)blockIdx.x + (warp - 2); t < total; t += 2 * (int64_t)gridDim.x) {
+        int64_t i = 0;
+        for (int64_t t = first; t < total; t += stride, ++i) {
+            // chunk i waits until i <= mine * (progress + 2 stages of lead) / work
+            uint32_t n = 0;
+            while (work > 0 && i * work > mine * ((int64_t)*progress + 2) && !*abort_flag) {
+                __nanosleep(1000);
+                if ((++n & 63u) == 0 && globaltimer_ns() > deadline) {
+                    *abort_flag = 1;
+                    set_status(ws, MOE_ERR_TIMEOUT);
+                }
+            }
             if (*abort_flag) break;
             const int e = z_list[t / (c0 + c1)];
             int64_t r = t % (c0 + c1);
@@ -507,6 +528,7 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
                 if (x < nv) tma_store_2d(tm, box0, x, y);
                 if (x + 64 < nv) tma_store_2d(tm, box0 + BOX, x + 64, y);
                 bulk_commit_group();
+                if (warp == 4) *progress = *progress + w.KB;
             }
         }
         if (lane == 0) bulk_wait_group_all();
