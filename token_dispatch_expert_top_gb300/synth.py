@@ -79,11 +79,16 @@ WORKLOADS = {
     # H=7168, E=256, top-8) with small experts (I=128), ~3 GB on the device.
     "dsv3_router_prof": Workload("dsv3_router_prof", N=8192, H=7168, I=128, E=256, k=8, S=64,
                                  dtype="mxfp8"),
+    # Profiling stand-in for the hot experts of the skewed layers: DeepSeek-V3 shapes,
+    # 8 experts that every token picks (k=8), so each expert's weight-gradient tiles
+    # reduce over 2048 slots; ~3 GB on the device.
+    "dsv3_mxfp8_hot8": Workload("dsv3_mxfp8_hot8", N=2048, H=7168, I=2048, E=8, k=8, S=16,
+                                dtype="mxfp8"),
 }
 
 # Workloads whose tensors are drawn on the device generator (too large for the host).
 DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_e32", "dsv3_router_prof",
-                "dsv3_mxfp8_skew_16k"}
+                "dsv3_mxfp8_skew_16k", "dsv3_mxfp8_hot8"}
 
 
 def master_dtype(w: Workload) -> torch.dtype:
