@@ -8,7 +8,8 @@
 // NVL72": section 01, each token picks a few experts per step; section 02, MXFP8
 // activation quantisation folded into the data path.)
 //
-// CTA = 16 warps:  w0 TMA producer, w1 MMA issuer + TMEM owner, w2-3 idle,
+// CTA = 16 warps:  w0 TMA producer (4-stage ring, 6 in split mode), w1 MMA issuer
+//                  + TMEM owner, w2-3 idle,
 //                  w4-11 x quantisers (MXFP8 only; one token row per thread, every
 //                  other K-stage), w12-15 top-k epilogue.
 // Split mode (E >= 64, E % 32 == 0): a cluster of two CTAs shares a 128-token tile,
@@ -24,18 +25,26 @@ namespace moe {
 
 namespace rt {
 constexpr int BM = 128;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * 128;            // 128 tokens x 64 BF16
-constexpr int B_MAX = 256 * 128;             // up to 256 experts x 64 BF16
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_BAR = OFF_B + STAGES * B_MAX;
-constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;   // full, empty, tfull, cand
-constexpr int OFF_BIAS = OFF_MISC + 16;
-constexpr int OFF_CAND = OFF_BIAS + 256 * 4;                // split mode: partner's candidates
 constexpr int THREADS = 512;
 constexpr int QUANT_WARPS = 8;
-inline size_t smem_bytes(int kmax) { return 1024 + OFF_CAND + (size_t)kmax * BM * 8; }
+// Shared-memory layout.  A CTA holds the weights of all E <= 256 experts (32 KB a
+// stage) in 4 stages, or in split mode those of E/2 <= 128 (16 KB a stage) in 6:
+// the same space, and 50% more bytes in flight for the latency-bound x stream.
+// The stage count is even, so a stage's index has the parity of its K-stages.
+template <bool SPLIT>
+struct Layout {
+    static constexpr int STAGES = SPLIT ? 6 : 4;
+    static constexpr int B_STRIDE = SPLIT ? 128 * 128 : 256 * 128;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_STRIDE;
+    static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;   // full, empty, tfull, cand
+    static constexpr int OFF_BIAS = OFF_MISC + 16;
+    static constexpr int OFF_CAND = OFF_BIAS + 256 * 4;                // split mode: partner's candidates
+};
+template <bool SPLIT>
+inline size_t smem_bytes(int kmax) { return 1024 + Layout<SPLIT>::OFF_CAND + (size_t)kmax * BM * 8; }
 }  // namespace rt
 
 struct RouteArgs {
@@ -77,6 +86,10 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     RouteArgs args) {
     using namespace rt;
+    using L = Layout<SPLIT>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int OFF_A = L::OFF_A, OFF_B = L::OFF_B, OFF_BAR = L::OFF_BAR, OFF_MISC = L::OFF_MISC;
+    constexpr int OFF_BIAS = L::OFF_BIAS, OFF_CAND = L::OFF_CAND, B_STRIDE = L::B_STRIDE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) break;
                 mbar_arrive_expect_tx(&full[stage], A_BYTES + b_bytes);
                 tma_load_2d(smem + OFF_A + stage * A_BYTES, &tmX, &full[stage], kb * 64, row0);
-                tma_load_2d(smem + OFF_B + stage * B_MAX, &tmW, &full[stage], kb * 64, e0);
+                tma_load_2d(smem + OFF_B + stage * B_STRIDE, &tmW, &full[stage], kb * 64, e0);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -157,7 +170,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + OFF_A + stage * A_BYTES);
-                const uint32_t sb = smem_u32(smem + OFF_B + stage * B_MAX);
+                const uint32_t sb = smem_u32(smem + OFF_B + stage * B_STRIDE);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem_base, sdesc_kmajor_sw128(sa + 32 * k), sdesc_kmajor_sw128(sb + 32 * k),
@@ -321,7 +334,7 @@ bool route_tc_supported(int dtype, int H, int E, int k) {
 template <int KMAX, bool QUANT>
 static cudaError_t launch_route(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
                                 int tiles, bool split, cudaStream_t st) {
-    const size_t smem = rt::smem_bytes(KMAX);
+    const size_t smem = split ? rt::smem_bytes<true>(KMAX) : rt::smem_bytes<false>(KMAX);
     if (!split) {
         auto kern = route_tc_kernel<KMAX, QUANT, false>;
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
