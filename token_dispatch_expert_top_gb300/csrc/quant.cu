@@ -121,13 +121,24 @@ __device__ __forceinline__ void load16(const In* src, float* v) {
 }
 
 // Pass 1: amax over the whole tensor.  Non-negative FP32 values order like their bit
-// patterns, so the block maxima meet in one atomicMax on the bits.
+// patterns, so the block maxima meet in one atomicMax on the bits.  Each thread
+// takes four blocks of 16 a round, their loads issued before any is used.
 template <typename In>
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const In* __restrict__ in, int64_t blocks16,
                                                          uint32_t* __restrict__ amax_bits) {
     uint32_t m = 0;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < blocks16;
-         b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; b + 3 * stride < blocks16; b += 4 * stride) {
+        float v[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load16(in + (b + u * stride) * 16, v[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = max(m, __float_as_uint(fabsf(v[u][i])));
+    }
+    for (; b < blocks16; b += stride) {
         float v[16];
         load16(in + b * 16, v);
 #pragma unroll
@@ -149,33 +160,51 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const In* __restrict__ 
 //   st = amax / 2688 (1 for an all-zero tensor),  sb = e4m3(amax_b / 6 / st),
 //   d = value(sb) * st,  code_i = e2m1(x_i / d)  (all codes 0 when d is 0).
 template <typename In>
+__device__ __forceinline__ void nvfp4_block(float* v, float st, uint8_t* __restrict__ codes,
+                                            uint8_t* __restrict__ scales, int64_t b) {
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+    const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), st);
+    const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
+    const float d = __fmul_rn(e4m3_value(sb), st);
+    uint2 out = make_uint2(0u, 0u);
+    if (d != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(v[i], d);
+        out.x = cvt_e2m1x8(v);
+        out.y = cvt_e2m1x8(v + 8);
+    }
+    *reinterpret_cast<uint2*>(codes + b * 8) = out;
+    scales[b] = (uint8_t)sb;
+}
+
+// Pass 2: blocks of 16 dealt over the threads (consecutive threads take consecutive
+// blocks of a row), two a round with both loads issued first.  Every FP32 step is
+// one correctly rounded operation:
+//   st = amax / 2688 (1 for an all-zero tensor),  sb = e4m3(amax_b / 6 / st),
+//   d = value(sb) * st,  code_i = e2m1(x_i / d)  (all codes 0 when d is 0).
+template <typename In>
 __global__ void __launch_bounds__(256) quantize_nvfp4_kernel(const In* __restrict__ in, int64_t rows,
                                                              int64_t K, float* __restrict__ st_amax,
                                                              uint8_t* __restrict__ codes,
                                                              uint8_t* __restrict__ scales) {
     const float amax = st_amax[1];
     const float st = amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-    const int64_t nb = K / 16;
-    const int64_t total = rows * nb;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
-         b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t total = rows * (K / 16);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; b + stride < total; b += 2 * stride) {
+        float v0[16], v1[16];
+        load16(in + b * 16, v0);
+        load16(in + (b + stride) * 16, v1);
+        nvfp4_block<In>(v0, st, codes, scales, b);
+        nvfp4_block<In>(v1, st, codes, scales, b + stride);
+    }
+    if (b < total) {
         float v[16];
         load16(in + b * 16, v);
-        float am = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
-        const float t = __fdiv_rn(__fdiv_rn(am, 6.0f), st);
-        const uint32_t sb = cvt_e4m3x2(t, 0.0f) & 0xFFu;
-        const float d = __fmul_rn(e4m3_value(sb), st);
-        uint2 out = make_uint2(0u, 0u);
-        if (d != 0.0f) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __fdiv_rn(v[i], d);
-            out.x = cvt_e2m1x8(v);
-            out.y = cvt_e2m1x8(v + 8);
-        }
-        *reinterpret_cast<uint2*>(codes + b * 8) = out;
-        scales[b] = (uint8_t)sb;
+        nvfp4_block<In>(v, st, codes, scales, b);
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) st_amax[0] = st;
 }
