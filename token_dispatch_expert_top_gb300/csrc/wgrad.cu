@@ -127,10 +127,13 @@ constexpr int kPackPitch16 = kPackCols + 8;     // BF16 elements per shared row
 
 template <int SRC, bool MX>
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgPackArgs a, WsHeader* ws) {
-    // BF16 sources (du|dv, x) are staged as their raw BF16 bits, which is exact and
-    // halves the shared memory (more CTAs per SM); computed ones (g*dY, h) as FP32.
-    constexpr bool RAW = SRC == WG_DUV || SRC == WG_X;
+    // BF16 sources (du|dv, x, dY) are staged as their raw BF16 bits, which is exact
+    // and halves the shared memory (more CTAs per SM); g*dY takes its slot's gate
+    // when it is quantised (the same FP32 product), and h, computed from u|v, is
+    // staged as FP32.
+    constexpr bool RAW = SRC == WG_DUV || SRC == WG_X || SRC == WG_DY;
     extern __shared__ uint4 smem_pack[];
+    __shared__ float sgate[32];
     float* tile = reinterpret_cast<float*>(smem_pack);        // [32][kPackPitch] FP32
     uint16_t* tile16 = reinterpret_cast<uint16_t*>(smem_pack); // [32][kPackPitch16] BF16
     const int P0 = blockIdx.x * 32;
@@ -179,6 +182,11 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
                 raw[j][hv][t] = ok ? ld_nc_v4(a.src + src_row[j] * a.ld + (t ? a.I : 0) + col)
                                    : make_uint4(0, 0, 0, 0);
         }
+    if constexpr (SRC == WG_DY) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (lane == 0) sgate[warp + 8 * j] = gs[j];
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -190,10 +198,7 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
             }
             float v[8];
             unpack_bf16x8_w(raw[j][hv][0], v);
-            if constexpr (SRC == WG_DY) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = gs[j] * v[q];
-            } else if constexpr (SRC == WG_H) {   // h = silu(u) * v from the kept u|v
+            if constexpr (SRC == WG_H) {   // h = silu(u) * v from the kept u|v
                 float w2[8];
                 unpack_bf16x8_w(raw[j][hv][1], w2);
 #pragma unroll
@@ -210,9 +215,11 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
         if (c >= a.Cp) break;
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 32; ++i) {
             v[i] = RAW ? bf16_to_f32(tile16[i * kPackPitch16 + hv * 256 + threadIdx.x])
                        : tile[i * kPackPitch + hv * 256 + threadIdx.x];
+            if constexpr (SRC == WG_DY) v[i] = sgate[i] * v[i];
+        }
         const int rb = c / 128, r = c % 128;
         if constexpr (MX) {
             uint32_t codes[8];
@@ -572,7 +579,7 @@ cudaError_t launch_wgrad(const WgradCall& c, cudaStream_t stream) {
         q.sf = sf;
         q.RB = Cp / 128;
         const dim3 grid((unsigned)(tp / 32), (unsigned)((Cp + kPackCols - 1) / kPackCols));
-        const size_t sm = (src == WG_DUV || src == WG_X) ? sizeof(uint16_t) * 32 * kPackPitch16
+        const size_t sm = (src == WG_DUV || src == WG_X || src == WG_DY) ? sizeof(uint16_t) * 32 * kPackPitch16
                                                          : sizeof(float) * 32 * kPackPitch;
 #define MOE_WG_PACK(S)                                                                                \
     if (mx) {                                                                                         \
