@@ -106,6 +106,20 @@ def test_route_topk_fused_x_quantisation_bit_exact(M, N, H, E, k):
     oc, os_ = O.quantize_mxfp8(O._f64(inp["x"]))
     np.testing.assert_array_equal(to_np(xs), os_)
     np.testing.assert_array_equal(to_np(xq), oc)
+    # Repeated under concurrent HBM traffic from another stream, which reorders the
+    # completion of the kernel's stage loads: the codes never change.
+    x_d, wr_d = inp["x"].cuda(), inp["w_router"].cuda()
+    noise = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    first_q, first_s = xq.clone(), xs.clone()
+    for rep in range(12):
+        with torch.cuda.stream(side):
+            noise.fill_(rep)
+        xq.zero_()
+        xs.zero_()
+        M.moe_route_topk(x_d, wr_d, None, shape, idx, gate, None, xq, xs)
+        torch.cuda.synchronize()
+        assert torch.equal(xq, first_q) and torch.equal(xs, first_s), rep
 
 
 # -------------------------------------------------------------------------- layout

@@ -10,8 +10,10 @@
 //
 // CTA = 16 warps:  w0 TMA producer (4-stage ring, 6 in split mode), w1 MMA issuer
 //                  + TMEM owner, w2-3 idle,
-//                  w4-11 x quantisers (MXFP8 only; one token row per thread, every
-//                  other K-stage), w12-15 top-k epilogue.
+//                  w4-11 x quantisers (MXFP8 only; two groups of four warps, one
+//                  token row per thread, each group every other K-stage; in split
+//                  mode all eight warps on every K-stage of the CTA's parity, one
+//                  32-element block per thread), w12-15 top-k epilogue.
 // Split mode (E >= 64, E % 32 == 0): a cluster of two CTAs shares a 128-token tile,
 // each computing the logits of half of the experts (twice the CTAs, half the
 // weight bytes each).  Each CTA quantises half of the K-stages of x.  The second
@@ -114,10 +116,11 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            // MMA + the quantiser group of the stage (split mode: only the stages of
-            // this CTA's parity are quantised here)
+            // MMA + the quantiser warps of the stage: in split mode all eight take
+            // the stages of this CTA's parity; otherwise a group of four takes the
+            // stages of its parity
             const bool quantised = QUANT && (!SPLIT || (s & 1) == half);
-            mbar_init(&empty[s], quantised ? 1 + QUANT_WARPS / 2 : 1);
+            mbar_init(&empty[s], quantised ? 1 + (SPLIT ? QUANT_WARPS : QUANT_WARPS / 2) : 1);
         }
         mbar_init(tfull, 1);
         mbar_init(cand_bar, 4);                               // the partner's four epilogue warps
@@ -185,26 +188,26 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         }
     } else if (warp >= 4 && warp < 12) {
         if constexpr (QUANT) {
-            // thread = (token row r, stage parity): it quantises both MX blocks of
-            // its row in every other stage and writes them as two full 32-byte
-            // sectors plus one 2-byte scale store
+            // Each quantiser warp waits on the fills of its stages in order, one phase
+            // at a time: a warp that skipped a fill of a stage could take that
+            // fill's completed phase for the next one (the wait tests only parity).
+            //   non-split (4 stages): thread = (token row r, group g); group g takes
+            //     the K-stages of parity g (always stages g and g + 2), both 32-element
+            //     blocks of row r;
+            //   split (6 stages): all 256 threads take every K-stage of this CTA's
+            //     parity; thread = (token row r, block b) quantises block b of row r.
             const int tq = (warp - 4) * 32 + lane;
             const int r = tq & (BM - 1);
-            const int grp = tq >> 7;              // quantiser group (warps 4-7, 8-11)
+            const int grp = tq >> 7;
             const int row = row0 + r;
-            // non-split: group g takes the stages of parity g; split: this CTA takes the
-            // stages of parity `half`, and group g every other one of them
-            const int kb_first = SPLIT ? half + 2 * grp : grp;
-            const int kb_step = SPLIT ? 4 : 2;
-            for (int kb = kb_first; kb < KB; kb += kb_step) {
+            const int kb_first = SPLIT ? half : grp;
+            const int b_first = SPLIT ? grp : 0, b_count = SPLIT ? 1 : 2;
+            for (int kb = kb_first; kb < KB; kb += 2) {
                 const int stage = kb % STAGES;
                 const uint32_t phase = (uint32_t)((kb / STAGES) & 1);
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
                 const uint8_t* tile = smem + OFF_A + stage * A_BYTES + r * 128;
-                uint32_t codes[16];
-                uint8_t sc[2];
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
+                for (int b = b_first; b < b_first + b_count; ++b) {
                     float v[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -219,16 +222,11 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                         }
                     }
                     uint32_t cb[8];
-                    sc[b] = mx_quantize32(v, cb);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) codes[8 * b + i] = cb[i];
-                }
-                if (row < args.N) {
-                    uint8_t* dst = args.xq + (int64_t)row * args.H + kb * 64;
-                    st_v8(dst, codes);
-                    st_v8(dst + 32, codes + 8);
-                    *reinterpret_cast<uint16_t*>(args.xq_sf + (int64_t)row * (args.H / 32) + kb * 2) =
-                        (uint16_t)(sc[0] | (sc[1] << 8));
+                    const uint8_t sc = mx_quantize32(v, cb);
+                    if (row < args.N) {   // one full 32-byte sector of codes and the block's scale
+                        st_v8(args.xq + (int64_t)row * args.H + kb * 64 + b * 32, cb);
+                        args.xq_sf[(int64_t)row * (args.H / 32) + kb * 2 + b] = sc;
+                    }
                 }
                 // Release the stage only after every lane has consumed what it read:
                 // the stores above use all of it, and the proxy fence orders these
