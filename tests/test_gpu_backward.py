@@ -264,6 +264,8 @@ BWD_LAYERS = [
     synth.Workload("bwd_mx", N=512, H=512, I=256, E=16, k=4, S=4, dtype="mxfp8"),
     synth.Workload("bwd_bf16", N=256, H=512, I=384, E=8, k=2, S=2, dtype="bf16"),
     synth.Workload("bwd_mx_skew", N=512, H=1024, I=256, E=32, k=8, S=4, dtype="mxfp8", skew=3.0),
+    # top-1: the renormalised gate is exactly 1, so the router gets no gradient
+    synth.Workload("bwd_top1", N=256, H=512, I=256, E=16, k=1, S=2, dtype="mxfp8"),
 ]
 
 
@@ -290,7 +292,9 @@ def test_backward_layer_matches_oracle(M, w):
     err_wr = row_rel_err(to_np(dwr)[used], ref["dw_router"][used])
     assert err_wr.max() < tol, err_wr.max()
     assert np.all(to_np(dwr)[~used] == 0.0)
-    assert np.abs(to_np(db) - ref["dbias"]).max() < tol * np.abs(ref["dbias"]).max()
+    assert np.abs(to_np(db) - ref["dbias"]).max() <= tol * np.abs(ref["dbias"]).max()
+    if w.k == 1:
+        assert not to_np(dwr).any() and not to_np(db).any()
     # expert weight gradients: every row of every expert with slots; zeros otherwise
     g_gu, g_d = to_np(dwgu), to_np(dwd)
     err_w = max(row_rel_err(g_gu[used].reshape(-1, w.H), ref["dw_gate_up"][used].reshape(-1, w.H)).max(),

@@ -65,3 +65,28 @@ def test_forward_empty_batch():
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     M.moe_forward(dummy, dummy, None, dummy, None, dummy, None, shape, None, dummy, None, None, ws)
     assert M.moe_last_device_status(ws) == 0
+
+
+# Degenerate shapes: top-1 with a ragged token count, every token on every
+# expert (k = E), a single expert (a dense SwiGLU FFN), and a bias so steep that
+# every token picks the same two experts (fourteen experts without slots).
+DEGENERATE = [
+    synth.Workload("top1_ragged", N=300, H=512, I=256, E=16, k=1, S=3, dtype="mxfp8"),
+    synth.Workload("k_eq_E", N=256, H=512, I=256, E=4, k=4, S=2, dtype="mxfp8"),
+    synth.Workload("one_expert", N=200, H=256, I=128, E=1, k=1, S=2, dtype="bf16"),
+    synth.Workload("two_hot", N=384, H=512, I=256, E=16, k=2, S=4, dtype="mxfp8", skew=50.0),
+]
+
+
+@pytest.mark.parametrize("w", DEGENERATE, ids=lambda w: w.name)
+def test_forward_degenerate_shapes(w):
+    layer, out = check_layer(w)
+    if w.k == w.E:
+        assert np.all(np.sort(to_np(layer.idx), axis=1) == np.arange(w.E))
+    if w.skew >= 50.0:
+        idx = to_np(layer.idx)
+        assert len(np.unique(idx)) == w.k        # all tokens on the same k experts
+    staged = out.clone()
+    fused = layer.forward(fused=True)
+    assert layer.device_status() == 0
+    assert torch.equal(fused, staged)
