@@ -16,14 +16,15 @@
 // tensor cores; section 02, SwiGLU and MXFP8 activation quantisation inside the
 // GEMM data path rather than a separate quantise kernel.)
 //
-// CTA = 8 warps, one CTA per SM:
+// CTA = 12 warps, one CTA per SM (the roles of gemm_roles.cuh):
 //   warp 0      TMA producer (A tile 128 x 128 B, B tile 256 x 128 B per stage)
 //   warp 1      TMEM allocator + MMA issuer (one thread)
 //   warp 2      scale-factor loader (MXFP8): reads the [rows][K/32] scale bytes,
 //               transposes them into the [32 lanes][4 words] blocks tcgen05.cp
 //               moves to tensor memory
-//   warp 3      idle after the prologue
-//   warps 4-7   epilogue: tensor memory -> registers -> SwiGLU / convert -> global
+//   warp 3      the expert m-tile prefix in the prologue, then idle (the fused
+//               kernel's dependency thread)
+//   warps 4-11  epilogue: tensor memory -> registers -> SwiGLU / convert -> global
 // Tile 128 x 256 (M x N), K-stage 128 bytes, 4-stage smem ring, FP32 accumulator
 // in 256 tensor-memory columns.  Every wait is bounded (a deadline on the GPU
 // clock); when one runs out the CTA records MOE_ERR_TIMEOUT and winds down.
