@@ -88,9 +88,13 @@ struct GemmSide {
 struct GemmMaps {
     const CUtensorMap *a0, *a1;       // A operand of GEMM1 / GEMM2
     const CUtensorMap *sfa0, *sfa1;   // A scales (TMA-staged) of GEMM1 / GEMM2
+    const CUtensorMap *t0, *t1;       // A operand with 32-row boxes, for tiles of <= 32 rows
+                                      // (an expert's ragged last m-tile); null: not used
     __device__ const CUtensorMap* a(int kind) const { return kind ? a1 : a0; }
     __device__ const CUtensorMap* sfa(int kind) const { return kind ? sfa1 : sfa0; }
+    __device__ const CUtensorMap* tail(int kind) const { return kind ? t1 : t0; }
 };
+constexpr int kTailRows = 32;
 
 // The two GEMM descriptions, picked the same way.  They point at kernel
 // parameters declared __grid_constant__, so nothing is copied to local memory.
@@ -203,8 +207,16 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
             if (!mbar_wait_bounded(&p.empty[stage], phase ^ 1, p.abort_flag, p.ws, p.deadline)) return;
             uint8_t* sa = p.smem + OFF_A + stage * A_BYTES;
             uint8_t* sb = p.smem + OFF_B + stage * B_BYTES;
-            mbar_arrive_expect_tx(&p.full[stage], A_BYTES + B_BYTES + (MX ? SFB_BYTES : 0));
-            tma_load_2d(sa, maps.a(tl.kind), &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
+            // A tile of a few rows: load only its first kTailRows rows; the MMA still
+            // runs all 128, and the rows past the tile are never stored
+            const CUtensorMap* ta = maps.a(tl.kind);
+            int a_bytes = A_BYTES;
+            if (tl.nrows <= kTailRows && maps.tail(tl.kind) != nullptr) {
+                ta = maps.tail(tl.kind);
+                a_bytes = kTailRows * 128;
+            }
+            mbar_arrive_expect_tx(&p.full[stage], a_bytes + B_BYTES + (MX ? SFB_BYTES : 0));
+            tma_load_2d(sa, ta, &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
             bulk_load(sb, sd.b_pk + (tile0 + kb) * B_TILE, B_TILE, &p.full[stage]);
             if (MX)
                 bulk_load(p.smem + OFF_SFB + stage * SFB_BYTES, sd.sfb_pk + (tile0 + kb) * SFB_TILE,

@@ -77,6 +77,7 @@ struct ExpertTiles {
 template <bool MX, int KIND, bool SAVE>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmT,
                            const __grid_constant__ CUtensorMap tmSFA,
                            const __grid_constant__ GemmSide side,
                            const int32_t* offsets, int E, WsHeader* ws,
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
     }
     __syncthreads();
     ExpertTiles<KIND, SAVE> src{offsets, mpre, E, side.n_tiles, mpre[E] * side.n_tiles};
-    const GemmMaps maps{&tmA, &tmA, &tmSFA, &tmSFA};
+    const GemmMaps maps{&tmA, &tmA, &tmSFA, &tmSFA, &tmT, &tmT};
     const GemmSides sides{&side, &side};
     run_gemm_pipeline<MX>(smem, maps, sides, src, ws, timeout_ns);
 }
@@ -116,14 +117,14 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
 inline size_t gemm_smem_bytes(int E) { return 1024 + tc::OFF_TAIL + sizeof(int32_t) * (E + 1); }
 
 template <bool MX, int KIND, bool SAVE = false>
-static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tsa, const GemmSide& side,
-                              const int32_t* offsets, int E, WsHeader* ws,
+static cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tt, const CUtensorMap& tsa,
+                              const GemmSide& side, const int32_t* offsets, int E, WsHeader* ws,
                               unsigned long long timeout_ns, int grid, cudaStream_t stream) {
     auto kern = tc_grouped_gemm_kernel<MX, KIND, SAVE>;
     const size_t smem = gemm_smem_bytes(E);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tsa, side, offsets, E, ws, timeout_ns);
+    kern<<<grid, tc::THREADS, smem, stream>>>(ta, tt, tsa, side, offsets, E, ws, timeout_ns);
     return cudaGetLastError();
 }
 
@@ -136,26 +137,27 @@ static bool encode_sfa_map(CUtensorMap* tsa, const void* a_sf, int a_rows, int K
     return encode_tmap(tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a_sf, da, sa, ba, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// A operand maps of both GEMMs (a [a_rows][H] and h [a_rows][I], 128-row boxes of
-// 128 bytes, 128-byte swizzle), the A scale maps when TMA-staged, and the two
-// GemmSides over the tile-packed weights.
-bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2) {
-    const bool mx = c.mx;
+// An A operand map: [rows][K] MXFP8 codes or BF16, boxes of `box_rows` rows x 128
+// bytes, 128-byte swizzle.
+static bool encode_a_map(CUtensorMap* m, bool mx, const void* base, int K, int rows, int box_rows) {
     const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t esz = mx ? 1 : 2;
-    const uint32_t bk = mx ? 128 : 64;
-    {
-        uint64_t dims[2] = {(uint64_t)c.H, (uint64_t)c.a_rows};
-        uint64_t str[1] = {(uint64_t)c.H * esz};
-        uint32_t box[2] = {bk, 128};
-        if (!encode_tmap(&m->a1, dt, 2, c.a, dims, str, box)) return false;
-    }
-    {
-        uint64_t dims[2] = {(uint64_t)c.I, (uint64_t)c.a_rows};
-        uint64_t str[1] = {(uint64_t)c.I * esz};
-        uint32_t box[2] = {bk, 128};
-        if (!encode_tmap(&m->a2, dt, 2, c.h, dims, str, box)) return false;
-    }
+    uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+    uint64_t str[1] = {(uint64_t)K * esz};
+    uint32_t box[2] = {mx ? 128u : 64u, (uint32_t)box_rows};
+    return encode_tmap(m, dt, 2, base, dims, str, box);
+}
+
+// A operand maps of both GEMMs (a [a_rows][H] and h [a_rows][I], 128-row boxes and
+// kTailRows-row boxes for ragged tiles), the A scale maps when TMA-staged, and the
+// two GemmSides over the tile-packed weights.
+bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2) {
+    const bool mx = c.mx;
+    if (!encode_a_map(&m->a1, mx, c.a, c.H, c.a_rows, 128) ||
+        !encode_a_map(&m->t1, mx, c.a, c.H, c.a_rows, kTailRows) ||
+        !encode_a_map(&m->a2, mx, c.h, c.I, c.a_rows, 128) ||
+        !encode_a_map(&m->t2, mx, c.h, c.I, c.a_rows, kTailRows))
+        return false;
     *s1 = GemmSide{};
     s1->K = c.H;
     s1->n_tiles = c.I / 128;
@@ -200,15 +202,15 @@ cudaError_t launch_expert_ffn_tc(const TcFfnCall& c, cudaStream_t stream) {
     if (!encode_ffn_maps(c, &m, &s1, &s2)) return cudaErrorInvalidValue;
     cudaError_t err;
     if (c.mx) {
-        err = c.uv ? launch_one<true, 0, true>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
-                   : launch_one<true, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = c.uv ? launch_one<true, 0, true>(m.a1, m.t1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                   : launch_one<true, 0>(m.a1, m.t1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<true, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<true, 1>(m.a2, m.t2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     } else {
-        err = c.uv ? launch_one<false, 0, true>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
-                   : launch_one<false, 0>(m.a1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = c.uv ? launch_one<false, 0, true>(m.a1, m.t1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                   : launch_one<false, 0>(m.a1, m.t1, m.s1a, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
         if (err != cudaSuccess) return err;
-        err = launch_one<false, 1>(m.a2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+        err = launch_one<false, 1>(m.a2, m.t2, m.s2a, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     }
     return err;
 }
@@ -225,20 +227,13 @@ cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
     const CUtensorMapDataType dt = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t esz = mx ? 1 : 2;
     const uint32_t bk = mx ? 128 : 64;
-    CUtensorMap m_dy, m_duv, s_dy = CUtensorMap{}, s_duv = CUtensorMap{};
-    {
-        uint64_t dims[2] = {(uint64_t)c.H, (uint64_t)c.a_rows};
-        uint64_t str[1] = {(uint64_t)c.H * esz};
-        uint32_t box[2] = {bk, 128};
-        if (!encode_tmap(&m_dy, dt, 2, c.dy, dims, str, box)) return cudaErrorInvalidValue;
-    }
+    CUtensorMap m_dy, m_duv, t_dy, t_duv, s_dy = CUtensorMap{}, s_duv = CUtensorMap{};
     const void* a1 = mx ? c.duv_q : c.duv;
-    {
-        uint64_t dims[2] = {(uint64_t)(2 * c.I), (uint64_t)c.a_rows};
-        uint64_t str[1] = {(uint64_t)(2 * c.I) * esz};
-        uint32_t box[2] = {bk, 128};
-        if (!encode_tmap(&m_duv, dt, 2, a1, dims, str, box)) return cudaErrorInvalidValue;
-    }
+    if (!encode_a_map(&m_dy, mx, c.dy, c.H, c.a_rows, 128) ||
+        !encode_a_map(&t_dy, mx, c.dy, c.H, c.a_rows, kTailRows) ||
+        !encode_a_map(&m_duv, mx, a1, 2 * c.I, c.a_rows, 128) ||
+        !encode_a_map(&t_duv, mx, a1, 2 * c.I, c.a_rows, kTailRows))
+        return cudaErrorInvalidValue;
     GemmSide s2{};   // dgrad of GEMM2 -> dh
     s2.K = c.H;
     s2.n_tiles = (c.I + tc::BN - 1) / tc::BN;
@@ -265,14 +260,14 @@ cudaError_t launch_ffn_dgrad_tc(const TcDgradCall& c, cudaStream_t stream) {
         if (s2.sf_tma && !encode_sfa_map(&s_dy, c.dy_sf, c.a_rows, c.H)) return cudaErrorInvalidValue;
         if (s1.sf_tma && !encode_sfa_map(&s_duv, c.duv_sf, c.a_rows, 2 * c.I)) return cudaErrorInvalidValue;
     }
-    cudaError_t err = mx ? launch_one<true, 1>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
-                         : launch_one<false, 1>(m_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+    cudaError_t err = mx ? launch_one<true, 1>(m_dy, t_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+                         : launch_one<false, 1>(m_dy, t_dy, s_dy, s2, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
     if (err != cudaSuccess) return err;
     err = launch_swiglu_backward(mx, c.dh, c.uv, c.T, c.I, c.duv, (uint8_t*)c.duv_q, (uint8_t*)c.duv_sf,
                                  c.num_sms, stream);
     if (err != cudaSuccess) return err;
-    return mx ? launch_one<true, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
-              : launch_one<false, 1>(m_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
+    return mx ? launch_one<true, 1>(m_duv, t_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream)
+              : launch_one<false, 1>(m_duv, t_duv, s_duv, s1, c.offsets, c.E, c.ws, c.timeout_ns, c.grid, stream);
 }
 
 }  // namespace moe

@@ -199,6 +199,7 @@ int fused_max_ctas();
 // TMA maps of both expert GEMMs (operands and, for MXFP8, staged scales).
 struct FfnMaps {
     CUtensorMap a1, a2, s1a, s2a;
+    CUtensorMap t1, t2;       // A operands with 32-row boxes (ragged last m-tiles)
 };
 struct GemmSide;
 bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2);
