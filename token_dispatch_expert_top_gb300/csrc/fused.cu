@@ -612,6 +612,7 @@ template <bool MX>
 __global__ void __launch_bounds__(tc::THREADS, 1)
     fused_forward_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmA2,
                          const __grid_constant__ CUtensorMap tmS1a, const __grid_constant__ CUtensorMap tmS2a,
+                         const __grid_constant__ CUtensorMap tmT1, const __grid_constant__ CUtensorMap tmT2,
                          const __grid_constant__ GemmSide s1, const __grid_constant__ GemmSide s2,
                          const __grid_constant__ FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(tc::THREADS, 1)
         __syncthreads();
         MinibatchTiles src{&a, off, tb, pb, el, ct, nmb, s1.n_tiles, s2.n_tiles, (int)blockIdx.x - a.G,
                            (int)gridDim.x - a.G};
-        const GemmMaps maps{&tmA1, &tmA2, &tmS1a, &tmS2a};
+        const GemmMaps maps{&tmA1, &tmA2, &tmS1a, &tmS2a, &tmT1, &tmT2};
         const GemmSides sides{&s1, &s2};
         run_gemm_pipeline<MX>(smem, maps, sides, src, a.ws, a.timeout_ns);
     }
@@ -733,7 +734,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     void* kern = c.ffn.mx ? (void*)fused_forward_kernel<true> : (void*)fused_forward_kernel<false>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    void* args[] = {&m.a1, &m.a2, &m.s1a, &m.s2a, &s1, &s2, &a};
+    void* args[] = {&m.a1, &m.a2, &m.s1a, &m.s2a, &m.t1, &m.t2, &s1, &s2, &a};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(c.G + c.C);
     cfg.blockDim = dim3(tc::THREADS);
