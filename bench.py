@@ -56,10 +56,10 @@ def job_rate(units_per_rank_step: float, steps: int, t_ms: float, world: int) ->
 # DRAM bytes (read + write) of one moe_expert_ffn call (its two grouped-GEMM
 # launches), from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the 32-expert DeepSeek-V3 stand-in (N=1024, same 256 slots per expert): GEMM1
-# 1.0428 + 0.0179 GB, GEMM2 0.5020 + 0.0980 GB.  The full layer has 8x the experts
+# 1.0400 + 0.0178 GB, GEMM2 0.5019 + 0.0980 GB.  The full layer has 8x the experts
 # and 8x the slots at the same load per expert, and both the weight and the
 # activation bytes grow in proportion, so a full call moves 8x that.
-FFN_TRAFFIC_BYTES = {"dsv3_mxfp8": 8 * (1.0418 + 0.0176 + 0.5020 + 0.0981) * 1e9}
+FFN_TRAFFIC_BYTES = {"dsv3_mxfp8": 8 * (1.0400 + 0.0178 + 0.5019 + 0.0980) * 1e9}
 
 
 def load_peaks():
