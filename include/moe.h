@@ -453,7 +453,8 @@ int moe_expert_wgrad(const void* duv, const void* x, const void* dout, const voi
                      size_t workspace_bytes, void* stream);
 
 /* The backward of the layer, one kernel per step on `stream`: reverse combine,
- * expert dgrad, reverse dispatch, router gradient, expert weight gradients.
+ * expert dgrad, reverse dispatch, router gradient, expert weight gradients.  With
+ * N = 0 every weight gradient is zero (dx has no rows).
  *   dout : [N][H] BF16;  x, w_router : the forward's inputs;  saved : filled by
  *   moe_forward_train;  wt_* : moe_pack_expert_weights_dgrad's output
  *   dx : [N][H] BF16;  dw_router : [E][H] FP32;  dbias : [E] FP32 or NULL;

@@ -360,3 +360,21 @@ def test_expert_wgrad_matches_oracle(M, dtype, N, H, I, E, k, hot, empty):
         err = max(row_rel_err(g_gu[e, :I], dwg).max(), row_rel_err(g_gu[e, I:], dwu).max(),
                   row_rel_err(g_d[e], dwdn).max())
         assert err < 2e-2, (e, counts[e], err)
+
+
+def test_backward_empty_batch_zeroes_weight_gradients(M):
+    """N = 0: no expert has slots, so every weight gradient is zero."""
+    w = synth.Workload("bwd_empty", N=0, H=512, I=256, E=8, k=2, S=1, dtype="mxfp8")
+    shape = M.Shape.of(w)
+    ws = torch.empty(max(M.moe_backward_workspace_bytes(shape), 256), dtype=torch.uint8, device="cuda")
+    M.moe_workspace_init(ws)
+    dummy = torch.empty(64, dtype=torch.bfloat16, device="cuda")
+    dwr = torch.full((w.E, w.H), float("nan"), device="cuda")
+    db = torch.full((w.E,), float("nan"), device="cuda")
+    dwgu = torch.full((w.E, 2 * w.I, w.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dwd = torch.full((w.E, w.H, w.I), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.moe_backward(dummy, dummy, dummy, M.Saved(), dummy, None, dummy, None, shape, None, dummy, dwr, db,
+                   dwgu, dwd, ws)
+    assert M.moe_last_device_status(ws) == 0
+    for t in (dwr, db, dwgu, dwd):
+        assert not t.float().isnan().any() and not t.float().any()

@@ -68,13 +68,17 @@ def test_forward_empty_batch():
 
 
 # Degenerate shapes: top-1 with a ragged token count, every token on every
-# expert (k = E), a single expert (a dense SwiGLU FFN), and a bias so steep that
-# every token picks the same two experts (fourteen experts without slots).
+# expert (k = E), a single expert (a dense SwiGLU FFN), a bias so steep that
+# every token picks the same two experts (fourteen experts without slots), 512
+# experts, and k = 32.
 DEGENERATE = [
     synth.Workload("top1_ragged", N=300, H=512, I=256, E=16, k=1, S=3, dtype="mxfp8"),
     synth.Workload("k_eq_E", N=256, H=512, I=256, E=4, k=4, S=2, dtype="mxfp8"),
     synth.Workload("one_expert", N=200, H=256, I=128, E=1, k=1, S=2, dtype="bf16"),
     synth.Workload("two_hot", N=384, H=512, I=256, E=16, k=2, S=4, dtype="mxfp8", skew=50.0),
+    # more experts than the tensor-core router takes (the SIMT router), and the largest k
+    synth.Workload("many_experts", N=512, H=512, I=256, E=512, k=8, S=4, dtype="mxfp8"),
+    synth.Workload("top32", N=256, H=512, I=256, E=64, k=32, S=2, dtype="mxfp8"),
 ]
 
 

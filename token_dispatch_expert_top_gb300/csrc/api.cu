@@ -868,7 +868,18 @@ int moe_backward(const void* dout, const void* x, const void* w_router, const mo
     (void)params;
     const moe_shape_t& s = *shape;
     if (!saved) return MOE_ERR_INVALID_ARG;
-    if (s.N == 0) return MOE_OK;
+    if (s.N == 0) {
+        // an empty batch: no expert has slots, so every weight gradient is zero (dx has
+        // no rows)
+        cudaStream_t st = (cudaStream_t)stream;
+        cudaError_t e = cudaSuccess;
+        if (dw_router) e = cudaMemsetAsync(dw_router, 0, (size_t)s.E * s.H * sizeof(float), st);
+        if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, (size_t)s.E * sizeof(float), st);
+        if (e == cudaSuccess && dw_gate_up)
+            e = cudaMemsetAsync(dw_gate_up, 0, (size_t)s.E * 2 * s.I * s.H * 2, st);
+        if (e == cudaSuccess && dw_down) e = cudaMemsetAsync(dw_down, 0, (size_t)s.E * s.H * s.I * 2, st);
+        return cuda_status(e);
+    }
     const bool mx = s.dtype == MOE_MXFP8;
     const BwdPlan pl = make_bwd_plan(s);
     void* ws = workspace;
