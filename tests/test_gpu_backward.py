@@ -266,6 +266,8 @@ BWD_LAYERS = [
     synth.Workload("bwd_mx_skew", N=512, H=1024, I=256, E=32, k=8, S=4, dtype="mxfp8", skew=3.0),
     # top-1: the renormalised gate is exactly 1, so the router gets no gradient
     synth.Workload("bwd_top1", N=256, H=512, I=256, E=16, k=1, S=2, dtype="mxfp8"),
+    # the largest expert count the library takes; many experts have no slots
+    synth.Workload("bwd_max_experts", N=512, H=256, I=128, E=1024, k=4, S=4, dtype="bf16"),
 ]
 
 
@@ -295,10 +297,18 @@ def test_backward_layer_matches_oracle(M, w):
     assert np.abs(to_np(db) - ref["dbias"]).max() <= tol * np.abs(ref["dbias"]).max()
     if w.k == 1:
         assert not to_np(dwr).any() and not to_np(db).any()
-    # expert weight gradients: every row of every expert with slots; zeros otherwise
+    # expert weight gradients: every row of every expert with at least 4 slots; an
+    # expert with fewer has a gradient of rank < 4 whose row i scales with one du_i
+    # (itself an FP32 sum rounded to BF16 that cancellation can leave a few BF16 ulps
+    # off), so it is measured against its whole matrix's largest entry; zeros otherwise
     g_gu, g_d = to_np(dwgu), to_np(dwd)
-    err_w = max(row_rel_err(g_gu[used].reshape(-1, w.H), ref["dw_gate_up"][used].reshape(-1, w.H)).max(),
-                row_rel_err(g_d[used].reshape(-1, w.I), ref["dw_down"][used].reshape(-1, w.I)).max())
+    cnt = np.diff(live)
+    many, few = cnt >= 4, (cnt > 0) & (cnt < 4)
+    err_w = max(row_rel_err(g_gu[many].reshape(-1, w.H), ref["dw_gate_up"][many].reshape(-1, w.H)).max(initial=0),
+                row_rel_err(g_d[many].reshape(-1, w.I), ref["dw_down"][many].reshape(-1, w.I)).max(initial=0))
+    for e in np.flatnonzero(few):
+        for got, want in ((g_gu[e], ref["dw_gate_up"][e]), (g_d[e], ref["dw_down"][e])):
+            err_w = max(err_w, np.abs(got - want).max() / max(np.abs(want).max(), 1e-30))
     assert err_w < tol, err_w
     assert np.all(g_gu[~used] == 0.0) and np.all(g_d[~used] == 0.0)
     # deterministic: a second backward is bitwise identical

@@ -70,7 +70,7 @@ def test_forward_empty_batch():
 # Degenerate shapes: top-1 with a ragged token count, every token on every
 # expert (k = E), a single expert (a dense SwiGLU FFN), a bias so steep that
 # every token picks the same two experts (fourteen experts without slots), 512
-# experts, and k = 32.
+# experts, k = 32, and the largest expert count the library takes (1024).
 DEGENERATE = [
     synth.Workload("top1_ragged", N=300, H=512, I=256, E=16, k=1, S=3, dtype="mxfp8"),
     synth.Workload("k_eq_E", N=256, H=512, I=256, E=4, k=4, S=2, dtype="mxfp8"),
@@ -79,6 +79,7 @@ DEGENERATE = [
     # more experts than the tensor-core router takes (the SIMT router), and the largest k
     synth.Workload("many_experts", N=512, H=512, I=256, E=512, k=8, S=4, dtype="mxfp8"),
     synth.Workload("top32", N=256, H=512, I=256, E=64, k=32, S=2, dtype="mxfp8"),
+    synth.Workload("max_experts", N=1024, H=256, I=128, E=1024, k=8, S=8, dtype="mxfp8"),
 ]
 
 
