@@ -249,9 +249,15 @@ def gpu_arm(args, rank, world):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # ---- value: moe_forward, device-resident inputs
+    def fwd(**kw):
+        if args.macrobatches > 1:
+            return layer.forward_macrobatched(args.macrobatches, x=kw.get("x"), out=kw.get("out"),
+                                              stream=kw.get("stream"))
+        return layer.forward(fused=args.fused, **kw)
+
+    # ---- value: moe_forward (or its macrobatched / fused form), device-resident inputs
     for _ in range(args.warmup):
-        layer.forward(fused=args.fused)
+        fwd()
     status = layer.device_status()
     if status != 0:
         raise RuntimeError(f"device status {M.status_name(status)} after warm-up")
@@ -260,7 +266,7 @@ def gpu_arm(args, rank, world):
     with ClockSampler(dev.index) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
-            layer.forward(fused=args.fused)
+            fwd()
         ev1.record(stream)
         barrier()
     t_ms = ev0.elapsed_time(ev1)
@@ -311,7 +317,7 @@ def gpu_arm(args, rank, world):
             stream.wait_event(h2d_done[b])
             if d2h_done[b] is not None:
                 stream.wait_event(d2h_done[b])                        # out_dev[b] read back
-            layer.forward(x=x_dev[b], fused=args.fused, out=out_dev[b], stream=stream)
+            fwd(x=x_dev[b], out=out_dev[b], stream=stream)
             comp_done[b] = ev()
             comp_done[b].record(stream)
             with torch.cuda.stream(s_d2h):
@@ -332,7 +338,7 @@ def gpu_arm(args, rank, world):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    assert torch.equal(out_host[(args.steps - 1) % 2].to(dev), layer.forward()), "e2e output differs"
+    assert torch.equal(out_host[(args.steps - 1) % 2].to(dev), fwd()), "e2e output differs"
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e = {"value": job_rate(w.N, args.steps, e2e_ms, world), "unit": "tokens/s",
            "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
@@ -386,7 +392,9 @@ def gpu_arm(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), drawn on the device)",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
-                   "S": w.S, "skew": w.skew, "path": "fused" if args.fused else "staged",
+                   "S": w.S, "skew": w.skew,
+                   "path": ("fused" if args.fused else
+                            f"staged, {args.macrobatches} macrobatches" if args.macrobatches > 1 else "staged"),
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: ~11.6 GB of MXFP8 expert weights streamed per step"},
         "layer_tflops": round(layer_tflops, 2),
@@ -397,7 +405,7 @@ def gpu_arm(args, rank, world):
         "hbm_peak_gbs": hbm, "hbm_peak_source": peak_src,
         "roofline": roofline,
         "nvfp4_quantize": nvfp4_quant_figures(M, layer.x, args.steps, hbm) if w.dtype != "f32" else None,
-        "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps,
+        "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps * max(1, args.macrobatches),
         "clocks": clk.summary(),
         "e2e": e2e,
     }
@@ -687,6 +695,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="dsv3_mxfp8", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--fused", action="store_true", help="time moe_forward_fused")
+    ap.add_argument("--macrobatches", type=int, default=1,
+                    help="time moe_forward_macrobatched with this many macrobatches")
     ap.add_argument("--sample-tokens", type=int, default=2,
                     help="tokens per oracle sample (CPU baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -121,6 +121,29 @@ const char* moe_status_string(int status);
 int moe_quantize_mxfp8(const void* in, int in_dtype, int64_t rows, int64_t K,
                        uint8_t* codes, uint8_t* scales, void* stream);
 
+/* Macrobatched forward: the N tokens are cut into `macrobatches` equal, consecutive
+ * macrobatches that run the staged path one after another on `stream`, while each
+ * macrobatch's combine runs on a second stream of the library's, so it overlaps the
+ * routing, layout and dispatch of the next macrobatch ([MoK-2.37x] section 02:
+ * the previous macrobatch's combine overlaps the next one's dispatch; [Kittens],
+ * ring-buffer paragraph).  Every step is per token or per slot, so `out` is
+ * bitwise equal to moe_forward's.  On one GPU the expert weights are streamed once
+ * per macrobatch, so more macrobatches are slower; the split serves the pipelined
+ * exchange of a multi-GPU layer.
+ *   N must be a multiple of macrobatches * S;  out : [N][H] (as moe_forward)
+ *   workspace : moe_macro_workspace_bytes() bytes, 256-byte aligned: one slice per
+ *               macrobatch of moe_workspace_bytes(shape with N / macrobatches)
+ *               rounded up to 256 bytes; the status word of every slice must be
+ *               zeroed with moe_workspace_init() before first use, and device errors
+ *               are recorded in the slice of the macrobatch that met them.
+ * The call returns after queueing; `stream` waits for every combine.  The second
+ * stream is created on the first call on a device. */
+size_t moe_macro_workspace_bytes(const moe_shape_t* shape, const moe_params_t* params, int macrobatches);
+int moe_forward_macrobatched(const void* x, const void* w_router, const float* bias, const void* w_gate_up,
+                             const void* w_gu_scales, const void* w_down, const void* w_d_scales,
+                             const moe_shape_t* shape, const moe_params_t* params, int macrobatches,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream);
+
 /* NVFP4 quantisation along K of a row-major [rows][K] matrix.  [Kittens] names
  * NVFP4, beside MXFP8, as a format of the team's earlier training kernels without
  * defining it (paragraph on the year of compute-only kernels); the format taken is the OCP MX v1.0 FP4 E2M1 element

@@ -95,3 +95,28 @@ def test_forward_degenerate_shapes(w):
     fused = layer.forward(fused=True)
     assert layer.device_status() == 0
     assert torch.equal(fused, staged)
+
+
+@pytest.mark.parametrize("w,macro", [(LAYER_CASES[2][0], 2), (LAYER_CASES[2][0], 4), (LAYER_CASES[1][0], 2),
+                                     (LAYER_CASES[3][0], 3)],
+                         ids=["mid_mxfp8-2", "mid_mxfp8-4", "mid_bf16-2", "mid_mxfp8_skew-3"])
+def test_macrobatched_forward_is_bitwise_equal(w, macro):
+    """Macrobatches (each combine on the library's second stream, overlapping the next
+    macrobatch's routing, layout and dispatch) give moe_forward's output bit for bit."""
+    need_cuda()
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+    layer = MoeLayer(w, synth.make_inputs(w, device="cpu"))
+    ref = layer.forward().clone()
+    for _ in range(3):
+        got = layer.forward_macrobatched(macro)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    assert layer.device_status() == 0
+
+
+def test_macrobatched_forward_rejects_uneven_split():
+    need_cuda()
+    from token_dispatch_expert_top_gb300 import moe as M
+    w = LAYER_CASES[2][0]          # N = 512, S = 4
+    assert M.moe_macro_workspace_bytes(M.Shape.of(w), None, 3) == 0     # 512 % (3 * 4) != 0
+    assert M.moe_macro_workspace_bytes(M.Shape.of(w), None, 4) > 0

@@ -462,13 +462,16 @@ int moe_combine(const void* y, const int32_t* inv, const float* gate, const moe_
 }
 
 // The staged forward; with `sv`, the routing, layout, y and u|v go to the
-// caller's saved-activation buffers (training).
+// caller's saved-activation buffers (training).  With `combine_stream`, the
+// combine runs there after `ffn_done` (recorded on `stream` once the FFN is
+// issued), so the caller's stream can go on to the next macrobatch.
 static int forward_staged(const void* x, const void* w_router, const float* bias,
                           const void* w_gate_up, const void* w_gu_scales, const void* w_down,
                           const void* w_d_scales, const moe_shape_t* shape,
                           const moe_params_t* params, void* out, int32_t* idx_out, float* gate_out,
                           const moe_saved_t* sv, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+                          void* stream, cudaStream_t combine_stream = nullptr,
+                          cudaEvent_t ffn_done = nullptr) {
     int rc = check_shape(shape);
     if (rc) return rc;
     rc = check_ws(shape, params, workspace, workspace_bytes);
@@ -527,6 +530,13 @@ static int forward_staged(const void* x, const void* w_router, const float* bias
                          w_d_scales, s, y, ws, timeout_of(params), st, sv ? sv->uv : nullptr);
     if (rc) return rc;
     // 5. combine + weighted merge
+    if (combine_stream) {
+        rc = cuda_status(cudaEventRecord(ffn_done, st));
+        if (rc) return rc;
+        rc = cuda_status(cudaStreamWaitEvent(combine_stream, ffn_done, 0));
+        if (rc) return rc;
+        st = combine_stream;
+    }
     rc = cuda_status(launch_combine(y, inv, gate, s.N, s.H, s.k, T, s.dtype, out,
                                     num_sms_current(), hdr, st));
     return rc;
@@ -538,6 +548,80 @@ int moe_forward(const void* x, const void* w_router, const float* bias, const vo
                 float* gate_out, void* workspace, size_t workspace_bytes, void* stream) {
     return forward_staged(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, shape,
                           params, out, idx_out, gate_out, nullptr, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- macrobatches
+// Workspace slice of one macrobatch (the shape with N / macrobatches tokens),
+// rounded up to 256 bytes; 0 if the split is not allowed.
+static size_t macro_slice_bytes(const moe_shape_t* shape, const moe_params_t* params, int macrobatches) {
+    if (check_shape(shape) != MOE_OK || macrobatches < 1) return 0;
+    if (shape->N % (macrobatches * shape->S) != 0) return 0;
+    moe_shape_t sm = *shape;
+    sm.N = shape->N / macrobatches;
+    if (sm.N == 0) return 0;
+    return (make_plan(sm, params).total + 255) / 256 * 256;
+}
+
+size_t moe_macro_workspace_bytes(const moe_shape_t* shape, const moe_params_t* params, int macrobatches) {
+    return macro_slice_bytes(shape, params, macrobatches) * (size_t)(macrobatches > 0 ? macrobatches : 0);
+}
+
+// A second stream per device for the macrobatches' combines, created on first use.
+static cudaStream_t macro_side_stream() {
+    static cudaStream_t side[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!side[dev] && cudaStreamCreateWithFlags(&side[dev], cudaStreamNonBlocking) != cudaSuccess)
+        side[dev] = nullptr;
+    return side[dev];
+}
+
+int moe_forward_macrobatched(const void* x, const void* w_router, const float* bias, const void* w_gate_up,
+                             const void* w_gu_scales, const void* w_down, const void* w_d_scales,
+                             const moe_shape_t* shape, const moe_params_t* params, int macrobatches,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    const moe_shape_t& s = *shape;
+    if (macrobatches < 1) return MOE_ERR_INVALID_ARG;
+    if (s.N == 0) return MOE_OK;
+    const size_t slice = macro_slice_bytes(shape, params, macrobatches);
+    if (slice == 0) return MOE_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < slice * (size_t)macrobatches) return MOE_ERR_WORKSPACE;
+    if (!x || !out) return MOE_ERR_INVALID_ARG;
+    moe_shape_t sm = s;
+    sm.N = s.N / macrobatches;
+    const size_t x_rows = (size_t)sm.N * s.H * op_elem(s.dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
+    const size_t o_rows = (size_t)sm.N * s.H * (s.dtype == MOE_F32 ? 4 : 2);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaStream_t side = macrobatches > 1 ? macro_side_stream() : nullptr;
+    if (macrobatches > 1 && !side) return MOE_ERR_CUDA;
+    // events: one per macrobatch (its FFN issued), one to join the side stream
+    cudaEvent_t ev[65] = {};
+    const int nev = macrobatches > 1 ? macrobatches + 1 : 0;
+    if (nev > 65) return MOE_ERR_UNSUPPORTED;
+    for (int i = 0; i < nev; ++i)
+        if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            return MOE_ERR_CUDA;
+        }
+    if (side) {   // the side stream starts after what the caller already queued
+        rc = cuda_status(cudaEventRecord(ev[macrobatches], st));
+        if (!rc) rc = cuda_status(cudaStreamWaitEvent(side, ev[macrobatches], 0));
+    }
+    for (int m = 0; !rc && m < macrobatches; ++m) {
+        rc = forward_staged((const uint8_t*)x + m * x_rows, w_router, bias, w_gate_up, w_gu_scales, w_down,
+                            w_d_scales, &sm, params, (uint8_t*)out + m * o_rows, nullptr, nullptr, nullptr,
+                            (uint8_t*)workspace + m * slice, slice, stream, side, side ? ev[m] : nullptr);
+    }
+    if (side) {   // the caller's stream resumes after every combine
+        const int rj = cuda_status(cudaEventRecord(ev[macrobatches], side));
+        const int rw = rj ? rj : cuda_status(cudaStreamWaitEvent(st, ev[macrobatches], 0));
+        if (!rc) rc = rw;
+    }
+    for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);   // released once their work completes
+    return rc;
 }
 
 int moe_forward_fused(const void* x, const void* w_router, const float* bias,

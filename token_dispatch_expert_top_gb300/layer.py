@@ -114,8 +114,32 @@ class MoeLayer:
            self.out if out is None else out, self.idx, self.gate, self.ws, stream)
         return self.out if out is None else out
 
+    def forward_macrobatched(self, macrobatches: int, x: torch.Tensor | None = None,
+                             out: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None):
+        """The forward in `macrobatches` macrobatches (moe_forward_macrobatched), on a
+        workspace of one slice per macrobatch, kept between calls."""
+        if getattr(self, "macro_n", None) != macrobatches:
+            nbytes = M.moe_macro_workspace_bytes(self.shape, self.params, macrobatches)
+            if nbytes == 0:
+                raise M.MoeError("moe_macro_workspace_bytes", M.MOE_ERR_INVALID_ARG)
+            self.macro_ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.out.device)
+            off = (-self.macro_ws.data_ptr()) % 256            # 256-byte aligned slices
+            self.macro_ws = self.macro_ws[off:off + nbytes]
+            self.macro_slice = nbytes // macrobatches
+            for m in range(macrobatches):
+                M.moe_workspace_init(self.macro_ws[m * self.macro_slice:(m + 1) * self.macro_slice])
+            self.macro_n = macrobatches
+        M.moe_forward_macrobatched(self.x if x is None else x, self.w_router, self.bias, self.wgu,
+                                   self.wgu_sf, self.wd, self.wd_sf, self.shape, self.params, macrobatches,
+                                   self.out if out is None else out, self.macro_ws, stream)
+        return self.out if out is None else out
+
     def device_status(self) -> int:
-        return M.moe_last_device_status(self.ws)
+        status = M.moe_last_device_status(self.ws)
+        for m in range(getattr(self, "macro_n", 0) or 0):
+            s = M.moe_last_device_status(self.macro_ws[m * self.macro_slice:(m + 1) * self.macro_slice])
+            status = status or s
+        return status
 
     def forward_train(self, x: torch.Tensor | None = None, out: torch.Tensor | None = None,
                       stream: torch.cuda.Stream | None = None):

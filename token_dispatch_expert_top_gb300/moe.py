@@ -25,7 +25,8 @@ DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "mxfp8": MOE_MXFP8}
 
 ENTRY_POINTS = (
     "moe_workspace_bytes", "moe_workspace_init", "moe_last_device_status", "moe_status_string",
-    "moe_quantize_mxfp8", "moe_quantize_nvfp4", "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
+    "moe_quantize_mxfp8", "moe_quantize_nvfp4", "moe_macro_workspace_bytes", "moe_forward_macrobatched",
+    "moe_route_topk", "moe_layout", "moe_dispatch_pull", "moe_expert_ffn",
     "moe_combine", "moe_forward", "moe_forward_fused", "moe_min_minibatch", "moe_layout_noalloc",
     "moe_pack_expert_weights", "moe_backward_workspace_bytes", "moe_pack_expert_weights_dgrad",
     "moe_expert_ffn_train", "moe_forward_train", "moe_reverse_combine", "moe_expert_ffn_dgrad",
@@ -83,6 +84,8 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_i]),
     "moe_quantize_mxfp8": (_i, [_vp, _i, _i64, _i64, _vp, _vp, _vp]),
     "moe_quantize_nvfp4": (_i, [_vp, _i, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "moe_macro_workspace_bytes": (_sz, [_shp, _prm, _i]),
+    "moe_forward_macrobatched": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _shp, _prm, _i, _vp, _vp, _sz, _vp]),
     "moe_route_topk": (_i, [_vp, _vp, _vp, _shp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_layout": (_i, [_vp, _shp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_dispatch_pull": (_i, [_vp, _vp, _shp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _sz, _vp]),
@@ -228,6 +231,19 @@ def moe_forward(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, s
         _p(x), _p(w_router), _p(bias), _p(w_gate_up), _p(w_gu_scales), _p(w_down), _p(w_d_scales),
         ctypes.byref(shape), ctypes.byref(params) if params else None, _p(out), _p(idx_out),
         _p(gate_out), _p(ws), _wsz(ws), _stream(stream)))
+
+
+def moe_macro_workspace_bytes(shape: Shape, params: Params | None, macrobatches: int) -> int:
+    return _lib.moe_macro_workspace_bytes(ctypes.byref(shape), ctypes.byref(params) if params else None,
+                                          macrobatches)
+
+
+def moe_forward_macrobatched(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, shape: Shape,
+                             params: Params | None, macrobatches: int, out, ws, stream=None) -> None:
+    _check("moe_forward_macrobatched", _lib.moe_forward_macrobatched(
+        _p(x), _p(w_router), _p(bias), _p(w_gate_up), _p(w_gu_scales), _p(w_down), _p(w_d_scales),
+        ctypes.byref(shape), ctypes.byref(params) if params else None, macrobatches, _p(out), _p(ws),
+        _wsz(ws), _stream(stream)))
 
 
 def moe_forward_fused(x, w_router, bias, w_gate_up, w_gu_scales, w_down, w_d_scales, shape: Shape,
