@@ -249,11 +249,13 @@ def gpu_arm(args, rank, world):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    rev = M.Params(0, 0, 0, 0, 0, 0, 1) if args.reverse_ring else None
+
     def fwd(**kw):
         if args.macrobatches > 1:
             return layer.forward_macrobatched(args.macrobatches, x=kw.get("x"), out=kw.get("out"),
                                               stream=kw.get("stream"))
-        return layer.forward(fused=args.fused, **kw)
+        return layer.forward(fused=args.fused, params=rev, **kw)
 
     # ---- value: moe_forward (or its macrobatched / fused form), device-resident inputs
     for _ in range(args.warmup):
@@ -393,7 +395,7 @@ def gpu_arm(args, rank, world):
         "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), drawn on the device)",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
                    "S": w.S, "skew": w.skew,
-                   "path": ("fused" if args.fused else
+                   "path": (("fused, reverse ring" if args.reverse_ring else "fused") if args.fused else
                             f"staged, {args.macrobatches} macrobatches" if args.macrobatches > 1 else "staged"),
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: ~11.6 GB of MXFP8 expert weights streamed per step"},
@@ -697,6 +699,8 @@ def main():
     ap.add_argument("--fused", action="store_true", help="time moe_forward_fused")
     ap.add_argument("--macrobatches", type=int, default=1,
                     help="time moe_forward_macrobatched with this many macrobatches")
+    ap.add_argument("--reverse-ring", action="store_true",
+                    help="with --fused: minibatches walk the slots from the last one down")
     ap.add_argument("--sample-tokens", type=int, default=2,
                     help="tokens per oracle sample (CPU baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -93,6 +93,11 @@ typedef struct {
     int test_skip_ready;   /* test hook, 0 = off.  When m+1 > 0, the gather role never
                               publishes minibatch m, so the compute role's bounded
                               wait runs out and the call reports MOE_ERR_TIMEOUT.  */
+    int reverse_ring;      /* fused forward: 0 = minibatches walk the slots in order; 1 =
+                              in reverse, the last slots first ([Kittens], ring-buffer
+                              paragraph: the forward walks the ring backwards so the
+                              backward finds the last activations still resident).
+                              The output is the same bit for bit.                    */
 } moe_params_t;
 
 /* Bytes of workspace every entry point below needs for this shape and these

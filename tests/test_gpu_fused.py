@@ -26,8 +26,8 @@ def _layers(w, params_list):
     return M, MoeLayer, inp
 
 
-def _params(M, ring=0, mb=0, g=0, c=0, timeout_ns=0, skip=0):
-    return M.Params(ring, mb, g, c, timeout_ns, skip)
+def _params(M, ring=0, mb=0, g=0, c=0, timeout_ns=0, skip=0, reverse=0):
+    return M.Params(ring, mb, g, c, timeout_ns, skip, reverse)
 
 
 @pytest.mark.parametrize("w", [MID_MX, MID_BF16, SKEW_MX], ids=lambda w: w.name)
@@ -101,3 +101,17 @@ def test_fused_rejects_bad_ring():
         layer.forward(fused=True, params=_params(M, ring=100, mb=64))     # ring not a multiple
     with pytest.raises(M.MoeError):
         layer.forward(fused=True, params=_params(M, g=100000))            # more CTAs than fit
+
+
+@pytest.mark.parametrize("w,ring,mb,g", [(SKEW_MX, 0, 0, 0), (SKEW_MX, 256, 128, 4), (SKEW_MX, 1024, 512, 16),
+                                         (SKEW_MX, 96, 32, 2), (MID_MX, 0, 0, 0), (MID_BF16, 128, 64, 2)],
+                         ids=["skew-default", "skew-256", "skew-1024", "skew-96", "mid-default", "bf16-128"])
+def test_fused_reverse_ring_traversal_bitwise(w, ring, mb, g):
+    """Minibatches cut from the last slot down (reverse ring traversal) give the
+    same output bit for bit."""
+    M, MoeLayer, inp = _layers(w, None)
+    layer = MoeLayer(w, inp, params=_params(M, ring=ring, mb=mb, g=g))
+    staged = layer.forward().clone()
+    fused = layer.forward(fused=True, params=_params(M, ring=ring, mb=mb, g=g, reverse=1))
+    assert layer.device_status() == 0
+    assert torch.equal(fused, staged), (ring, mb, g)

@@ -711,6 +711,7 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
     c.row_bytes = row_bytes;
     c.sf_bytes = mx ? s.H / 32 : 0;
     c.skip_ready = (params && params->test_skip_ready > 0) ? params->test_skip_ready - 1 : -1;
+    c.reverse = (params && params->reverse_ring) ? 1 : 0;
     c.sched = sched;
     c.inv = inv;
     c.gate = gate;

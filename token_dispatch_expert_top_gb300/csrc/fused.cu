@@ -143,11 +143,39 @@ __device__ int minibatch_cut(const int32_t* off, int E, int T, int MB, int lo) {
     return target;
 }
 
+// Start of the minibatch that ends at slot hi when the slots are cut from the
+// last one down (reverse traversal): the mirror of minibatch_cut.  It starts on
+// an expert boundary when one falls in the minibatch's upper half of slots, else
+// inside the expert that crosses hi - MB at a whole number of 128-row m-tiles from
+// that expert's start (rounded up, so the minibatch holds at most MB slots).
+__device__ int minibatch_cut_rev(const int32_t* off, int E, int MB, int hi) {
+    const int target = hi - MB;
+    if (target <= 0) return 0;
+    const int half = MB / 2 > 1 ? MB / 2 : 1;
+    int a = 0, z = E - 1;                 // expert e with off[e] <= target < off[e+1]
+    while (a < z) {
+        const int mid = (a + z + 1) >> 1;
+        if (off[mid] <= target) a = mid; else z = mid - 1;
+    }
+    if (off[a] == target) return target;
+    if (hi - off[a + 1] >= half) return off[a + 1];
+    const int c2 = off[a] + ((target - off[a] + tc::BM - 1) / tc::BM) * tc::BM;
+    if (c2 < hi && hi - c2 >= half) return c2;
+    return target;
+}
+
+// Minibatch b is the slots between cut[b] and cut[b+1] (ascending cuts in slot
+// order, descending in reverse traversal).
+__device__ __forceinline__ void minibatch_range(const int32_t* cut, int b, int& lo, int& hi) {
+    lo = min(cut[b], cut[b + 1]);
+    hi = max(cut[b], cut[b + 1]);
+}
+
 // One block: cuts the slots into minibatches, then per-minibatch m-tile counts,
 // prefixes and first experts; zeroes the counters.
 __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restrict__ offsets, int E,
                                                           int T, int MB, int nmb_max, int nt1, int nt2,
-                                                          int interleave, FusedPlan plan,
+                                                          int interleave, int reverse, FusedPlan plan,
                                                           int counters_len, int* counters, WsHeader* ws) {
     extern __shared__ int32_t off[];
     __shared__ int s_nmb;
@@ -155,20 +183,32 @@ __global__ void __launch_bounds__(1024) fused_plan_kernel(const int32_t* __restr
     for (int i = threadIdx.x; i < counters_len; i += blockDim.x) counters[i] = 0;
     __syncthreads();
     if (threadIdx.x == 0) {
-        int b = 0, lo = 0;
-        while (lo < T && b < nmb_max) {
-            plan.cut[b++] = lo;
-            lo = minibatch_cut(off, E, T, MB, lo);
+        int b = 0;
+        if (!reverse) {
+            int lo = 0;
+            while (lo < T && b < nmb_max) {
+                plan.cut[b++] = lo;
+                lo = minibatch_cut(off, E, T, MB, lo);
+            }
+            if (lo < T) set_status(ws, MOE_ERR_DEVICE_CHECK);   // cannot happen: the bound holds
+            plan.cut[b] = T;
+        } else {
+            int hi = T;
+            while (hi > 0 && b < nmb_max) {
+                plan.cut[b++] = hi;
+                hi = minibatch_cut_rev(off, E, MB, hi);
+            }
+            if (hi > 0) set_status(ws, MOE_ERR_DEVICE_CHECK);   // cannot happen: the bound holds
+            plan.cut[b] = 0;
         }
-        if (lo < T) set_status(ws, MOE_ERR_DEVICE_CHECK);   // cannot happen: the bound holds
-        plan.cut[b] = T;
         *plan.nmb = b;
         s_nmb = b;
     }
     __syncthreads();
     const int nmb = s_nmb;
     for (int b = threadIdx.x; b < nmb; b += blockDim.x) {
-        const int lo = plan.cut[b], hi = plan.cut[b + 1];
+        int lo, hi;
+        minibatch_range(plan.cut, b, lo, hi);
         int a = 0, z = E;  // first e with off[e+1] > lo
         while (a < z) {
             const int mid = (a + z) >> 1;
@@ -267,7 +307,8 @@ struct MinibatchTiles {
         int r = t - tb[lo];              // tile within the segment
         TileInfo tl;
         tl.kind = sg.kind;
-        const int s_lo = ct[b], s_hi = ct[b + 1];
+        int s_lo, s_hi;
+        minibatch_range(ct, b, s_lo, s_hi);
         int e = el[b], mbase = 0, mt = 0;   // expert piece, its first m-tile index, its m-tiles
         for (; e < a->E; ++e) {
             const int len = min(off[e + 1], s_hi) - max(off[e], s_lo);
@@ -361,7 +402,8 @@ __device__ __forceinline__ void copy_slot_row(uint8_t* __restrict__ dst, const u
 __device__ void gather_minibatch(const FusedArgs& a, int b, int gw, int nw) {
     const int lane = threadIdx.x & 31;
     const FusedPlan& pl = a.plan;
-    const int lo = pl.cut[b], hi = pl.cut[b + 1];
+    int lo, hi;
+    minibatch_range(pl.cut, b, lo, hi);
     const int base = (b % a.NR) * a.MB;
     for (int t = lo + gw; t < hi; t += nw) {
         const int s = a.sched[2 * (int64_t)t];
@@ -397,7 +439,8 @@ __device__ int gather_stream_bulk(const FusedArgs& a, int b, int gs, int ns, uin
                                   int nbuf, int q0, volatile int* abort_flag, unsigned long long deadline) {
     const int lane = threadIdx.x & 31;
     const FusedPlan& pl = a.plan;
-    const int lo = pl.cut[b], hi = pl.cut[b + 1];
+    int lo, hi;
+    minibatch_range(pl.cut, b, lo, hi);
     const int base = (b % a.NR) * a.MB;
     const int unit = a.row_bytes + a.sf_bytes;
     const int nslots = hi - lo;
@@ -694,7 +737,7 @@ cudaError_t launch_fused_forward(const FusedCall& c, cudaStream_t stream) {
     GemmSide s1, s2;
     if (!encode_ffn_maps(c.ffn, &m, &s1, &s2)) return cudaErrorInvalidValue;
     fused_plan_kernel<<<1, 1024, sizeof(int32_t) * (c.E + 1), stream>>>(
-        c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles, s2.n_tiles, (c.R / c.MB) >= 2 ? 1 : 0, pl,
+        c.ffn.offsets, c.E, c.T, c.MB, c.nmb, s1.n_tiles, s2.n_tiles, (c.R / c.MB) >= 2 ? 1 : 0, c.reverse, pl,
         counters_len, counters, c.ffn.ws);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -185,6 +185,7 @@ struct FusedCall {
     int MB, R, nmb, G, C;
     int row_bytes, sf_bytes;
     int skip_ready;           // -1: none
+    int reverse;              // minibatches cut from the last slot down
     const int32_t* sched;
     const int32_t* inv;
     const float* gate;

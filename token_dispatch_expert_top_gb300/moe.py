@@ -53,7 +53,8 @@ class Shape(ctypes.Structure):
 class Params(ctypes.Structure):
     _fields_ = [("ring_slots", ctypes.c_int), ("minibatch", ctypes.c_int),
                 ("gather_ctas", ctypes.c_int), ("compute_ctas", ctypes.c_int),
-                ("timeout_ns", ctypes.c_longlong), ("test_skip_ready", ctypes.c_int)]
+                ("timeout_ns", ctypes.c_longlong), ("test_skip_ready", ctypes.c_int),
+                ("reverse_ring", ctypes.c_int)]
 
 
 class Saved(ctypes.Structure):
