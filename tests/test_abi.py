@@ -105,3 +105,21 @@ def test_backward_host_checks():
     # misaligned du|dv output
     assert lib.moe_expert_ffn_dgrad(16, 16, 32, 16, 16, 16, 16, 16, ctypes.byref(mx), 48, 32, 16, 32,
                                     32, 1 << 20, None) == M.MOE_ERR_INVALID_ARG
+
+
+def test_macrobatch_host_checks():
+    """Macrobatch workspace sizing and argument errors, decided on the host."""
+    w = synth.Workload("mb", N=512, H=512, I=256, E=16, k=4, S=4, dtype="mxfp8")
+    shape = M.Shape.of(w)
+    one = M.moe_workspace_bytes(M.Shape.of(w.scaled(N=256)), None)
+    assert M.moe_macro_workspace_bytes(shape, None, 2) == 2 * ((one + 255) // 256 * 256)
+    assert M.moe_macro_workspace_bytes(shape, None, 3) == 0      # 512 is not a multiple of 3 * 4
+    assert M.moe_macro_workspace_bytes(shape, None, 0) == 0
+    lib = M.lib()
+    args = [None] * 7 + [ctypes.byref(shape), None]
+    assert lib.moe_forward_macrobatched(*args, 0, None, None, 0, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_macrobatched(*args, 3, None, None, 0, None) == M.MOE_ERR_INVALID_ARG
+    assert lib.moe_forward_macrobatched(*args, 2, None, None, 0, None) == M.MOE_ERR_WORKSPACE
+    # the reverse-ring flag sits at the end of moe_params_t; it leaves the workspace unchanged
+    p = M.Params(0, 0, 0, 0, 0, 0, 1)
+    assert M.moe_workspace_bytes(shape, p) == M.moe_workspace_bytes(shape, M.Params(0, 0, 0, 0, 0, 0, 0))
