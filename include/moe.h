@@ -61,7 +61,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
-    MOE_ERR_UNSUPPORTED = 2,   /* a shape or dtype this build has no kernel for */
+    MOE_ERR_UNSUPPORTED = 2,   /* a shape or dtype the library has no kernel for */
     MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_bytes() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (see moe_params_t.timeout_ns) */
