@@ -20,6 +20,20 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+constexpr int kLayoutIters = kLayoutChunk / 32;
+
+// A warp's expert ids of one chunk, all loads issued before any is used (lane l
+// holds choice begin + 32*i + l in v[i]; -1 past the end), so a chunk costs one
+// load latency rather than one per 32 choices.
+__device__ __forceinline__ void load_chunk(const int32_t* __restrict__ idx, int begin, int end, int lane,
+                                           int (&v)[kLayoutIters]) {
+#pragma unroll
+    for (int i = 0; i < kLayoutIters; ++i) {
+        const int t = begin + 32 * i + lane;
+        v[i] = (t < end) ? idx[t] : -1;
+    }
+}
+
 // Chunk c covers flat choices [c*kLayoutChunk, min((c+1)*kLayoutChunk, T)).
 // One warp per chunk; counts go to cnt[e][c] (expert-major, so that each
 // expert's per-chunk counts are contiguous for the scan).
@@ -31,13 +45,16 @@ __global__ void __launch_bounds__(kLayoutWarps * 32) layout_count_kernel(
     int32_t* hist = sh + warp * E;
     const int c = blockIdx.x * kLayoutWarps + warp;
     if (c >= nchunks) return;
-    for (int e = lane; e < E; e += 32) hist[e] = 0;
-    __syncwarp();
     const int begin = c * kLayoutChunk;
     const int end = min(begin + kLayoutChunk, T);
-    for (int base = begin; base < end; base += 32) {
-        const int t = base + lane;
-        int e = (t < end) ? idx[t] : -1;
+    int ev[kLayoutIters];
+    load_chunk(idx, begin, end, lane, ev);
+    for (int e = lane; e < E; e += 32) hist[e] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < kLayoutIters; ++i) {
+        const int t = begin + 32 * i + lane;
+        int e = ev[i];
         if (t < end && (e < 0 || e >= E)) {
             set_status(ws, MOE_ERR_DEVICE_CHECK);
             e = -1;
@@ -52,18 +69,40 @@ __global__ void __launch_bounds__(kLayoutWarps * 32) layout_count_kernel(
 // Exclusive scan over an int array of length n by one warp: each lane takes a
 // contiguous run, the run totals are scanned with shuffles.  Writes out[i] =
 // base + sum_{i' < i} in[i'] and returns the total (in every lane).
+// Runs of up to 8 values are held in registers, their loads issued together.
+__device__ __forceinline__ int warp_inclusive_sum(int s, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+    }
+    return s;
+}
+
 __device__ __forceinline__ int warp_exclusive_scan(const int32_t* in, int32_t* out, int n, int base,
                                                    int lane) {
     const int per = (n + 31) / 32;
     const int lo = min(lane * per, n), hi = min(lo + per, n);
+    if (per <= 8) {
+        int v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (lo + j < hi) ? in[lo + j] : 0;
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += v[j];
+        const int incl = warp_inclusive_sum(s, lane);
+        int run = base + incl - s;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (lo + j < hi) {
+                out[lo + j] = run;
+                run += v[j];
+            }
+        return __shfl_sync(0xffffffffu, incl, 31);
+    }
     int s = 0;
     for (int i = lo; i < hi; ++i) s += in[i];
-    int incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
+    const int incl = warp_inclusive_sum(s, lane);
     int run = base + incl - s;
     for (int i = lo; i < hi; ++i) {
         const int c = in[i];
@@ -97,6 +136,11 @@ __global__ void __launch_bounds__(kLayoutWarps * 32) layout_place_kernel(
     int32_t* off = sh;                         // [E+1]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     int32_t* cursor = sh + (E + 1) + warp * E;
+    const int c = blockIdx.x * kLayoutWarps + warp;
+    const int begin = c * kLayoutChunk;
+    const int end = min(begin + kLayoutChunk, T);
+    int ev[kLayoutIters];
+    load_chunk(idx, begin, end, lane, ev);   // in flight while the offsets are scanned
     if (warp == 0) {
         const int total = warp_exclusive_scan(counts, off, E, 0, lane);
         if (lane == 0) off[E] = total;
@@ -104,15 +148,13 @@ __global__ void __launch_bounds__(kLayoutWarps * 32) layout_place_kernel(
     __syncthreads();
     if (blockIdx.x == 0)
         for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
-    const int c = blockIdx.x * kLayoutWarps + warp;
     if (c >= nchunks) return;
     for (int e = lane; e < E; e += 32) cursor[e] = off[e] + base[(int64_t)e * nchunks + c];
     __syncwarp();
-    const int begin = c * kLayoutChunk;
-    const int end = min(begin + kLayoutChunk, T);
-    for (int b = begin; b < end; b += 32) {
-        const int t = b + lane;
-        int e = (t < end) ? idx[t] : -1;
+#pragma unroll
+    for (int i = 0; i < kLayoutIters; ++i) {
+        const int t = begin + 32 * i + lane;
+        int e = ev[i];
         if (e >= E) e = -1;
         const uint32_t same = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(same & lanemask_lt());
