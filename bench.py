@@ -231,6 +231,38 @@ def nvfp4_quant_figures(M, x: torch.Tensor, steps: int, hbm: float) -> dict:
             "algorithmic_bytes": nbytes, "l2": "flushed (256 MB write) before each call"}
 
 
+def router_figures(st, steps: int, hbm: float) -> dict:
+    """Time moe_route_topk as the layer calls it (x codes and scales written for
+    MXFP8), L2 flushed before each call.  Algorithmic bytes per call: x read once,
+    W_r read once, the x codes and scales and idx/gate written."""
+    M, L, w = st.M, st.L, st.L.w
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=L.x.device)
+
+    def call():
+        M.moe_route_topk(L.x, L.w_router, L.bias, L.shape, st.idx, st.gate, None, st.xq, st.xq_sf, L.ws)
+
+    for _ in range(3):
+        call()
+    total = 0.0
+    for _ in range(steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    ms = total / steps
+    nbytes = L.x.numel() * L.x.element_size() + L.w_router.numel() * L.w_router.element_size() \
+        + st.idx.numel() * 4 + st.gate.numel() * 4
+    if st.xq is not None:
+        nbytes += st.xq.numel() + st.xq_sf.numel()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"what": f"moe_route_topk, {w.N} tokens x {w.E} experts, H={w.H}", "ms": round(ms, 4),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "algorithmic_bytes": nbytes,
+            "l2": "flushed (256 MB write) before each call"}
+
+
 def gpu_arm(args, rank, world):
     from token_dispatch_expert_top_gb300 import moe as M
     from token_dispatch_expert_top_gb300.layer import MoeLayer
@@ -407,6 +439,7 @@ def gpu_arm(args, rank, world):
         "hbm_peak_gbs": hbm, "hbm_peak_source": peak_src,
         "roofline": roofline,
         "nvfp4_quantize": nvfp4_quant_figures(M, layer.x, args.steps, hbm) if w.dtype != "f32" else None,
+        "router": router_figures(st, args.steps, hbm),
         "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps * max(1, args.macrobatches),
         "clocks": clk.summary(),
         "e2e": e2e,

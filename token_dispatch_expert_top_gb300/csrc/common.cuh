@@ -137,6 +137,36 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     return true;
 }
 
+// The same wait with cluster-scope acquire: for a phase completed by arrivals
+// (release, cluster scope) from another CTA of the cluster, after which this
+// thread reads what that CTA wrote into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort, WsHeader* ws,
+                                                          unsigned long long deadline) {
+    uint32_t n = 0;
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort) return false;
+        if ((++n & 255u) == 0 && globaltimer_ns() > deadline) {
+            *abort = 1;
+            set_status(ws, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 // Orders generic-proxy accesses to GLOBAL memory with async-proxy (TMA, bulk
 // copy) accesses.  Restricted to the global state space: the unrestricted form
 // also covers the CTA's shared memory, where the thread's own TMA loads may be
@@ -323,6 +353,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                      mapa_shared(smem_u32(bar), rank))
+                 : "memory");
+}
+// 16-byte store into the shared memory of a CTA of this cluster (address from
+// mapa_shared).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
                  : "memory");
 }
 // Make barrier initialisation visible to the other CTAs of the cluster.

@@ -8,17 +8,18 @@
 // NVL72": section 01, each token picks a few experts per step; section 02, MXFP8
 // activation quantisation folded into the data path.)
 //
-// CTA = 16 warps:  w0 TMA producer (4-stage ring, 6 in split mode), w1 MMA issuer
-//                  + TMEM owner, w2-3 idle,
+// CTA = 16 warps:  w0 TMA producer (4-stage ring), w1 MMA issuer + TMEM owner,
+//                  w2-3 idle,
 //                  w4-11 x quantisers (MXFP8 only; two groups of four warps, one
-//                  token row per thread, each group every other K-stage; in split
-//                  mode all eight warps on every K-stage of the CTA's parity, one
-//                  32-element block per thread), w12-15 top-k epilogue.
-// Split mode (E >= 64, E % 32 == 0): a cluster of two CTAs shares a 128-token tile,
-// each computing the logits of half of the experts (twice the CTAs, half the
-// weight bytes each).  Each CTA quantises half of the K-stages of x.  The second
-// CTA hands its per-token top-k candidates to the first through distributed
-// shared memory; the first merges the two sorted lists and writes idx and gates.
+//                  token row per thread, each group every other K-stage),
+//                  w12-15 top-k epilogue.
+// Split mode (E >= 64, E % 32 == 0, H >= 128): a cluster of two CTAs shares a
+// 128-token tile, each taking half of K for every expert (twice the CTAs; each x
+// byte crosses from L2 once) and quantising its half of x.  The partial logits
+// then cross through distributed shared memory, into the partner's drained x
+// ring: each CTA completes the logits of half of the experts and takes their
+// top-k, and the second CTA hands its per-token candidates to the first, which
+// merges the two sorted lists and writes idx and gates.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "tmap.cuh"
@@ -28,25 +29,21 @@ namespace moe {
 namespace rt {
 constexpr int BM = 128;
 constexpr int A_BYTES = BM * 128;            // 128 tokens x 64 BF16
+constexpr int B_BYTES = 256 * 128;           // up to 256 experts x 64 BF16
 constexpr int THREADS = 512;
 constexpr int QUANT_WARPS = 8;
-// Shared-memory layout.  A CTA holds the weights of all E <= 256 experts (32 KB a
-// stage) in 4 stages, or in split mode those of E/2 <= 128 (16 KB a stage) in 6:
-// the same space, and 50% more bytes in flight for the latency-bound x stream.
-// The stage count is even, so a stage's index has the parity of its K-stages.
-template <bool SPLIT>
-struct Layout {
-    static constexpr int STAGES = SPLIT ? 6 : 4;
-    static constexpr int B_STRIDE = SPLIT ? 128 * 128 : 256 * 128;
-    static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_BAR = OFF_B + STAGES * B_STRIDE;
-    static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;   // full, empty, tfull, cand
-    static constexpr int OFF_BIAS = OFF_MISC + 16;
-    static constexpr int OFF_CAND = OFF_BIAS + 256 * 4;                // split mode: partner's candidates
-};
-template <bool SPLIT>
-inline size_t smem_bytes(int kmax) { return 1024 + Layout<SPLIT>::OFF_CAND + (size_t)kmax * BM * 8; }
+constexpr int STAGES = 4;                    // even: a stage's index has the parity of its K-stages
+// Shared-memory layout: a ring of x tiles and weight tiles.  In split mode the x
+// part of the ring (64 KB) afterwards receives the partner CTA's partial logits.
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, tfull, cand, qdone, pfree, xdata
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem base, abort flag
+constexpr int OFF_BIAS = OFF_MISC + 16;
+constexpr int OFF_CAND = OFF_BIAS + 256 * 4;       // split mode: partner's candidates
+inline size_t smem_bytes(int kmax) { return 1024 + OFF_CAND + (size_t)kmax * BM * 8; }
+static_assert(STAGES * A_BYTES >= BM * 128 * 4, "the x ring holds 128 partial logits per token");
 }  // namespace rt
 
 struct RouteArgs {
@@ -88,42 +85,48 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     RouteArgs args) {
     using namespace rt;
-    using L = Layout<SPLIT>;
-    constexpr int STAGES = L::STAGES;
-    constexpr int OFF_A = L::OFF_A, OFF_B = L::OFF_B, OFF_BAR = L::OFF_BAR, OFF_MISC = L::OFF_MISC;
-    constexpr int OFF_BIAS = L::OFF_BIAS, OFF_CAND = L::OFF_CAND, B_STRIDE = L::B_STRIDE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = full + 2 * STAGES;
-    uint64_t* cand_bar = full + 2 * STAGES + 1;
+    uint64_t* cand_bar = tfull + 1;     // split: the partner's top-k candidates are here
+    uint64_t* qdone = tfull + 2;        // split: this CTA's quantisers are past their last stage
+    uint64_t* pfree = tfull + 3;        // split: the partner's x ring may be overwritten
+    uint64_t* xdata = tfull + 4;        // split: the partner's partial logits are here
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     float* cand_v = reinterpret_cast<float*>(smem + OFF_CAND);                 // [BM][KMAX]
     int* cand_i = reinterpret_cast<int*>(smem + OFF_CAND + BM * KMAX * 4);     // [BM][KMAX]
+    // split: the partner's partial logits of this CTA's experts, [EH/4][BM][4] FP32,
+    // written over the x part of the ring once neither CTA reads it any more
+    float* xpart = reinterpret_cast<float*>(smem + OFF_A);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     float* sbias = reinterpret_cast<float*>(smem + OFF_BIAS);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int half = SPLIT ? (int)cluster_ctarank() : 0;      // which half of the experts
+    const int half = SPLIT ? (int)cluster_ctarank() : 0;      // which half of K, and of the experts' top-k
+    const uint32_t peer = (uint32_t)half ^ 1u;
     const int row0 = (SPLIT ? blockIdx.x / 2 : blockIdx.x) * BM;
     const int KB = args.H / 64;
-    const int E = SPLIT ? args.E / 2 : args.E;                // experts of this CTA
-    const int e0 = half * E;                                  // first of them
+    const int kb_lo = SPLIT ? half * ((KB + 1) / 2) : 0;     // first K-stage of this CTA
+    const int nkb = SPLIT ? (half ? KB / 2 : (KB + 1) / 2) : KB;
+    const int E = args.E;                                     // MMA width: every expert
+    const int EH = SPLIT ? E / 2 : E;                         // experts whose top-k this CTA takes
+    const int e0 = half * EH;                                 // first of them
     const uint32_t b_bytes = (uint32_t)E * 128;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            // MMA + the quantiser warps of the stage: in split mode all eight take
-            // the stages of this CTA's parity; otherwise a group of four takes the
-            // stages of its parity
-            const bool quantised = QUANT && (!SPLIT || (s & 1) == half);
-            mbar_init(&empty[s], quantised ? 1 + (SPLIT ? QUANT_WARPS : QUANT_WARPS / 2) : 1);
+            // MMA + the group of four quantiser warps that takes the stage
+            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS / 2 : 1);
         }
         mbar_init(tfull, 1);
         mbar_init(cand_bar, 4);                               // the partner's four epilogue warps
+        mbar_init(qdone, QUANT_WARPS);
+        mbar_init(pfree, 4);                                  // the partner's four epilogue warps
+        mbar_init(xdata, 4);                                  // the partner's four epilogue warps
         *abort_flag = 0;
         if (SPLIT)
             fence_mbar_init_cluster();
@@ -137,10 +140,10 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         tmem_relinquish();
     }
     if (warp >= 12)
-        for (int e = threadIdx.x - 384; e < E; e += 128) sbias[e] = args.bias ? args.bias[e0 + e] : 0.f;
+        for (int e = threadIdx.x - 384; e < EH; e += 128) sbias[e] = args.bias ? args.bias[e0 + e] : 0.f;
     tc_fence_before();
     __syncthreads();
-    if constexpr (SPLIT) cluster_sync();   // the first CTA's candidate barrier exists before any arrival
+    if constexpr (SPLIT) cluster_sync();   // the partner's barriers exist before any arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const unsigned long long deadline = globaltimer_ns() + args.timeout_ns;
@@ -149,11 +152,11 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int j = 0; j < nkb; ++j) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, args.ws, deadline)) break;
                 mbar_arrive_expect_tx(&full[stage], A_BYTES + b_bytes);
-                tma_load_2d(smem + OFF_A + stage * A_BYTES, &tmX, &full[stage], kb * 64, row0);
-                tma_load_2d(smem + OFF_B + stage * B_STRIDE, &tmW, &full[stage], kb * 64, e0);
+                tma_load_2d(smem + OFF_A + stage * A_BYTES, &tmX, &full[stage], (kb_lo + j) * 64, row0);
+                tma_load_2d(smem + OFF_B + stage * B_BYTES, &tmW, &full[stage], (kb_lo + j) * 64, 0);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1;
@@ -166,18 +169,18 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             const uint32_t idesc = idesc_bf16(BM, E);
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int j = 0; j < nkb; ++j) {
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + OFF_A + stage * A_BYTES);
-                const uint32_t sb = smem_u32(smem + OFF_B + stage * B_STRIDE);
+                const uint32_t sb = smem_u32(smem + OFF_B + stage * B_BYTES);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mma_bf16(tmem_base, sdesc_kmajor_sw128(sa + 32 * k), sdesc_kmajor_sw128(sb + 32 * k),
-                             idesc, (kb | k) != 0);
+                             idesc, (j | k) != 0);
                 mma_commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -188,26 +191,24 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         }
     } else if (warp >= 4 && warp < 12) {
         if constexpr (QUANT) {
-            // Each quantiser warp waits on the fills of its stages in order, one phase
-            // at a time: a warp that skipped a fill of a stage could take that
-            // fill's completed phase for the next one (the wait tests only parity).
-            //   non-split (4 stages): thread = (token row r, group g); group g takes
-            //     the K-stages of parity g (always stages g and g + 2), both 32-element
-            //     blocks of row r;
-            //   split (6 stages): all 256 threads take every K-stage of this CTA's
-            //     parity; thread = (token row r, block b) quantises block b of row r.
+            // Thread = (token row r, group g).  Group g takes this CTA's K-stages of
+            // parity g (always ring stages g and g + 2), both 32-element blocks of
+            // row r.  Each warp waits on the fills of its stages in order, one
+            // phase at a time: a warp that skipped a fill of a stage could take
+            // that fill's completed phase for the next one (the wait tests only
+            // parity).
             const int tq = (warp - 4) * 32 + lane;
             const int r = tq & (BM - 1);
             const int grp = tq >> 7;
             const int row = row0 + r;
-            const int kb_first = SPLIT ? half : grp;
-            const int b_first = SPLIT ? grp : 0, b_count = SPLIT ? 1 : 2;
-            for (int kb = kb_first; kb < KB; kb += 2) {
-                const int stage = kb % STAGES;
-                const uint32_t phase = (uint32_t)((kb / STAGES) & 1);
+            for (int j = grp; j < nkb; j += 2) {
+                const int stage = j % STAGES;
+                const uint32_t phase = (uint32_t)((j / STAGES) & 1);
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
+                const int kb = kb_lo + j;
                 const uint8_t* tile = smem + OFF_A + stage * A_BYTES + r * 128;
-                for (int b = b_first; b < b_first + b_count; ++b) {
+#pragma unroll 1
+                for (int b = 0; b < 2; ++b) {
                     float v[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -235,6 +236,10 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
             }
+            if constexpr (SPLIT) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qdone);
+            }
         }
     } else if (warp >= 12) {
         const int q = warp & 3;
@@ -247,17 +252,55 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
             tv[i] = -INFINITY;
             ti[i] = -1;
         }
-        const bool got = mbar_wait_bounded(tfull, 0, abort_flag, args.ws, deadline);
+        bool got = mbar_wait_bounded(tfull, 0, abort_flag, args.ws, deadline);
+        if (got) tc_fence_after();
+        const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+        if constexpr (SPLIT) {
+            // Each CTA holds partial logits over its half of K for every expert.
+            // Once this CTA's ring is idle (MMAs and quantisers done), the partner
+            // may write into it; this warp then sends its rows' partials of the
+            // partner's experts into the partner's ring and waits for the reverse.
+            if (got && QUANT) got = mbar_wait_bounded(qdone, 0, abort_flag, args.ws, deadline);
+            __syncwarp();
+            if (got && lane == 0) mbar_arrive_remote(pfree, peer);
+            if (got) got = mbar_wait_bounded_cluster(pfree, 0, abort_flag, args.ws, deadline);
+            if (got) {
+                for (int c = 0; c < EH / 16; ++c) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tq + peer * EH + 16 * c, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_cluster_v4(mapa_shared(smem_u32(xpart + ((4 * c + i) * BM + rl) * 4), peer),
+                                      r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(xdata, peer);
+                got = mbar_wait_bounded_cluster(xdata, 0, abort_flag, args.ws, deadline);
+            }
+        }
         if (got) {
-            tc_fence_after();
-            const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
-            for (int c = 0; c < E / 16; ++c) {
+            for (int c = 0; c < EH / 16; ++c) {
                 uint32_t r[16];
-                tmem_ld_32x32b_x16(tq + 16 * c, r);
+                tmem_ld_32x32b_x16(tq + e0 + 16 * c, r);
                 tmem_ld_wait();
                 float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + sbias[16 * c + i];
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                if constexpr (SPLIT) {
+                    // the two K halves add in the same order on both CTAs (FP32
+                    // addition commutes), so a logit does not depend on its owner
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 pp = *reinterpret_cast<const float4*>(xpart + ((4 * c + i) * BM + rl) * 4);
+                        v[4 * i] += pp.x;
+                        v[4 * i + 1] += pp.y;
+                        v[4 * i + 2] += pp.z;
+                        v[4 * i + 3] += pp.w;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += sbias[16 * c + i];
                 if (args.logits_out && row < args.N) {
                     float* dst = args.logits_out + (int64_t)row * args.E + e0 + 16 * c;
 #pragma unroll
@@ -274,20 +317,22 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
             if (half == 1) {
                 // hand this half's candidates to the first CTA of the pair (its
                 // shared memory, through the cluster), then tell it they are there
+                if (got) {
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) {
-                    const uint32_t av = mapa_shared(smem_u32(cand_v + rl * KMAX + j), 0);
-                    const uint32_t ai = mapa_shared(smem_u32(cand_i + rl * KMAX + j), 0);
-                    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(av), "r"(__float_as_uint(tv[j])) : "memory");
-                    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(ai), "r"(ti[j]) : "memory");
+                    for (int j = 0; j < KMAX; ++j) {
+                        const uint32_t av = mapa_shared(smem_u32(cand_v + rl * KMAX + j), 0);
+                        const uint32_t ai = mapa_shared(smem_u32(cand_i + rl * KMAX + j), 0);
+                        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(av), "r"(__float_as_uint(tv[j])) : "memory");
+                        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(ai), "r"(ti[j]) : "memory");
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(cand_bar, 0);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(cand_bar, 0);
                 write = false;
             } else {
                 // the other half's top-k joins after this half's: its experts have
                 // higher indices, so equal logits keep the lower index first
-                if (mbar_wait_bounded(cand_bar, 0, abort_flag, args.ws, deadline)) {
+                if (got && mbar_wait_bounded_cluster(cand_bar, 0, abort_flag, args.ws, deadline)) {
 #pragma unroll
                     for (int j = 0; j < KMAX; ++j)
                         topk_insert<KMAX>(tv, ti, cand_v[rl * KMAX + j], cand_i[rl * KMAX + j]);
@@ -321,6 +366,8 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // neither CTA of a pair leaves while the other may still write to its memory
+    if constexpr (SPLIT) cluster_sync();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
 }
@@ -332,7 +379,7 @@ bool route_tc_supported(int dtype, int H, int E, int k) {
 template <int KMAX, bool QUANT>
 static cudaError_t launch_route(const CUtensorMap& tx, const CUtensorMap& tw, const RouteArgs& a,
                                 int tiles, bool split, cudaStream_t st) {
-    const size_t smem = split ? rt::smem_bytes<true>(KMAX) : rt::smem_bytes<false>(KMAX);
+    const size_t smem = rt::smem_bytes(KMAX);
     if (!split) {
         auto kern = route_tc_kernel<KMAX, QUANT, false>;
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -363,10 +410,10 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
                                  uint8_t* xq, uint8_t* xq_sf, WsHeader* ws,
                                  unsigned long long timeout_ns, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
-    // two CTAs per token tile, each with half of the experts, when the halves are
-    // whole MMA widths of at least 32
-    const bool split = E >= 64 && E % 32 == 0;
-    const int EC = split ? E / 2 : E;          // experts per CTA
+    // two CTAs per token tile, each with half of K, when there are two K-stages
+    // and the experts' halves (whose top-k each CTA takes) are whole 16-column
+    // tensor-memory loads of at least 32
+    const bool split = E >= 64 && E % 32 == 0 && H >= 128;
     CUtensorMap tx, tw;
     {
         uint64_t dims[2] = {(uint64_t)H, (uint64_t)N};
@@ -375,7 +422,7 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
         if (!encode_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, str, box))
             return cudaErrorInvalidValue;
         uint64_t dw[2] = {(uint64_t)H, (uint64_t)E};
-        uint32_t bw[2] = {64, (uint32_t)EC};
+        uint32_t bw[2] = {64, (uint32_t)E};
         if (!encode_tmap(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dw, str, bw))
             return cudaErrorInvalidValue;
     }
@@ -393,7 +440,7 @@ cudaError_t launch_route_topk_tc(const void* x, const void* w, const float* bias
     a.ws = ws;
     a.timeout_ns = timeout_ns;
     uint32_t cols = 32;
-    while (cols < (uint32_t)EC) cols <<= 1;
+    while (cols < (uint32_t)E) cols <<= 1;
     a.tmem_cols = cols;
     const int tiles = (N + rt::BM - 1) / rt::BM;
     const bool quant = xq != nullptr;
