@@ -66,6 +66,10 @@ ROUTE_CASES = [
     synth.WORKLOADS["small_bf16"],
     synth.Workload("route_skew", N=1024, H=512, I=128, E=64, k=8, S=4, dtype="bf16", skew=3.0),
     synth.Workload("route_e256", N=640, H=256, I=128, E=256, k=8, S=5, dtype="mxfp8"),
+    # 48-expert halves of the pair's partial logits (three 16-column loads each),
+    # ragged last token tile
+    synth.Workload("route_e96", N=257, H=512, I=128, E=96, k=6, S=1, dtype="mxfp8"),
+    synth.Workload("route_e64_bf16", N=300, H=256, I=128, E=64, k=4, S=3, dtype="bf16"),
 ]
 
 
@@ -91,7 +95,8 @@ def test_route_topk(M, w):
     assert check_routing(g_idx, r_idx, ref, O.topk_gap(ref, w.k)) > 0.98
 
 
-@pytest.mark.parametrize("N,H,E,k", [(640, 512, 256, 8), (200, 1024, 32, 4), (8192, 7168, 256, 8)])
+@pytest.mark.parametrize("N,H,E,k", [(640, 512, 256, 8), (200, 1024, 32, 4), (8192, 7168, 256, 8),
+                                     (257, 512, 96, 6)])
 def test_route_topk_fused_x_quantisation_bit_exact(M, N, H, E, k):
     """The MXFP8 copy of x written by the router pass equals the oracle's quantiser."""
     w = synth.Workload("route_xq", N=N, H=H, I=128, E=E, k=k, S=N // 8 if N % 8 == 0 else 1,
