@@ -205,7 +205,10 @@ int moe_pack_expert_weights(const moe_shape_t* shape, const void* w_gate_up,
  *   xq_codes, xq_scales : for MOE_MXFP8, [N][H] and [N][H/32] MXFP8 copy of x
  *                (the dispatch operand), or NULL to skip
  * Logits accumulate in FP32 (BF16 products on tensor cores when E%16==0,
- * E<=256 and H%64==0; FP32 SIMT otherwise). */
+ * E<=256 and H%64==0; FP32 SIMT otherwise).  With E>=64 and E%32==0 the two
+ * halves of H accumulate separately and their FP32 sums are added once, so a
+ * logit may differ in its last bits from a single running sum; idx and gate are
+ * always the selection on the returned logits. */
 int moe_route_topk(const void* x, const void* w_router, const float* bias,
                    const moe_shape_t* shape, int32_t* idx, float* gate, float* logits_out,
                    uint8_t* xq_codes, uint8_t* xq_scales,
