@@ -405,6 +405,13 @@ def round_along_slots(m: np.ndarray, fmt: str) -> np.ndarray:
     return np.ascontiguousarray(mxfp8_values(np.ascontiguousarray(mp.T)).T[:R])
 
 
+def round_dgrad_operand(m: np.ndarray, fmt: str) -> np.ndarray:
+    """A dgrad GEMM's token-side operand m [slots, K] in its storage format: each
+    slot row on its own, MXFP8 blocks of 32 consecutive elements along K, the
+    GEMM's reduction axis (dy: K = H; du and dv: K = I)."""
+    return round_to(m, fmt)
+
+
 def expert_operands_dgrad(w_gate_up_e, w_down_e, dtype: str):
     """FP64 values of one expert's weights as the dgrad GEMMs see them: (Wg [I,H],
     Wu [I,H], Wd [H,I]) with the reduction running over I (gate/up) and over H
@@ -428,8 +435,9 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
       dh = round_dh(dy_b Wd_b),  (du, dv) = swiglu_backward(u_s, v_s, dh),
       da = round_da(du_b Wg_b + dv_b Wu_b),
       dWg = du^T a,  dWu = dv^T a,  dWd = dy^T h   (h after its rounding),
-    where _b marks a dgrad GEMM operand in its storage format (BWD_FORMATS; the
-    weights ``wb`` = expert_operands_dgrad, default the forward's values) and
+    where _b marks a dgrad GEMM operand in its storage format (BWD_FORMATS, each
+    slot row quantised along K by round_dgrad_operand; the weights ``wb`` =
+    expert_operands_dgrad, default the forward's values) and
     u_s, v_s the kept pre-activations.  With a wgrad format (WGRAD_FORMATS) the
     weight gradients are GEMMs over the slots too, each operand rounded along the
     slots (round_along_slots) and the result rounded to BF16:
@@ -447,9 +455,10 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     h = round_to(swiglu(u, v), fmt_h)
     y = round_to(h @ wd.T, fmt_y)
     u_s, v_s = round_to(u, f_uv), round_to(v, f_uv)
-    dh = round_to(round_to(dy, f_dy) @ wd_b, f_dh)
+    dh = round_to(round_dgrad_operand(dy, f_dy) @ wd_b, f_dh)
     du, dv = swiglu_backward(u_s, v_s, dh)
-    da = round_to(round_to(du, f_duv) @ wg_b + round_to(dv, f_duv) @ wu_b, f_da)
+    da = round_to(round_dgrad_operand(du, f_duv) @ wg_b + round_dgrad_operand(dv, f_duv) @ wu_b,
+                  f_da)
     if WGRAD_FORMATS[dtype] is None:
         dwg, dwu, dwd = du.T @ a, dv.T @ a, dy.T @ h
     else:

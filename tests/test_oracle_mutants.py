@@ -8,6 +8,7 @@ import pytest
 
 import oracle as O
 import test_oracle_backward as B
+import test_oracle_backward_axes as X
 import test_oracle_formats as F
 import test_oracle_layer as L
 import test_oracle_nvfp4 as N
@@ -134,6 +135,49 @@ def _e2m1_ties_away(orig):
     return f
 
 
+def _dgrad_weights_along_forward_axis(orig):
+    def f(w_gate_up_e, w_down_e, dtype):
+        if dtype != "mxfp8":
+            return orig(w_gate_up_e, w_down_e, dtype)
+        return O.expert_operands(w_gate_up_e, w_down_e, dtype)     # along H and I
+    return f
+
+
+def _dgrad_operand_along_slots_for(K):
+    """Quantise the dgrad operand whose reduction length is K down the slots
+    instead of along K (the pins use K = 64 for dy and K = 32 for du, dv)."""
+    def mutant(orig):
+        def f(m, fmt):
+            if fmt == "mxfp8" and m.shape[1] == K:
+                return O.round_along_slots(m, fmt)
+            return orig(m, fmt)
+        return f
+    return mutant
+
+
+def _bwd_format(pos, fmt):
+    """Keep one dgrad operand of the MXFP8 layer in BF16 instead of MXFP8."""
+    def mutant(orig):
+        row = list(orig["mxfp8"])
+        row[pos] = fmt
+        return {**orig, "mxfp8": tuple(row)}
+    return mutant
+
+
+def _wgrad_operands_along_rows(orig):
+    return lambda m, fmt: O.round_to(m, fmt)
+
+
+def _wgrad_blocks_end_at_the_segment(orig):
+    def f(m, fmt):
+        if fmt != "mxfp8":
+            return orig(m, fmt)
+        pad = (-m.shape[0]) % 32          # the partial block first instead of last
+        mp = np.vstack([np.zeros((pad, m.shape[1])), m]) if pad else m
+        return np.ascontiguousarray(O.mxfp8_values(np.ascontiguousarray(mp.T)).T[pad:])
+    return f
+
+
 def _autograd_pin():
     B.test_matches_torch_autograd(16, 32, 24, 8, 2, True)
 
@@ -160,10 +204,31 @@ CASES = [
     ("quantize_nvfp4", _nvfp4_scale_without_tensor_scale,
      [lambda: N.test_nvfp4_reproduces_exactly_representable_blocks(5)]),
     ("e2m1_encode", _e2m1_ties_away, [N.test_e2m1_encode_is_round_to_nearest_even_with_saturation]),
+    ("expert_operands_dgrad", _dgrad_weights_along_forward_axis,
+     [X.test_dgrad_weights_are_quantised_down_their_reduction_axis]),
+    ("round_dgrad_operand", _dgrad_operand_along_slots_for(64),
+     [lambda: X.test_dgrad_dy_is_quantised_along_H_per_slot("random")]),
+    ("round_dgrad_operand", _dgrad_operand_along_slots_for(64),
+     [lambda: X.test_dgrad_dy_is_quantised_along_H_per_slot("hand")]),
+    ("round_dgrad_operand", _dgrad_operand_along_slots_for(32),
+     [lambda: X.test_dgrad_du_dv_are_quantised_along_I_per_slot("random")]),
+    ("round_dgrad_operand", _dgrad_operand_along_slots_for(32),
+     [lambda: X.test_dgrad_du_dv_are_quantised_along_I_per_slot("hand")]),
+    ("BWD_FORMATS", _bwd_format(0, "bf16"), [lambda: X.test_dgrad_dy_is_quantised_along_H_per_slot("hand")]),
+    ("BWD_FORMATS", _bwd_format(2, "bf16"),
+     [lambda: X.test_dgrad_du_dv_are_quantised_along_I_per_slot("hand")]),
+    ("round_along_slots", _wgrad_operands_along_rows,
+     [lambda: X.test_wgrad_operands_are_quantised_along_the_slots(64, "random")]),
+    ("round_along_slots", _wgrad_operands_along_rows,
+     [lambda: X.test_wgrad_operands_are_quantised_along_the_slots(64, "hand")]),
+    ("round_along_slots", _wgrad_blocks_end_at_the_segment,
+     [lambda: X.test_wgrad_operands_are_quantised_along_the_slots(40, "random"),
+      B.test_round_along_slots_blocks_start_at_the_segment]),
 ]
 
 
-@pytest.mark.parametrize("name,mutant,pins", CASES, ids=[c[1].__name__.strip("_") for c in CASES])
+@pytest.mark.parametrize("name,mutant,pins", CASES,
+                         ids=[f"{i}-{c[0]}-{c[1].__name__.strip('_')}" for i, c in enumerate(CASES)])
 def test_planted_mistake_is_caught(monkeypatch, name, mutant, pins):
     monkeypatch.setattr(O, name, mutant(getattr(O, name)))
     assert any(_fails(p) for p in pins), f"no pin caught the planted mistake in {name}"
