@@ -55,11 +55,57 @@ def job_rate(units_per_rank_step: float, steps: int, t_ms: float, world: int) ->
 
 # DRAM bytes (read + write) of one moe_expert_ffn call (its two grouped-GEMM
 # launches), from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the 32-expert DeepSeek-V3 stand-in (N=1024, same 256 slots per expert): GEMM1
-# 1.0400 + 0.0178 GB, GEMM2 0.5019 + 0.0980 GB.  The full layer has 8x the experts
-# and 8x the slots at the same load per expert, and both the weight and the
-# activation bytes grow in proportion, so a full call moves 8x that.
-FFN_TRAFFIC_BYTES = {"dsv3_mxfp8": 8 * (1.0400 + 0.0178 + 0.5019 + 0.0980) * 1e9}
+# of the 32-expert DeepSeek-V3 stand-in (N=1024, same 256 slots per expert).  The
+# full layer has 8x the experts and 8x the slots at the same load per expert, and
+# both the weight and the activation bytes grow in proportion, so a full call
+# moves 8x that.  Each entry names its capture and the hash of the GEMM sources it
+# was taken on (GEMM_SOURCES); a build whose sources hash differently reports no
+# traffic, since the counters no longer describe it.
+GEMM_SOURCES = ["token_dispatch_expert_top_gb300/csrc/gemm_roles.cuh",
+                "token_dispatch_expert_top_gb300/csrc/gemm_tc.cu",
+                "token_dispatch_expert_top_gb300/csrc/common.cuh",
+                "token_dispatch_expert_top_gb300/csrc/pack.cu"]
+FFN_TRAFFIC = {
+    "dsv3_mxfp8": {"bytes": 8 * (1.0400 + 0.0178 + 0.5019 + 0.0980) * 1e9,
+                   "capture": "profiles/expert_ffn_gemm_dsv3_e32.md", "sources": "50b5b8c190cf73ba"},
+}
+
+
+def gemm_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ffn_traffic(workload: str):
+    """(bytes per call or None, note) for the expert FFN's two GEMM launches."""
+    t = FFN_TRAFFIC.get(workload)
+    if t is None:
+        return None, "no capture for this workload"
+    cur = gemm_sources_hash()
+    if cur != t["sources"]:
+        return None, f"GEMM sources changed since {t['capture']} (sources {t['sources']}, now {cur})"
+    return t["bytes"], f"{t['capture']} (x8 from the 32-expert stand-in; sources {cur})"
+
+
+def tensor_peak_at(peaks: dict, peak_src: str, dtype: str, clocks: dict):
+    """The dense tensor peak for a kernel timed inside the bench's steps: the
+    measured burst BF16 GEMM rate (x the nominal FP8/BF16 ratio for MXFP8), scaled
+    by the median SM clock sampled during the timed region over the maximum SM clock
+    (the burst figure was taken at the maximum clock).  Returns (peak, note)."""
+    if dtype == "f32":
+        return None, "FP32 SIMT"
+    base = peaks["bf16_tflops"] * (FP8_PER_BF16 if dtype == "mxfp8" else 1.0)
+    what = f"{peak_src} burst BF16 {peaks['bf16_tflops']:g}" + (
+        f" x {FP8_PER_BF16:g} (nominal FP8/BF16)" if dtype == "mxfp8" else "")
+    sm, mx = (clocks or {}).get("sm_mhz"), (clocks or {}).get("sm_max_mhz")
+    if sm and mx:
+        f = min(1.0, sm / mx)
+        return base * f, f"{what} x median SM clock {sm:g} / max {mx:g} MHz"
+    return base, f"{what} (no clock samples: not scaled)"
 
 
 def load_peaks():
@@ -389,15 +435,9 @@ def gpu_arm(args, rank, world):
     combine_bytes = w.T * w.H * act + w.N * w.H * act + w.T * 8
     ffn_s = stage_ms["expert_ffn"] / 1e3
     ffn_tflops = ffn_flops / ffn_s / 1e12
-    if w.dtype == "mxfp8":
-        tensor_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
-        peak_note = f"MXFP8 = {peak_src} sustained BF16 x {FP8_PER_BF16:g} (nominal FP8/BF16)"
-    elif w.dtype == "bf16":
-        tensor_peak = peaks["bf16_tflops_sustained"]
-        peak_note = f"{peak_src} sustained BF16"
-    else:
-        tensor_peak = None
-        peak_note = "FP32 SIMT"
+    clocks = clk.summary()
+    tensor_peak, peak_note = tensor_peak_at(peaks, peak_src, w.dtype, clocks)
+    traffic, traffic_note = ffn_traffic(w.name)
     if args.fused:
         # the persistent kernel runs gather + FFN + combine; its time is the step minus
         # the router and layout launches that precede it (same kernels, timed above)
@@ -412,7 +452,8 @@ def gpu_arm(args, rank, world):
         "bound": "tensor", "achieved": round(ffn_tflops, 2),
         "peak": round(tensor_peak, 1) if tensor_peak else None, "unit": "TFLOP/s",
         "frac": round(ffn_tflops / tensor_peak, 4) if tensor_peak else None,
-        "traffic": (None if args.fused else FFN_TRAFFIC_BYTES.get(w.name)), "traffic_unit": "bytes",
+        "traffic": (None if args.fused else traffic), "traffic_unit": "bytes",
+        "traffic_source": "fused kernel: no capture" if args.fused else traffic_note,
         "peak_source": peak_note,
         "algorithmic": f"{ffn_flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
     }
@@ -441,10 +482,46 @@ def gpu_arm(args, rank, world):
         "nvfp4_quantize": nvfp4_quant_figures(M, layer.x, args.steps, hbm) if w.dtype != "f32" else None,
         "router": router_figures(st, args.steps, hbm),
         "gpu_launches": kernel_launches_per_step(w, args.fused) * args.steps * max(1, args.macrobatches),
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": e2e,
     }
+    if w.skew:
+        counts = np.bincount(st.idx.cpu().numpy().ravel(), minlength=w.E)
+        res["config"]["load_max_over_mean"] = round(float(counts.max() / counts.mean()), 2)
+        res["config"]["empty_experts"] = int((counts == 0).sum())
+    if args.ring_sweep:
+        res["ring_sweep"] = ring_sweep(M, layer, args)
     return res, layer
+
+
+def ring_sweep(M, layer, args) -> list:
+    """The persistent fused forward over ring sizes of 64, 256 and 1024 slots
+    (minibatch = half the ring) and 4, 8 and 16 gather CTAs, each timed with CUDA
+    events over --steps steps after 3 warm-up steps, and checked bit for bit
+    against the staged forward."""
+    sweep = [M.Params(ring, ring // 2, g, 0, 0, 0, 0) for ring in (64, 256, 1024) for g in (4, 8, 16)]
+    need = max([M.moe_workspace_bytes(layer.shape, p) for p in sweep] + [layer.ws.numel()])
+    if need > layer.ws.numel():                 # one workspace that fits every setting
+        layer.ws = torch.empty(need, dtype=torch.uint8, device=layer.out.device)
+        M.moe_workspace_init(layer.ws)
+    staged = layer.forward().clone()
+    rows = []
+    for p in sweep:
+        for _ in range(3):
+            layer.forward(fused=True, params=p)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            out = layer.forward(fused=True, params=p)
+        e1.record()
+        torch.cuda.synchronize()
+        st = layer.device_status()
+        rows.append({"ring_slots": p.ring_slots, "minibatch": p.minibatch, "gather_ctas": p.gather_ctas,
+                     "ms_per_step": round(e0.elapsed_time(e1) / args.steps, 4),
+                     "bitwise_equal_staged": bool(st == 0 and torch.equal(out, staged)),
+                     "status": M.status_name(st)})
+    return rows
 
 
 # ------------------------------------------------------------- training step
@@ -591,7 +668,8 @@ def train_arm(args, rank, world):
            "overlap": "none (copies and the step on one stream)"}
 
     peaks, peak_src = load_peaks()
-    tensor_peak = peaks["bf16_tflops_sustained"] * (FP8_PER_BF16 if w.dtype == "mxfp8" else 1)
+    clocks = clk.summary()
+    tensor_peak, peak_note = tensor_peak_at(peaks, peak_src, w.dtype, clocks)
     flops = w.ffn_flops                      # each of dgrad and wgrad: 6*H*I per slot
     dgrad_tf = flops / (stage_ms["expert_dgrad"] / 1e3) / 1e12
     wgrad_tf = flops / (stage_ms["expert_wgrad"] / 1e3) / 1e12
@@ -617,7 +695,7 @@ def train_arm(args, rank, world):
                        else "expert dgrad (two grouped GEMMs and the SwiGLU derivative)"),
             "bound": "tensor", "achieved": round(dom_tf, 2), "peak": round(tensor_peak, 1),
             "unit": "TFLOP/s", "frac": round(dom_tf / tensor_peak, 4), "traffic": None,
-            "peak_source": f"{peak_src} sustained BF16" + (f" x {FP8_PER_BF16:g}" if w.dtype == "mxfp8" else ""),
+            "peak_source": peak_note,
             "algorithmic": f"{flops / 1e12:.3f} TFLOP per call (6*H*I per slot x {w.T} slots)",
         }
     counts = np.bincount(layer.saved["idx"].cpu().numpy().ravel(), minlength=w.E)
@@ -638,29 +716,53 @@ def train_arm(args, rank, world):
         "wgrad_tflops": round(wgrad_tf, 2),
         "roofline": roofline,
         "gpu_launches": train_launches_per_step(w) * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": e2e,
     }
     return res, layer
 
 
 # ------------------------------------------------------------- the oracle (CPU)
-def oracle_sample(w, inp, n_tokens: int, seed: int):
-    """One bounded sample of the layer on the oracle: routing and layout of all N
-    tokens, expert FFN and combine for n_tokens sampled tokens.  Returns seconds."""
+def oracle_layer_estimate(w, inp, n_experts: int, seed: int):
+    """One bounded sample of the forward layer on the oracle, scaled to the whole
+    layer.  Timed parts: the router, top-k and layout of all N tokens; the dispatch
+    and expert FFN of every slot of n_experts experts drawn at random among those
+    with slots (each quantising its own weights, as the layer does once per call);
+    the combine and output rounding of min(256, N) tokens.  Returns (estimated
+    seconds for the whole layer = route/layout + (experts with slots / n_experts) x
+    the sampled experts' time + (N / combined tokens) x the combine time, wall
+    seconds spent)."""
     sys.path.insert(0, os.path.join(ROOT, "oracle"))
-    import numpy as np
     import oracle as O
 
-    toks = np.random.default_rng(seed).choice(w.N, size=n_tokens, replace=False)
-
-    def weights(e):
-        return O.expert_operands(inp["w_gate_up"][e].cpu(), inp["w_down"][e].cpu(), w.dtype)
-
+    rng = np.random.default_rng(seed)
     t0 = time.perf_counter()
-    O.forward({"x": inp["x"], "w_router": inp["w_router"], "bias": inp["bias"]}, w.E, w.k, w.S,
-              w.dtype, tokens=toks, weights=weights)
-    return time.perf_counter() - t0
+    x = O._f64(inp["x"])
+    logits = O.router_logits(x, inp["w_router"], inp["bias"])
+    idx, gate = O.route_topk(logits, w.k)
+    counts, offsets, sched, inv = O.layout(idx, w.E, w.S)
+    t_route = time.perf_counter() - t0
+    live = np.nonzero(counts)[0]
+    pick = rng.choice(live, size=min(n_experts, len(live)), replace=False)
+    t1 = time.perf_counter()
+    fmt_a = O.FORMATS[w.dtype][0]
+    for e in pick:
+        rows = sched[offsets[e]:offsets[e + 1]]
+        tok = rows[:, 0].astype(np.int64) * w.rows_per_shard + rows[:, 1]
+        a = x[tok]
+        if fmt_a == "mxfp8":
+            a = O.mxfp8_values(a)
+        wg, wu, wd = O.expert_operands(inp["w_gate_up"][int(e)].cpu(), inp["w_down"][int(e)].cpu(), w.dtype)
+        O.expert_ffn(a, wg, wu, wd, w.dtype)
+    t_exp = time.perf_counter() - t1
+    t2 = time.perf_counter()
+    nc = min(256, w.N)
+    y = rng.standard_normal((nc * w.k, w.H))
+    out = O.combine(y, np.arange(nc * w.k, dtype=np.int32).reshape(nc, w.k), gate[:nc])
+    O.round_to(out, O.FORMATS[w.dtype][3])
+    t_comb = time.perf_counter() - t2
+    est = t_route + t_exp * len(live) / len(pick) + t_comb * w.N / nc
+    return est, time.perf_counter() - t0
 
 
 def oracle_train_sample(w, inp, n_tokens: int, seed: int):
@@ -698,20 +800,23 @@ def reference_arm(args, rank, world):
     w = synth.WORKLOADS[args.workload]
     dev = "cuda" if (w.name in synth.DEVICE_DRAWN and torch.cuda.is_available()) else "cpu"
     inp = synth.make_inputs(w, device=dev)
-    n_tok = args.sample_tokens
-    times = []
+    n_exp = args.sample_experts
+    est, wall = [], []
     for i in range(args.warmup + args.steps):
-        dt = oracle_sample(w, inp, n_tok, seed=i)
+        e, t = oracle_layer_estimate(w, inp, n_exp, seed=i)
         if i >= args.warmup:
-            times.append(dt)
-    total = sum(times)
-    value = n_tok * args.steps / total
-    sample = (f"per step: routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
-              f"random tokens (FP64 oracle)")
+            est.append(e)
+            wall.append(t)
+    value = w.N * args.steps / sum(est)
+    nc = min(256, w.N)
+    sample = (f"per step: routing, top-k and layout of all {w.N} tokens, dispatch + expert FFN of "
+              f"every slot of {n_exp} random expert(s) with slots, combine of {nc} tokens (FP64 "
+              f"oracle); the layer time is extrapolated from them (experts with slots / {n_exp}, "
+              f"N / {nc}); {sum(wall):.1f} s of CPU wall time over {args.steps} steps")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(1e3 * total / args.steps, 2), "higher_is_better": True,
+        "ms_per_step": round(1e3 * sum(est) / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "N": w.N, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
                    "S": w.S, "skew": w.skew},
@@ -735,10 +840,16 @@ def main():
     ap.add_argument("--reverse-ring", action="store_true",
                     help="with --fused: minibatches walk the slots from the last one down")
     ap.add_argument("--sample-tokens", type=int, default=2,
-                    help="tokens per oracle sample (CPU baseline / reference arm)")
+                    help="tokens per oracle sample of the training step's CPU baseline")
+    ap.add_argument("--sample-experts", type=int, default=1,
+                    help="experts per oracle sample (reference arm; the forward's CPU baseline "
+                         "takes at least 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time the training step (forward_train + backward) instead of the forward")
+    ap.add_argument("--ring-sweep", action="store_true",
+                    help="also time the fused forward over rings of 64/256/1024 slots x 4/8/16 "
+                         "gather CTAs (added to the JSON line as ring_sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -769,11 +880,17 @@ def main():
                 dt = oracle_train_sample(w, inp, n_tok, seed=12345)
                 what = (f"forward and input-gradient backward of {n_tok} random tokens (routing and "
                         f"layout of all {w.N}), FP64 oracle, {dt:.1f} s")
+                value = n_tok / dt
             else:
-                dt = oracle_sample(w, inp, n_tok, seed=12345)
-                what = (f"routing+layout of all {w.N} tokens, expert FFN+combine of {n_tok} "
-                        f"random tokens, FP64 oracle, {dt:.1f} s")
-            res["cpu_baseline"] = {"value": round(n_tok / dt, 4), "unit": "tokens/s",
+                n_exp = max(16, args.sample_experts)
+                est, dt = oracle_layer_estimate(w, inp, n_exp, seed=12345)
+                what = (f"routing, top-k and layout of all {w.N} tokens, dispatch + expert FFN of "
+                        f"every slot of {n_exp} random experts with slots, combine of "
+                        f"{min(256, w.N)} tokens, "
+                        f"FP64 oracle, {dt:.1f} s; the whole layer extrapolated from them: "
+                        f"{est:.1f} s")
+                value = w.N / est
+            res["cpu_baseline"] = {"value": round(value, 4), "unit": "tokens/s",
                                    "cores": cpu_cores(), "kind": "oracle", "sample": what}
         print(json.dumps(res), flush=True)
     if world > 1:

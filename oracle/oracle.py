@@ -427,7 +427,8 @@ def expert_operands_dgrad(w_gate_up_e, w_down_e, dtype: str):
 
 
 def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray,
-                        dy: np.ndarray, dtype: str, wb=None, a_master=None) -> dict:
+                        dy: np.ndarray, dtype: str, wb=None, a_master=None,
+                        want_wgrad: bool = True) -> dict:
     """Backward of one expert's SwiGLU FFN over its rows a, given dy = dL/dy.
 
     Forward as ``expert_ffn``: u = a Wg^T, v = a Wu^T, h = round_h(silu(u) v),
@@ -445,7 +446,7 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     with du_s, dv_s the BF16 copies of du, dv, a_w the master rows a_master (x,
     unquantised), h_w = silu(u_s) v_s recomputed from the kept u|v, every one of
     them then rounded along the slots.  For "f64" nothing is rounded and this is
-    the exact derivative.
+    the exact derivative.  want_wgrad=False skips the weight gradients (None).
     Returns dict(u, v, h, y, dh, du, dv, da, dwg, dwu, dwd)."""
     _, fmt_h, fmt_y, _ = FORMATS[dtype]
     f_dy, f_uv, f_duv, f_da, f_dh = BWD_FORMATS[dtype]
@@ -459,7 +460,9 @@ def expert_ffn_backward(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.nd
     du, dv = swiglu_backward(u_s, v_s, dh)
     da = round_to(round_dgrad_operand(du, f_duv) @ wg_b + round_dgrad_operand(dv, f_duv) @ wu_b,
                   f_da)
-    if WGRAD_FORMATS[dtype] is None:
+    if not want_wgrad:
+        dwg = dwu = dwd = None
+    elif WGRAD_FORMATS[dtype] is None:
         dwg, dwu, dwd = du.T @ a, dv.T @ a, dy.T @ h
     else:
         dwg, dwu, dwd = expert_wgrad(a if a_master is None else a_master, round_bf16(du),
@@ -481,7 +484,7 @@ def expert_wgrad(a: np.ndarray, du: np.ndarray, dv: np.ndarray, dy: np.ndarray, 
 
 
 def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, experts=None,
-             weights=None) -> dict:
+             weights=None, router_experts=None) -> dict:
     """Gradients of the forward layer, L = sum(dout * out), on the oracle.
 
     The backward the pages describe for the layer ([MoK-2.37x] section 01: training
@@ -514,14 +517,19 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     dbias = sum_n dlogit.
 
     tokens:  optional token subset for dx and the per-pair outputs of those tokens.
-    experts: optional expert subset for dW_gate_up, dW_down, dW_r rows and dbias.
-    Without either, every output covers the whole layer.  The per-pair arrays cover
-    exactly the pairs listed in ``pairs`` (pair id = n*k + j), which are all pairs
-    of ``tokens``, of the tokens routed to ``experts`` (their dlogit needs every
-    choice's dgate) and every pair routed to ``experts``.
-    Returns dict(idx, gate, inv, counts, offsets, pairs, dy, dgate, dh, du, dv, da,
-    tokens, dx_ffn, dx_router, dx, dlogit, experts, dw_router, dbias, dw_gate_up,
-    dw_down).
+    experts: optional expert subset for dW_gate_up and dW_down.
+    router_experts: optional expert subset for the dW_r rows and dbias entries
+             (default: ``experts``).
+    Without them, every output covers the whole layer.  The per-pair arrays cover
+    the pairs listed in ``pairs`` (pair id = n*k + j): all pairs of ``tokens``, of
+    the tokens routed to ``router_experts`` (their dlogit needs every choice's
+    dgate) and every pair routed to ``experts``.  The FFN backward (dh, du, dv,
+    da) is taken for the pairs where ``full`` is set: those of ``tokens`` and
+    those routed to ``experts``; the other listed pairs only need the forward's y
+    for their dgate, and hold zeros in dh, du, dv and da.
+    Returns dict(idx, gate, inv, counts, offsets, pairs, full, dy, dgate, dh, du, dv,
+    da, tokens, dx_ffn, dx_router, dx, dlogit, experts, router_experts, dw_router,
+    dbias, dw_gate_up, dw_down).
     """
     fmt_a = FORMATS[dtype][0]
     x = _f64(inp["x"])
@@ -534,12 +542,16 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     pair_e = idx.ravel().astype(np.int64)
     toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
     exps = np.arange(E) if experts is None else np.asarray(experts, dtype=np.int64)
+    rexps = exps if router_experts is None else np.asarray(router_experts, dtype=np.int64)
 
-    # the tokens whose dlogit is needed, and every pair whose FFN gradient is needed
-    routed = np.isin(idx, exps).any(axis=1)
+    # the tokens whose dlogit is needed, the pairs whose FFN gradient is needed
+    # (full), and the pairs that only need y for their dgate
+    routed = np.isin(idx, rexps).any(axis=1)
     need_tok = np.union1d(toks, np.nonzero(routed)[0])
-    pairs = np.union1d((need_tok[:, None] * k + np.arange(k)[None, :]).ravel(),
-                       np.nonzero(np.isin(pair_e, exps))[0])
+    full_ids = np.union1d((toks[:, None] * k + np.arange(k)[None, :]).ravel(),
+                          np.nonzero(np.isin(pair_e, exps))[0])
+    pairs = np.union1d((need_tok[:, None] * k + np.arange(k)[None, :]).ravel(), full_ids)
+    full = np.isin(pairs, full_ids)
     pos = {int(p): i for i, p in enumerate(pairs)}
     ptok = pairs // k
     P = len(pairs)
@@ -558,12 +570,19 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     dwd = np.zeros((len(exps), H, I))
     exp_pos = {int(e): i for i, e in enumerate(exps)}
     for e in np.unique(pair_e[pairs]):
-        sel = np.nonzero(pair_e[pairs] == e)[0]
-        a = a_rows[sel]
+        on_e = pair_e[pairs] == e
         wg, wu, wd = weights(int(e)) if weights is not None else expert_operands(
             inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
+        fwd_only = np.nonzero(on_e & ~full)[0]
+        if len(fwd_only):
+            y_f = expert_ffn(a_rows[fwd_only], wg, wu, wd, dtype)
+            dgate_p[fwd_only] = np.einsum("ph,ph->p", dY[ptok[fwd_only]], y_f)
+        sel = np.nonzero(on_e & full)[0]
+        if not len(sel):
+            continue
         wb = expert_operands_dgrad(inp["w_gate_up"][int(e)], inp["w_down"][int(e)], dtype)
-        r = expert_ffn_backward(a, wg, wu, wd, dy[sel], dtype, wb, x[ptok[sel]])
+        r = expert_ffn_backward(a_rows[sel], wg, wu, wd, dy[sel], dtype, wb, x[ptok[sel]],
+                                want_wgrad=int(e) in exp_pos)
         dgate_p[sel] = np.einsum("ph,ph->p", dY[ptok[sel]], r["y"])
         dh[sel], du[sel], dv[sel], da[sel] = r["dh"], r["du"], r["dv"], r["da"]
         if int(e) in exp_pos:
@@ -589,10 +608,10 @@ def backward(inp: dict, E: int, k: int, S: int, dtype: str, dout, tokens=None, e
     rows = np.repeat(need_tok, k)
     dlogit[rows, idx[need_tok].ravel()] = dlsel.ravel()
     dx_router = dlogit[toks] @ wr
-    dw_router = dlogit[:, exps].T @ x
-    dbias = dlogit[:, exps].sum(axis=0)
+    dw_router = dlogit[:, rexps].T @ x
+    dbias = dlogit[:, rexps].sum(axis=0)
     return dict(idx=idx, gate=gate, inv=inv, counts=counts, offsets=offsets, pairs=pairs,
-                dy=dy, dgate=dgate_full, dh=dh, du=du, dv=dv, da=da, tokens=toks,
+                full=full, dy=dy, dgate=dgate_full, dh=dh, du=du, dv=dv, da=da, tokens=toks,
                 dx_ffn=dx_ffn, dx_router=dx_router, dx=round_to(dx_ffn + dx_router, f_dx),
-                dlogit=dlogit,
-                experts=exps, dw_router=dw_router, dbias=dbias, dw_gate_up=dwgu, dw_down=dwd)
+                dlogit=dlogit, experts=exps, router_experts=rexps, dw_router=dw_router,
+                dbias=dbias, dw_gate_up=dwgu, dw_down=dwd)

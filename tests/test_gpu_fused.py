@@ -115,3 +115,16 @@ def test_fused_reverse_ring_traversal_bitwise(w, ring, mb, g):
     fused = layer.forward(fused=True, params=_params(M, ring=ring, mb=mb, g=g, reverse=1))
     assert layer.device_status() == 0
     assert torch.equal(fused, staged), (ring, mb, g)
+
+
+@pytest.mark.parametrize("ring,mb,g", [(256, 128, 4), (0, 0, 0)], ids=["ring256", "default"])
+def test_fused_reverse_ring_matches_oracle(ring, mb, g):
+    """Reverse ring traversal against the oracle directly (every token)."""
+    w = SKEW_MX
+    M, MoeLayer, inp = _layers(w, None)
+    layer = MoeLayer(w, inp, params=_params(M, ring=ring, mb=mb, g=g))
+    out = to_np(layer.forward(fused=True, params=_params(M, ring=ring, mb=mb, g=g, reverse=1)))
+    assert layer.device_status() == 0
+    ref = O.forward(inp, w.E, w.k, w.S, w.dtype)
+    ok = ref["gap"] >= TIE_TAU
+    assert row_rel_err(out[ok], ref["out"][ok]).max() < TOL[w.dtype]

@@ -16,7 +16,7 @@ LAYER_CASES = [
     (synth.Workload("mid_mxfp8", N=512, H=512, I=256, E=16, k=4, S=4, dtype="mxfp8"), None),
     (synth.Workload("mid_mxfp8_skew", N=768, H=1024, I=384, E=32, k=6, S=8, dtype="mxfp8",
                     skew=3.0), None),
-    (synth.WORKLOADS["small_bf16"], 192),
+    (synth.WORKLOADS["small_bf16"], None),      # every token
 ]
 
 
@@ -112,6 +112,23 @@ def test_macrobatched_forward_is_bitwise_equal(w, macro):
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
     assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("w,macro", [(LAYER_CASES[3][0], 3), (LAYER_CASES[2][0], 4)],
+                         ids=["mid_mxfp8_skew-3", "mid_mxfp8-4"])
+def test_macrobatched_forward_matches_oracle(w, macro):
+    """The macrobatched forward against the oracle directly (every token)."""
+    need_cuda()
+    from token_dispatch_expert_top_gb300.layer import MoeLayer
+    inp = synth.make_inputs(w, device="cpu")
+    layer = MoeLayer(w, inp)
+    out = layer.forward_macrobatched(macro)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    ref = O.forward(inp, w.E, w.k, w.S, w.dtype)
+    ok = ref["gap"] >= TIE_TAU
+    err = row_rel_err(to_np(out)[ok], ref["out"][ok])
+    assert err.max() < TOL[w.dtype], (w.name, macro, err.max())
 
 
 def test_macrobatched_forward_rejects_uneven_split():

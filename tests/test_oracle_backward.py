@@ -259,9 +259,19 @@ def test_subsets_agree_with_the_full_backward():
     np.testing.assert_allclose(part["dw_down"], full["dw_down"][[2, 5]], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(part["dw_router"], full["dw_router"][[2, 5]], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(part["dbias"], full["dbias"][[2, 5]], rtol=1e-13, atol=1e-14)
+    assert part["full"].any() and not part["full"].all()
     for i, p in enumerate(part["pairs"]):
         j = int(np.nonzero(full["pairs"] == p)[0][0])
-        np.testing.assert_allclose(part["da"][i], full["da"][j], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(part["dgate"].ravel()[p], full["dgate"].ravel()[p], rtol=1e-13,
+                                   atol=1e-14)
+        if part["full"][i]:
+            np.testing.assert_allclose(part["da"][i], full["da"][j], rtol=1e-13, atol=1e-14)
+    # the router rows of one set of experts and the weight gradients of another
+    r = O.backward(inp, 6, 2, 3, "bf16", dout, tokens=[4], experts=[1], router_experts=[0, 3])
+    np.testing.assert_allclose(r["dw_router"], full["dw_router"][[0, 3]], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["dbias"], full["dbias"][[0, 3]], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["dw_gate_up"], full["dw_gate_up"][[1]], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["dx"], full["dx"][[4]], rtol=1e-13, atol=1e-14)
 
 
 def test_round_along_slots_blocks_start_at_the_segment():

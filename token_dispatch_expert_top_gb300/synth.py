@@ -68,6 +68,12 @@ WORKLOADS = {
     # Same shapes with a Zipf-like router bias b_e = 3*log(1/rank_e).
     "dsv3_mxfp8_skew": Workload("dsv3_mxfp8_skew", N=8192, H=7168, I=2048, E=256, k=8, S=64,
                                 dtype="mxfp8", skew=3.0),
+    # The same layer at the mid skew the skewed configuration describes (hottest
+    # expert about 18x the mean, a long tail of small experts, none empty): the
+    # bias coefficient 0.5 instead of 3, which saturates (8 experts take every
+    # token, 225 are empty).
+    "dsv3_mxfp8_skew05": Workload("dsv3_mxfp8_skew05", N=8192, H=7168, I=2048, E=256, k=8, S=64,
+                                  dtype="mxfp8", skew=0.5),
     # Profiling stand-in: DeepSeek-V3 shapes and per-expert load (T/E = 256 rows),
     # 32 experts, so a capture holds ~1.4 GB of weights instead of 11.6 GB.
     "dsv3_mxfp8_e32": Workload("dsv3_mxfp8_e32", N=1024, H=7168, I=2048, E=32, k=8, S=8,
@@ -87,8 +93,8 @@ WORKLOADS = {
 }
 
 # Workloads whose tensors are drawn on the device generator (too large for the host).
-DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_e32", "dsv3_router_prof",
-                "dsv3_mxfp8_skew_16k", "dsv3_mxfp8_hot8"}
+DEVICE_DRAWN = {"dsv3_mxfp8", "dsv3_mxfp8_skew", "dsv3_mxfp8_skew05", "dsv3_mxfp8_e32",
+                "dsv3_router_prof", "dsv3_mxfp8_skew_16k", "dsv3_mxfp8_hot8"}
 
 
 def master_dtype(w: Workload) -> torch.dtype:
