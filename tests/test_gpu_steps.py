@@ -311,6 +311,11 @@ FFN_CASES = [
     ("bf16", 2048, 1408, [200, 0, 383, 129, 257, 1, 640, 128]),
     ("mxfp8", 2048, 1408, [200, 0, 383, 129, 257, 1, 640, 128]),
     ("mxfp8", 7168, 2048, [37, 0, 256, 129]),
+    # ragged last m-tiles of every size class: 1, 31, 32 (a 32-row A box), 33 and more
+    # (the 128-row box), full tiles, empty experts
+    ("mxfp8", 512, 256, [160, 161, 288, 289, 129, 32, 31, 0, 1, 401, 128, 256]),
+    ("bf16", 512, 256, [160, 161, 288, 289, 129, 32, 31, 0, 1, 401, 128, 256]),
+    ("mxfp8", 7168, 2048, [160, 272, 257, 33]),
 ]
 
 
@@ -352,3 +357,4 @@ def test_expert_ffn_matches_oracle(M, dtype, H, I, counts):
         ref = O.expert_ffn(a64[lo:hi], wg, wu, wdd, dtype)
         err = row_rel_err(got[lo:hi], ref)
         assert err.max() < TOL[dtype], (e, err.max())
+
