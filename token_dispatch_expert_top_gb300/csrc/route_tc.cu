@@ -10,9 +10,12 @@
 //
 // CTA = 16 warps:  w0 TMA producer (4-stage ring), w1 MMA issuer + TMEM owner,
 //                  w2-3 idle,
-//                  w4-11 x quantisers (MXFP8 only; two groups of four warps, one
-//                  token row per thread, each group every other K-stage),
-//                  w12-15 top-k epilogue.
+//                  w4-11 x quantisers (MXFP8 only; every K-stage, one 32-element
+//                  block of one token row per thread),
+//                  then all 16 warps: the top-k epilogue.  Warp w reads the logits of
+//                  token rows 32(w%4)..+31 (its tensor-memory lane quarter) over one
+//                  of up to four column ranges (w/4), keeps their top-k, and the
+//                  first warp of each quarter merges the four sorted lists.
 // Split mode (E >= 64, E % 32 == 0, H >= 128): a cluster of two CTAs shares a
 // 128-token tile, each taking half of K for every expert (twice the CTAs; each x
 // byte crosses from L2 once) and quantising its half of x.  The partial logits
@@ -39,11 +42,15 @@ constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, tfull, cand, qdone, pfree, xdata
+constexpr int WARPS = THREADS / 32;
+constexpr int MAX_SUB = 4;                   // column ranges of the epilogue's top-k
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;   // tmem base, abort flag
 constexpr int OFF_BIAS = OFF_MISC + 16;
 constexpr int OFF_CAND = OFF_BIAS + 256 * 4;       // split mode: partner's candidates
 inline size_t smem_bytes(int kmax) { return 1024 + OFF_CAND + (size_t)kmax * BM * 8; }
 static_assert(STAGES * A_BYTES >= BM * 128 * 4, "the x ring holds 128 partial logits per token");
+static_assert(STAGES * B_BYTES >= BM * MAX_SUB * 32 * 8, "the weight ring holds every sub-list (k <= 32)");
+static_assert(BM * 8 * 8 >= QUANT_WARPS * 32 * 4, "the candidate area holds the quantisers' scratch words");
 }  // namespace rt
 
 struct RouteArgs {
@@ -61,22 +68,24 @@ struct RouteArgs {
 
 // Keep the KMAX largest (value, index) pairs, sorted by descending value; equal
 // values keep the earlier (lower) index first because a newcomer only moves up
-// past strictly smaller values.
+// past strictly smaller values.  The comparisons against the old list are
+// independent of each other: entries from the newcomer's position on shift down
+// by one in a single pass of selects, with no chain of compare-and-swap steps.
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(float (&tv)[KMAX], int (&ti)[KMAX], float v, int e) {
-    if (!(v > tv[KMAX - 1])) return;
-    tv[KMAX - 1] = v;
-    ti[KMAX - 1] = e;
+    bool gt[KMAX];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) gt[i] = v > tv[i];      // true from the insertion point on
 #pragma unroll
     for (int i = KMAX - 1; i > 0; --i) {
-        if (tv[i] > tv[i - 1]) {
-            const float fv = tv[i];
-            tv[i] = tv[i - 1];
-            tv[i - 1] = fv;
-            const int fi = ti[i];
-            ti[i] = ti[i - 1];
-            ti[i - 1] = fi;
-        }
+        const float nv = gt[i - 1] ? tv[i - 1] : v;
+        const int ni = gt[i - 1] ? ti[i - 1] : e;
+        tv[i] = gt[i] ? nv : tv[i];
+        ti[i] = gt[i] ? ni : ti[i];
+    }
+    if (gt[0]) {
+        tv[0] = v;
+        ti[0] = e;
     }
 }
 
@@ -103,6 +112,9 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     float* xpart = reinterpret_cast<float*>(smem + OFF_A);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     float* sbias = reinterpret_cast<float*>(smem + OFF_BIAS);
+    // the quantisers' scratch words: the candidate area, which the partner fills
+    // only after every warp of this CTA has left its main-loop role
+    volatile uint32_t* sdep = reinterpret_cast<volatile uint32_t*>(smem + OFF_CAND);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int half = SPLIT ? (int)cluster_ctarank() : 0;      // which half of K, and of the experts' top-k
@@ -119,14 +131,14 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            // MMA + the group of four quantiser warps that takes the stage
-            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS / 2 : 1);
+            // MMA + every quantiser warp
+            mbar_init(&empty[s], QUANT ? 1 + QUANT_WARPS : 1);
         }
         mbar_init(tfull, 1);
-        mbar_init(cand_bar, 4);                               // the partner's four epilogue warps
+        mbar_init(cand_bar, 4);                               // the partner's four merging warps
         mbar_init(qdone, QUANT_WARPS);
-        mbar_init(pfree, 4);                                  // the partner's four epilogue warps
-        mbar_init(xdata, 4);                                  // the partner's four epilogue warps
+        mbar_init(pfree, WARPS);                              // every warp of the partner
+        mbar_init(xdata, WARPS);                              // every warp of the partner
         *abort_flag = 0;
         if (SPLIT)
             fence_mbar_init_cluster();
@@ -139,8 +151,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         tmem_alloc(tmem_slot, args.tmem_cols);
         tmem_relinquish();
     }
-    if (warp >= 12)
-        for (int e = threadIdx.x - 384; e < EH; e += 128) sbias[e] = args.bias ? args.bias[e0 + e] : 0.f;
+    for (int e = threadIdx.x; e < EH; e += THREADS) sbias[e] = args.bias ? args.bias[e0 + e] : 0.f;
     tc_fence_before();
     __syncthreads();
     if constexpr (SPLIT) cluster_sync();   // the partner's barriers exist before any arrival
@@ -191,60 +202,76 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         }
     } else if (warp >= 4 && warp < 12) {
         if constexpr (QUANT) {
-            // Thread = (token row r, group g).  Group g takes this CTA's K-stages of
-            // parity g (always ring stages g and g + 2), both 32-element blocks of
-            // row r.  Each warp waits on the fills of its stages in order, one
-            // phase at a time: a warp that skipped a fill of a stage could take
-            // that fill's completed phase for the next one (the wait tests only
-            // parity).
+            // Thread = (token row r, 32-element block b of the stage's 64).  Every
+            // quantiser warp takes every K-stage in order, so the stage is released
+            // once each thread has converted one block.
             const int tq = (warp - 4) * 32 + lane;
             const int r = tq & (BM - 1);
-            const int grp = tq >> 7;
+            const int b = tq >> 7;
             const int row = row0 + r;
-            for (int j = grp; j < nkb; j += 2) {
-                const int stage = j % STAGES;
-                const uint32_t phase = (uint32_t)((j / STAGES) & 1);
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int j = 0; j < nkb; ++j) {
                 if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.ws, deadline)) break;
                 const int kb = kb_lo + j;
                 const uint8_t* tile = smem + OFF_A + stage * A_BYTES + r * 128;
-#pragma unroll 1
-                for (int b = 0; b < 2; ++b) {
-                    float v[32];
+                uint4 qv[4];
+                uint32_t dep = 0;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        // 128-byte swizzle: 16-byte chunk cc of row r sits at chunk cc ^ (r % 8)
-                        const int cc = 4 * b + c;
-                        const uint4 q = *reinterpret_cast<const uint4*>(tile + ((cc ^ (r & 7)) << 4));
-                        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            v[8 * c + 2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
-                            v[8 * c + 2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
-                        }
-                    }
-                    uint32_t cb[8];
-                    const uint8_t sc = mx_quantize32(v, cb);
-                    if (row < args.N) {   // one full 32-byte sector of codes and the block's scale
-                        st_v8(args.xq + (int64_t)row * args.H + kb * 64 + b * 32, cb);
-                        args.xq_sf[(int64_t)row * (args.H / 32) + kb * 2 + b] = sc;
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    // 128-byte swizzle: 16-byte chunk cc of row r sits at chunk cc ^ (r % 8)
+                    const int cc = 4 * b + c;
+                    qv[c] = *reinterpret_cast<const uint4*>(tile + ((cc ^ (r & 7)) << 4));
+                    dep ^= qv[c].x ^ qv[c].y ^ qv[c].z ^ qv[c].w;
                 }
-                // Release the stage only after every lane has consumed what it read:
-                // the stores above use all of it, and the proxy fence orders these
-                // generic-proxy reads before the next TMA (async-proxy) refill.
+                // Release the stage as soon as every lane holds its words: a store of
+                // `dep` (which needs every loaded word) into this thread's scratch word
+                // cannot be performed before the reads have returned, and the proxy
+                // fence orders it, and the reads, before the next TMA (async-proxy)
+                // refill.  The conversion and the global stores then run off the
+                // ring's path.
+                sdep[tq] = dep;
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
+                float v[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t w[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        v[8 * c + 2 * p] = bf16_to_f32((uint16_t)(w[p] & 0xFFFF));
+                        v[8 * c + 2 * p + 1] = bf16_to_f32((uint16_t)(w[p] >> 16));
+                    }
+                }
+                uint32_t cb[8];
+                const uint8_t sc = mx_quantize32(v, cb);
+                if (row < args.N) {   // one full 32-byte sector of codes and the block's scale
+                    st_v8(args.xq + (int64_t)row * args.H + kb * 64 + b * 32, cb);
+                    args.xq_sf[(int64_t)row * (args.H / 32) + kb * 2 + b] = sc;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
             }
             if constexpr (SPLIT) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qdone);
             }
         }
-    } else if (warp >= 12) {
+    }
+
+    // ------------------------------------------------------------ epilogue (all warps)
+    __syncwarp();
+    {
         const int q = warp & 3;
+        const int sub = warp >> 2;
         const int rl = 32 * q + lane;             // token row within the tile
         const int row = row0 + rl;
+        const int nsub = EH % 64 == 0 ? 4 : (EH % 32 == 0 ? 2 : 1);   // column ranges, 16-column multiples
+        const int per = EH / nsub;
+        const bool active = sub < nsub;
         float tv[KMAX];
         int ti[KMAX];
 #pragma unroll
@@ -258,31 +285,34 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
         if constexpr (SPLIT) {
             // Each CTA holds partial logits over its half of K for every expert.
             // Once this CTA's ring is idle (MMAs and quantisers done), the partner
-            // may write into it; this warp then sends its rows' partials of the
-            // partner's experts into the partner's ring and waits for the reverse.
+            // may write into it; every warp then sends its rows' partials of its
+            // column range of the partner's experts into the partner's ring and
+            // waits for the reverse.
             if (got && QUANT) got = mbar_wait_bounded(qdone, 0, abort_flag, args.ws, deadline);
             __syncwarp();
             if (got && lane == 0) mbar_arrive_remote(pfree, peer);
             if (got) got = mbar_wait_bounded_cluster(pfree, 0, abort_flag, args.ws, deadline);
-            if (got) {
-                for (int c = 0; c < EH / 16; ++c) {
+            if (got && active) {
+                for (int c = 0; c < per / 16; ++c) {
+                    const int col = sub * per + 16 * c;
                     uint32_t r[16];
-                    tmem_ld_32x32b_x16(tq + peer * EH + 16 * c, r);
+                    tmem_ld_32x32b_x16(tq + peer * EH + col, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        st_cluster_v4(mapa_shared(smem_u32(xpart + ((4 * c + i) * BM + rl) * 4), peer),
+                        st_cluster_v4(mapa_shared(smem_u32(xpart + ((col / 4 + i) * BM + rl) * 4), peer),
                                       r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(xdata, peer);
-                got = mbar_wait_bounded_cluster(xdata, 0, abort_flag, args.ws, deadline);
             }
+            __syncwarp();
+            if (got && lane == 0) mbar_arrive_remote(xdata, peer);
+            if (got) got = mbar_wait_bounded_cluster(xdata, 0, abort_flag, args.ws, deadline);
         }
-        if (got) {
-            for (int c = 0; c < EH / 16; ++c) {
+        if (got && active) {
+            for (int c = 0; c < per / 16; ++c) {
+                const int col = sub * per + 16 * c;
                 uint32_t r[16];
-                tmem_ld_32x32b_x16(tq + e0 + 16 * c, r);
+                tmem_ld_32x32b_x16(tq + e0 + col, r);
                 tmem_ld_wait();
                 float v[16];
 #pragma unroll
@@ -292,7 +322,7 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                     // addition commutes), so a logit does not depend on its owner
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float4 pp = *reinterpret_cast<const float4*>(xpart + ((4 * c + i) * BM + rl) * 4);
+                        const float4 pp = *reinterpret_cast<const float4*>(xpart + ((col / 4 + i) * BM + rl) * 4);
                         v[4 * i] += pp.x;
                         v[4 * i + 1] += pp.y;
                         v[4 * i + 2] += pp.z;
@@ -300,60 +330,100 @@ __global__ void __launch_bounds__(rt::THREADS, 1)
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] += sbias[16 * c + i];
+                for (int i = 0; i < 16; ++i) v[i] += sbias[col + i];
                 if (args.logits_out && row < args.N) {
-                    float* dst = args.logits_out + (int64_t)row * args.E + e0 + 16 * c;
+                    float* dst = args.logits_out + (int64_t)row * args.E + e0 + col;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         st_v4(dst + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
                                                       __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) topk_insert<KMAX>(tv, ti, v[i], e0 + 16 * c + i);
+                for (int i = 0; i < 16; ++i) topk_insert<KMAX>(tv, ti, v[i], e0 + col + i);
             }
         }
-        bool write = row < args.N;
-        if constexpr (SPLIT) {
-            if (half == 1) {
-                // hand this half's candidates to the first CTA of the pair (its
-                // shared memory, through the cluster), then tell it they are there
-                if (got) {
+        // Publish each column range's sorted list in the idle weight ring, then the
+        // quarter's first warp merges them: repeatedly the largest head, the lower
+        // expert index first on equal logits -- the order topk_insert keeps -- so
+        // the result is the top-k of all this CTA's experts.
+        float* lv = reinterpret_cast<float*>(smem + OFF_B);                       // [BM][MAX_SUB][KMAX]
+        int* li = reinterpret_cast<int*>(smem + OFF_B + BM * MAX_SUB * KMAX * 4);
+        if (got && active) {
 #pragma unroll
-                    for (int j = 0; j < KMAX; ++j) {
-                        const uint32_t av = mapa_shared(smem_u32(cand_v + rl * KMAX + j), 0);
-                        const uint32_t ai = mapa_shared(smem_u32(cand_i + rl * KMAX + j), 0);
-                        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(av), "r"(__float_as_uint(tv[j])) : "memory");
-                        asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(ai), "r"(ti[j]) : "memory");
+            for (int j = 0; j < KMAX; ++j) {
+                lv[(rl * MAX_SUB + sub) * KMAX + j] = tv[j];
+                li[(rl * MAX_SUB + sub) * KMAX + j] = ti[j];
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(128) : "memory");    // the 4 warps of quarter q
+        if (sub == 0) {
+            if (got) {
+                int head[MAX_SUB] = {0, 0, 0, 0};
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    int best = -1, bi = 0;
+                    float bv = 0.f;
+#pragma unroll
+                    for (int u = 0; u < MAX_SUB; ++u) {
+                        if (u >= nsub || head[u] >= KMAX) continue;
+                        const float v = lv[(rl * MAX_SUB + u) * KMAX + head[u]];
+                        const int i = li[(rl * MAX_SUB + u) * KMAX + head[u]];
+                        if (best < 0 || v > bv || (v == bv && i < bi)) {
+                            best = u;
+                            bv = v;
+                            bi = i;
+                        }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(cand_bar, 0);
-                }
-                write = false;
-            } else {
-                // the other half's top-k joins after this half's: its experts have
-                // higher indices, so equal logits keep the lower index first
-                if (got && mbar_wait_bounded_cluster(cand_bar, 0, abort_flag, args.ws, deadline)) {
 #pragma unroll
-                    for (int j = 0; j < KMAX; ++j)
-                        topk_insert<KMAX>(tv, ti, cand_v[rl * KMAX + j], cand_i[rl * KMAX + j]);
-                } else {
+                    for (int u = 0; u < MAX_SUB; ++u) head[u] += best == u ? 1 : 0;
+                    tv[j] = bv;
+                    ti[j] = bi;
+                }
+            }
+            bool write = row < args.N;
+            if constexpr (SPLIT) {
+                if (half == 1) {
+                    // hand this half's candidates to the first CTA of the pair (its
+                    // shared memory, through the cluster), then tell it they are there
+                    if (got) {
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j) {
+                            const uint32_t av = mapa_shared(smem_u32(cand_v + rl * KMAX + j), 0);
+                            const uint32_t ai = mapa_shared(smem_u32(cand_i + rl * KMAX + j), 0);
+                            asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(av), "r"(__float_as_uint(tv[j]))
+                                         : "memory");
+                            asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(ai), "r"(ti[j]) : "memory");
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_remote(cand_bar, 0);
+                    }
                     write = false;
+                } else {
+                    // the other half's top-k joins after this half's: its experts have
+                    // higher indices, so equal logits keep the lower index first
+                    if (got && mbar_wait_bounded_cluster(cand_bar, 0, abort_flag, args.ws, deadline)) {
+#pragma unroll
+                        for (int j = 0; j < KMAX; ++j)
+                            topk_insert<KMAX>(tv, ti, cand_v[rl * KMAX + j], cand_i[rl * KMAX + j]);
+                    } else {
+                        write = false;
+                    }
                 }
             }
-        }
-        if (got && write) {
-            float z = 0.f;
-            float p[KMAX];
+            if (got && write) {
+                float z = 0.f;
+                float p[KMAX];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                p[j] = (j < args.k) ? expf(tv[j] - tv[0]) : 0.f;
-                z += p[j];
-            }
+                for (int j = 0; j < KMAX; ++j) {
+                    p[j] = (j < args.k) ? expf(tv[j] - tv[0]) : 0.f;
+                    z += p[j];
+                }
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (j < args.k) {
-                    args.idx[(int64_t)row * args.k + j] = ti[j];
-                    args.gate[(int64_t)row * args.k + j] = p[j] / z;
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < args.k) {
+                        args.idx[(int64_t)row * args.k + j] = ti[j];
+                        args.gate[(int64_t)row * args.k + j] = p[j] / z;
+                    }
                 }
             }
         }
