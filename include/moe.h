@@ -18,6 +18,9 @@
  *   - Every tensor pointer is a DEVICE pointer owned by the caller (typically a
  *     PyTorch allocation).  The library never allocates device memory; scratch
  *     space comes from a caller-owned workspace sized by moe_workspace_bytes().
+ *     One exception: moe_layout_noalloc's fixed 1 MiB scratch array, part of the
+ *     library's device image on every GPU that loads it, held from the library's
+ *     load until the process exits.
  *   - Shapes and parameters are passed in HOST structs and read during the call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call only enqueues work and returns; none synchronises the
@@ -319,14 +322,18 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
  * serving process that reserves all its device memory at start-up and allocates
  * nothing afterwards, or a plug-in whose host owns the allocator.  The pages
  * describe no such entry point; it exists for those callers only.
- *   Same arguments and results as moe_layout, minus the workspace.  Its scratch
+ *   Same arguments, shape checks and results as moe_layout, minus the workspace
+ *   (H, I and dtype are checked exactly as moe_layout checks them).  Its scratch
  *   (per-chunk expert counts and their scan) is a fixed 1 MiB __device__ array
  *   compiled into the library, resident on every GPU that loads it until the
  *   process exits.  Shapes with ceil(N*k/256) * E > 131072 are rejected with
  *   MOE_ERR_WORKSPACE before anything is launched.
  *   The first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress (that device must be current); make that first call
- *   before any stream capture begins.
+ *   before any stream capture begins.  The address is cached with the id of the
+ *   device's current context; after a device reset (or another teardown of the
+ *   context) the next call looks it up again, so that call, too, belongs
+ *   before any capture.
  *   Every call on a device uses that device's one copy of the array and leaves
  *   its contents behind: calls that overlap on the same GPU (for example on two
  *   streams) race.  Calls on different GPUs use different copies.

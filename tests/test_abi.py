@@ -123,3 +123,22 @@ def test_macrobatch_host_checks():
     # the reverse-ring flag sits at the end of moe_params_t; it leaves the workspace unchanged
     p = M.Params(0, 0, 0, 0, 0, 0, 1)
     assert M.moe_workspace_bytes(shape, p) == M.moe_workspace_bytes(shape, M.Params(0, 0, 0, 0, 0, 0, 0))
+
+
+def test_layout_noalloc_checks_shapes_as_layout_does():
+    """moe_layout_noalloc rejects exactly the shapes moe_layout rejects, with the
+    same status, before it touches the device."""
+    lib = M.lib()
+    bad = [
+        dict(N=64, H=100, I=128, E=8, k=2, S=2, dtype=1),     # H not a multiple of 32
+        dict(N=64, H=256, I=96, E=8, k=2, S=2, dtype=2),      # MXFP8: I not a multiple of 128
+        dict(N=64, H=256, I=128, E=8, k=2, S=2, dtype=7),     # no such dtype
+        dict(N=64, H=256, I=128, E=8, k=9, S=2, dtype=1),     # k > E
+        dict(N=63, H=256, I=128, E=8, k=2, S=2, dtype=1),     # N not a multiple of S
+        dict(N=64, H=256, I=128, E=2048, k=2, S=2, dtype=1),  # too many experts
+    ]
+    for d in bad:
+        shape = M.Shape(**d)
+        a = lib.moe_layout(None, ctypes.byref(shape), None, None, None, None, None, 0, None)
+        b = lib.moe_layout_noalloc(None, ctypes.byref(shape), None, None, None, None, None)
+        assert a == b != 0, (d, M.status_name(a), M.status_name(b))

@@ -259,6 +259,10 @@ int expert_ffn_impl(const void* a, const void* a_scales, int a_rows, const int32
 }
 
 }  // namespace
+
+// The shape checks every entry point runs first (the no-allocation layout's too).
+int validate_shape(const moe_shape_t* s) { return check_shape(s); }
+
 }  // namespace moe
 
 using namespace moe;

@@ -205,4 +205,8 @@ struct FfnMaps {
 struct GemmSide;
 bool encode_ffn_maps(const TcFfnCall& c, FfnMaps* m, GemmSide* s1, GemmSide* s2);
 
+// Shape validation shared by the entry points (api.cu): MOE_OK or the status to
+// return before anything is launched.
+int validate_shape(const moe_shape_t* s);
+
 }  // namespace moe

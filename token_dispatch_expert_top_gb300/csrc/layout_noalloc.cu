@@ -28,11 +28,45 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 // may be given it.
 static __device__ __align__(256) unsigned char g_layout_scratch[kNoAllocScratchBytes];
 
-// Device address of g_layout_scratch on the current device, looked up once per
-// device (with that device current) and cached.  Returns nullptr on failure.
+// Id of the calling thread's current CUDA context (unique for the life of the
+// process), or 0 when there is none or the driver query is unavailable.  The
+// driver entry points are fetched through the runtime, so the library does not
+// link libcuda.  Called with the cache's mutex held.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    }
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_layout_scratch on the current device, looked up with that
+// device current and cached with the id of the context it belongs to.  A device
+// reset (or any teardown of the context) reloads the library's device image, and
+// the array may then live elsewhere: when the current context's id differs from
+// the cached one, or cannot be read, the address is looked up again.  Returns
+// nullptr on failure.
 void* scratch_on_current_device(cudaError_t* err) {
     static std::mutex mu;
     static void* addr[256] = {};
+    static unsigned long long ctx[256] = {};
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return nullptr;
@@ -41,11 +75,13 @@ void* scratch_on_current_device(cudaError_t* err) {
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    const unsigned long long id = current_context_id();
+    if (!addr[dev] || id == 0 || id != ctx[dev]) {
         void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_layout_scratch);
+        *err = cudaGetSymbolAddress(&p, g_layout_scratch);   // makes the primary context current
         if (*err != cudaSuccess || p == nullptr) return nullptr;
         addr[dev] = p;
+        ctx[dev] = current_context_id();
     }
     return addr[dev];
 }
@@ -56,11 +92,9 @@ void* scratch_on_current_device(cudaError_t* err) {
 extern "C" int moe_layout_noalloc(const int32_t* idx, const moe_shape_t* shape, int32_t* counts,
                                   int32_t* offsets, int32_t* sched, int32_t* inv, void* stream) {
     using namespace moe;
-    if (!shape) return MOE_ERR_INVALID_ARG;
+    const int rc = validate_shape(shape);     // the same checks, and statuses, as moe_layout
+    if (rc != MOE_OK) return rc;
     const moe_shape_t& s = *shape;
-    if (s.N < 0 || s.E <= 0 || s.k <= 0 || s.S <= 0 || s.k > s.E || s.N % s.S != 0)
-        return MOE_ERR_INVALID_ARG;
-    if (s.k > 32 || s.E > 1024 || (int64_t)s.N * s.k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
     if (!counts || !offsets || (s.N > 0 && (!idx || !sched || !inv))) return MOE_ERR_INVALID_ARG;
     const int T = s.N * s.k;
     const size_t per_array = sizeof(int32_t) * (size_t)layout_chunks(T) * (size_t)s.E;
