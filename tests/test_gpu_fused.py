@@ -128,3 +128,20 @@ def test_fused_reverse_ring_matches_oracle(ring, mb, g):
     ref = O.forward(inp, w.E, w.k, w.S, w.dtype)
     ok = ref["gap"] >= TIE_TAU
     assert row_rel_err(out[ok], ref["out"][ok]).max() < TOL[w.dtype]
+
+
+@pytest.mark.parametrize("H", [256, 768], ids=["H256", "H768"])
+def test_fused_first_call_scale_rows_not_16_byte_multiples(H):
+    """MXFP8 scale rows of H/32 = 8 or 24 bytes: the fused kernel's own gather must
+    copy them whole.  The fused forward runs first on a fresh workspace, so no
+    earlier call has filled the ring, and is checked against the oracle, then
+    against the staged forward bit for bit."""
+    w = synth.Workload(f"fused_h{H}", N=256, H=H, I=256, E=16, k=4, S=4, dtype="mxfp8")
+    M, MoeLayer, inp = _layers(w, None)
+    layer = MoeLayer(w, inp)
+    fused = layer.forward(fused=True).clone()
+    assert layer.device_status() == 0
+    ref = O.forward(inp, w.E, w.k, w.S, w.dtype)
+    ok = ref["gap"] >= TIE_TAU
+    assert row_rel_err(to_np(fused)[ok], ref["out"][ok]).max() < TOL[w.dtype]
+    assert torch.equal(layer.forward(), fused)

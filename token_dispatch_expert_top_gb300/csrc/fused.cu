@@ -375,26 +375,27 @@ struct MinibatchTiles {
     }
 };
 
+// One slot's row (n16 16-byte words) and its MXFP8 scales (m8 8-byte words: a
+// scale row is H/32 bytes, a multiple of 8 but not always of 16), by one warp.
 __device__ __forceinline__ void copy_slot_row(uint8_t* __restrict__ dst, const uint8_t* __restrict__ src,
                                               int n16, uint8_t* __restrict__ dst2,
-                                              const uint8_t* __restrict__ src2, int m16, int lane) {
+                                              const uint8_t* __restrict__ src2, int m8, int lane) {
     constexpr int U = 16;
-    for (int b = 0; b < n16 || b < m16; b += 32 * U) {
-        uint4 v[U], w;
+    for (int b = 0; b < n16; b += 32 * U) {
+        uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = b + lane + 32 * u;
             if (j < n16) v[u] = ld_nc_v4(src + 16 * (int64_t)j);
         }
-        const int j2 = b + lane;
-        if (j2 < m16) w = ld_nc_v4(src2 + 16 * (int64_t)j2);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = b + lane + 32 * u;
             if (j < n16) st_v4(dst + 16 * (int64_t)j, v[u]);
         }
-        if (j2 < m16) st_v4(dst2 + 16 * (int64_t)j2, w);
     }
+    for (int j = lane; j < m8; j += 32)
+        reinterpret_cast<uint2*>(dst2)[j] = reinterpret_cast<const uint2*>(src2)[j];
 }
 
 // Copy the rows of minibatch b into its ring buffer, warp gw of nw, then make
@@ -417,7 +418,7 @@ __device__ void gather_minibatch(const FusedArgs& a, int b, int gw, int nw) {
         copy_slot_row(a.ring + dr * a.row_bytes, a.shard_rows[s] + (int64_t)r * a.row_bytes,
                       a.row_bytes >> 4, has_sf ? a.ring_sf + dr * a.sf_bytes : nullptr,
                       has_sf ? a.shard_sf[s] + (int64_t)r * a.sf_bytes : nullptr,
-                      has_sf ? a.sf_bytes >> 4 : 0, lane);
+                      has_sf ? a.sf_bytes >> 3 : 0, lane);
     }
     publish_fence();
     __syncthreads();
