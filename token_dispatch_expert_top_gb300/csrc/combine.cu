@@ -34,16 +34,32 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
         float acc[VEC];
 #pragma unroll
         for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int slot = __shfl_sync(0xffffffffu, my_slot, j);
-            const float g = __shfl_sync(0xffffffffu, my_g, j);
-            if (slot < 0 || slot >= T) {
-                if (lane == 0) set_status(ws, MOE_ERR_DEVICE_CHECK);
-                continue;
+        // the k slot rows in groups of KB: every load of a group is issued before
+        // the group is summed, still in j order
+        constexpr int KB = 8;
+        for (int j0 = 0; j0 < k; j0 += KB) {
+            uint4 q[KB];
+            float gj[KB];
+#pragma unroll
+            for (int jj = 0; jj < KB; ++jj) {
+                const int j = j0 + jj;
+                const int slot = __shfl_sync(0xffffffffu, my_slot, j & 31);
+                gj[jj] = __shfl_sync(0xffffffffu, my_g, j & 31);
+                q[jj] = make_uint4(0u, 0u, 0u, 0u);
+                if (j < k) {
+                    if (slot < 0 || slot >= T) {
+                        if (lane == 0) set_status(ws, MOE_ERR_DEVICE_CHECK);
+                        gj[jj] = 0.f;     // skipped, as an out-of-range slot always was
+                    } else if (col < H) {
+                        q[jj] = ld_nc_v4(y + ((int64_t)slot * H + col) * ESZ);
+                    }
+                }
             }
-            if (col < H) {
-                const uint4 q = ld_nc_v4(y + ((int64_t)slot * H + col) * ESZ);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int jj = 0; jj < KB; ++jj) {
+                if (j0 + jj >= k) break;
+                const uint32_t w[4] = {q[jj].x, q[jj].y, q[jj].z, q[jj].w};
+                const float g = gj[jj];
                 if constexpr (BF16) {
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
