@@ -70,6 +70,9 @@ ROUTE_CASES = [
     # ragged last token tile
     synth.Workload("route_e96", N=257, H=512, I=128, E=96, k=6, S=1, dtype="mxfp8"),
     synth.Workload("route_e64_bf16", N=300, H=256, I=128, E=64, k=4, S=3, dtype="bf16"),
+    # k > 8: the 16- and 32-entry top-k lists (two column ranges per quarter for k > 16)
+    synth.Workload("route_k12", N=384, H=512, I=128, E=256, k=12, S=3, dtype="bf16"),
+    synth.Workload("route_k20", N=200, H=512, I=128, E=128, k=20, S=1, dtype="mxfp8"),
 ]
 
 
