@@ -317,10 +317,9 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
                       const moe_params_t* params, void* out, int32_t* idx_out, float* gate_out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
-/* moe_layout without a workspace, for callers that cannot allocate device memory:
- * code running inside a stream capture (an allocation there breaks the capture), a
- * serving process that reserves all its device memory at start-up and allocates
- * nothing afterwards, or a plug-in whose host owns the allocator.  The pages
+/* moe_layout without a workspace, for callers that cannot allocate device memory at
+ * call time: a serving process that reserves all its device memory at start-up and
+ * allocates nothing afterwards, or a plug-in whose host owns the allocator.  The pages
  * describe no such entry point; it exists for those callers only.
  *   Same arguments, shape checks and results as moe_layout, minus the workspace
  *   (H, I and dtype are checked exactly as moe_layout checks them).  Its scratch
@@ -329,11 +328,9 @@ int moe_forward_fused(const void* x, const void* w_router, const float* bias,
  *   process exits.  Shapes with ceil(N*k/256) * E > 131072 are rejected with
  *   MOE_ERR_WORKSPACE before anything is launched.
  *   The first call on each device looks up the array's device address with
- *   cudaGetSymbolAddress (that device must be current); make that first call
- *   before any stream capture begins.  The address is cached with the id of the
- *   device's current context; after a device reset (or another teardown of the
- *   context) the next call looks it up again, so that call, too, belongs
- *   before any capture.
+ *   cudaGetSymbolAddress (that device must be current).  The address is cached
+ *   with the id of the device's current context; after a device reset (or another
+ *   teardown of the context) the next call looks it up again.
  *   Every call on a device uses that device's one copy of the array and leaves
  *   its contents behind: calls that overlap on the same GPU (for example on two
  *   streams) race.  Calls on different GPUs use different copies.

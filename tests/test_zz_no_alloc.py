@@ -1,5 +1,5 @@
 """moe_layout_noalloc: the layout entry point for callers that cannot allocate
-device memory (inside a stream capture, or under a host that forbids allocation),
+device memory (under a host that forbids allocation after start-up),
 whose scratch is the library's fixed device array instead of a workspace.
 
 It must give exactly what moe_layout gives, on two calls in a row through the C

@@ -1,11 +1,9 @@
 // layout_noalloc.cu -- moe_layout_noalloc: the sort-free layout for callers that
 // cannot allocate device memory, with its scratch in a fixed device array.
 //
-// Who needs it: code that runs where cudaMalloc is not an option -- inside a
-// region being captured into a CUDA graph (an allocation there breaks the
-// capture), in a serving process that reserves all of its device memory up front
-// and forbids allocation afterwards, or in a plug-in whose host owns the allocator
-// and hands out no scratch.  moe_layout needs a caller-supplied workspace for its
+// Who needs it: code that runs where cudaMalloc is not an option -- a serving
+// process that reserves all of its device memory up front and forbids allocation
+// afterwards, or a plug-in whose host owns the allocator and hands out no scratch.  moe_layout needs a caller-supplied workspace for its
 // per-chunk counts; this variant needs none, because that scratch lives in a
 // file-scope __device__ array that is part of the library's image.
 //
