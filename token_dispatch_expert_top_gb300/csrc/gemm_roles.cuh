@@ -215,12 +215,14 @@ __device__ void producer_role(const Pipe& p, const GemmMaps& maps, const GemmSid
                 ta = maps.tail(tl.kind);
                 a_bytes = kTailRows * 128;
             }
+            // the weight tile first: for the first CTA on an (expert, N tile) it comes
+            // from DRAM, the longer wait (measured 0.8% faster than A first)
             mbar_arrive_expect_tx(&p.full[stage], a_bytes + B_BYTES + (MX ? SFB_BYTES : 0));
-            tma_load_2d(sa, ta, &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
             bulk_load(sb, sd.b_pk + (tile0 + kb) * B_TILE, B_TILE, &p.full[stage]);
             if (MX)
                 bulk_load(p.smem + OFF_SFB + stage * SFB_BYTES, sd.sfb_pk + (tile0 + kb) * SFB_TILE,
                           SFB_TILE, &p.full[stage]);
+            tma_load_2d(sa, ta, &p.full[stage], kb * (MX ? 128 : 64), tl.a_row0);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1;
