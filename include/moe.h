@@ -241,20 +241,22 @@ int moe_layout(const int32_t* idx, const moe_shape_t* shape, int32_t* counts, in
  *   shard_scales : DEVICE array of S device pointers to [N/S][H/32] scales
  *                  (MXFP8 only; NULL otherwise)
  *   sched        : [T][2] from moe_layout
- *   inv          : [N][k] from moe_layout, or NULL.  Given, the slots are visited
- *                  in its order (token by token), so the k slots that pull the same
- *                  source row come one after another and the row is fetched from
- *                  HBM once; each slot still reads its own schedule entry.  NULL:
- *                  slot order
+ *   inv          : [N][k] from the same moe_layout call as sched, or NULL.  Given,
+ *                  the k slots of each token are handled together: every slot's
+ *                  schedule entry is read, the row named by the token's first slot
+ *                  in range is fetched from HBM once and written to each of its
+ *                  slots in range; a slot whose entry names another row is skipped
+ *                  and recorded as MOE_ERR_DEVICE_CHECK.  NULL: slot order, each
+ *                  slot copying its own schedule entry
  *   ring, ring_scales : [ring_slots][row] destination (ring_scales MXFP8 only),
  *                  16-byte aligned
  * Shard row bases must be 16-byte aligned: a schedule entry whose source row is
  * not (or lies outside its shard) is skipped and recorded as
  * MOE_ERR_DEVICE_CHECK.  When both the row and its scale row are multiples of 16
- * bytes, rows move through the bulk-copy engine (per warp, one lane streams slots
- * through a ring of shared-memory row buffers: bulk load, then bulk store);
- * otherwise one warp per slot row copies with 16- or 4-byte vector loads and
- * stores, in slot order. */
+ * bytes, rows move through the bulk-copy engine (per warp, one lane streams rows
+ * through a ring of shared-memory row buffers: a bulk load, then one bulk store
+ * per slot); otherwise one warp per slot row copies with 16- or 4-byte vector
+ * loads and stores, in slot order. */
 int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
                       const moe_shape_t* shape, const int32_t* sched, const int32_t* inv,
                       int slot_begin, int slot_count, void* ring, void* ring_scales, int ring_slots,

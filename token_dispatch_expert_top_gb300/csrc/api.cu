@@ -424,7 +424,7 @@ int moe_dispatch_pull(const void* const* shard_rows, const void* const* shard_sc
     if (!workspace || workspace_bytes < sizeof(WsHeader)) return MOE_ERR_WORKSPACE;
     const int row_bytes = s.H * (int)op_elem(s.dtype);
     const int scale_bytes = mx ? s.H / 32 : 0;
-    return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, inv, T, slot_begin,
+    return cuda_status(launch_dispatch_pull(shard_rows, shard_scales, sched, inv, T, s.k, slot_begin,
                                             slot_count, s.S, s.N / s.S, row_bytes, scale_bytes, ring,
                                             ring_scales, ring_slots, num_sms_current(),
                                             at<WsHeader>(workspace, 0), kDefaultTimeoutNs,
@@ -524,7 +524,7 @@ static int forward_staged(const void* x, const void* w_router, const float* bias
     void* ring = at<void>(ws, pl.ring);
     void* ring_sf = mx ? at<void>(ws, pl.ring_sf) : nullptr;
     rc = cuda_status(launch_dispatch_pull((const void* const*)tab, (const void* const*)tab_sf, sched,
-                                          inv, T, 0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
+                                          inv, T, s.k, 0, T, s.S, rows, row_bytes, mx ? s.H / 32 : 0, ring,
                                           ring_sf, pl.ring_slots, num_sms_current(), hdr,
                                           timeout_of(params), st));
     if (rc) return rc;

@@ -86,24 +86,20 @@ __global__ void __launch_bounds__(kGatherWarps * 32, 2) dispatch_pull_kernel(
 // streamed out) -- so a few threads per SM keep ~100 KB+ in flight without
 // holding the data in registers.  A buffer is refilled once the bulk store that
 // read it is LAG stores old and has finished reading (bulk-group accounting).
-// With `order` (the inverse map [N][k], flattened) the slots are visited token by
-// token: the k slots that pull the same source row come one after another, so the
-// row is fetched from HBM once and the other k-1 loads hit L2.  Each slot still
-// takes its (shard, row) from its schedule entry; slots outside [slot_begin,
-// slot_begin + slot_count) are skipped.
-// Sizing, measured on the DeepSeek-V3 layer's dispatch (545 MB, L2 flushed): a
-// store lag of 1 and two CTAs of 4 warps per SM (about 100 KB of buffers each)
-// take 103 us, against 108 us for one CTA with 200 KB and a lag of 2.
+// This kernel visits the slots in slot order (no inverse map given); with the
+// inverse map the token-broadcast kernel below is used.
+// Sizing (both kernels), measured on the DeepSeek-V3 layer's dispatch (545 MB,
+// L2 flushed): a store lag of 1 and two CTAs of 4 warps per SM (about 100 KB of
+// buffers each).
 constexpr int kBulkWarps = 4;
 constexpr int kBulkLag = 1;
 constexpr int kBulkMaxBuf = 16;
 
 __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
     const uint8_t* const* __restrict__ shard_rows, const uint8_t* const* __restrict__ shard_scales,
-    const int32_t* __restrict__ sched, const int32_t* __restrict__ order, int npos, int slot_begin,
-    int slot_count, int S, int rows_per_shard, int row_bytes, int scale_bytes,
-    uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales, int ring_slots, int nbuf, WsHeader* ws,
-    unsigned long long timeout_ns) {
+    const int32_t* __restrict__ sched, int slot_begin, int slot_count, int S, int rows_per_shard,
+    int row_bytes, int scale_bytes, uint8_t* __restrict__ ring, uint8_t* __restrict__ ring_scales,
+    int ring_slots, int nbuf, WsHeader* ws, unsigned long long timeout_ns) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort[kBulkWarps];
     __shared__ int s_slot[kBulkWarps][kBulkMaxBuf];   // destination slot of each row buffer
@@ -118,8 +114,9 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
     }
     __syncwarp();
 
-    // This warp's positions (slots, or entries of order): chunks of 32 consecutive
+    // This warp's positions (slot_begin + position): chunks of 32 consecutive
     // positions, chunk c = gw + i * nw.
+    const int npos = slot_count;
     const int gw = blockIdx.x * kBulkWarps + warp, nw = gridDim.x * kBulkWarps;
     const int nchunks = (npos + 31) / 32;
     if (gw >= nchunks) return;
@@ -144,12 +141,10 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
             const int i = pos_of(c0) + lane;
             my_t = -1;
             if (i < npos) {
-                const int t = order ? order[i] : slot_begin + i;
-                if (t >= slot_begin && t < slot_begin + slot_count) {
-                    my_t = t;
-                    my_s = sched[2 * (int64_t)t];
-                    my_r = sched[2 * (int64_t)t + 1];
-                }
+                const int t = slot_begin + i;
+                my_t = t;
+                my_s = sched[2 * (int64_t)t];
+                my_r = sched[2 * (int64_t)t + 1];
             }
         }
         const int sidx = __shfl_sync(0xffffffffu, my_s, q & 31);
@@ -215,8 +210,129 @@ __global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bulk_kernel(
     }
 }
 
+// ------------------------------------------------------ token-broadcast variant
+// With the inverse map, the k slots of token n all pull the same source row: the
+// warp reads each slot's schedule entry, fetches the row named by the first slot
+// in range once (one bulk load into a shared-memory buffer) and writes it to every
+// slot in range with k bulk stores from that buffer.  A slot whose schedule entry
+// names another row is skipped and recorded as MOE_ERR_DEVICE_CHECK (inv and
+// sched come from one moe_layout call, where this cannot happen).  One HBM read
+// per token feeds k ring rows, so few loads in flight keep the stores busy and
+// the kernel runs at the HBM write rate.  Warp w takes tokens w, w + nw, ...; a
+// buffer is refilled once its store group is LAG groups old and has finished
+// reading it.
+constexpr int kBcastMaxBuf = 8;
+
+__global__ void __launch_bounds__(kBulkWarps * 32, 1) dispatch_bcast_kernel(
+    const uint8_t* const* __restrict__ shard_rows, const uint8_t* const* __restrict__ shard_scales,
+    const int32_t* __restrict__ sched, const int32_t* __restrict__ inv, int N, int k, int slot_begin,
+    int slot_count, int S, int rows_per_shard, int row_bytes, int scale_bytes, uint8_t* __restrict__ ring,
+    uint8_t* __restrict__ ring_scales, int ring_slots, int nbuf, WsHeader* ws, unsigned long long timeout_ns) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort[kBulkWarps];
+    __shared__ int s_dst[kBulkWarps][kBcastMaxBuf][32];   // ring row per slot of the buffer's token (-1: none)
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int unit = row_bytes + scale_bytes;
+    const int64_t T = (int64_t)N * k;
+    uint8_t* buf = smem + (size_t)warp * nbuf * unit;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkWarps * nbuf * unit) + warp * kBcastMaxBuf;
+    if (lane == 0) {
+        for (int b = 0; b < nbuf; ++b) mbar_init(&bars[b], 1);
+        s_abort[warp] = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int gw = blockIdx.x * kBulkWarps + warp, nw = gridDim.x * kBulkWarps;
+    if (gw >= N) return;
+    const int total = (N - gw + nw - 1) / nw;     // tokens of this warp
+    const unsigned long long deadline = globaltimer_ns() + timeout_ns;
+    const uint64_t stream = l2_policy_evict_first();
+    volatile int* abort_flag = &s_abort[warp];
+    uint32_t bad = 0;          // bit b: buffer b holds nothing to store
+
+    // Read the schedule entries of the q-th token's slots (lane j: slot j) and
+    // issue the bulk load of its row into buffer q % nbuf (lane 0).
+    auto load = [&](int q) {
+        const int64_t n = gw + (int64_t)q * nw;
+        const int b = q % nbuf;
+        int t = -1, s = -1, r = -1;
+        if (lane < k) {
+            t = inv[n * k + lane];
+            if (t >= 0 && t < T) {
+                s = sched[2 * (int64_t)t];
+                r = sched[2 * (int64_t)t + 1];
+            } else {
+                set_status(ws, MOE_ERR_DEVICE_CHECK);
+                t = -1;
+            }
+        }
+        const bool in_range = t >= slot_begin && t < slot_begin + slot_count;
+        const uint32_t m = __ballot_sync(0xffffffffu, in_range);
+        const int first = m ? __ffs(m) - 1 : 0;
+        const int s0 = __shfl_sync(0xffffffffu, s, first);
+        const int r0 = __shfl_sync(0xffffffffu, r, first);
+        bool ok = m != 0 && s0 >= 0 && s0 < S && r0 >= 0 && r0 < rows_per_shard;
+        const uint8_t* src = ok ? shard_rows[s0] + (int64_t)r0 * row_bytes : nullptr;
+        const uint8_t* ssrc = (ok && scale_bytes) ? shard_scales[s0] + (int64_t)r0 * scale_bytes : nullptr;
+        if (ok && ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(ssrc)) & 15)) ok = false;
+        const bool mine = ok && in_range && s == s0 && r == r0;
+        if (in_range && !mine) set_status(ws, MOE_ERR_DEVICE_CHECK);
+        s_dst[warp][b][lane] = mine ? (int)(t % ring_slots) : -1;
+        const bool any = __any_sync(0xffffffffu, mine);
+        __syncwarp();
+        if (lane == 0) {
+            if (any) {
+                bad &= ~(1u << b);
+                mbar_arrive_expect_tx(&bars[b], (uint32_t)unit);
+                uint8_t* dst = buf + (size_t)b * unit;
+                bulk_load(dst, src, (uint32_t)row_bytes, &bars[b]);
+                if (scale_bytes) bulk_load(dst + row_bytes, ssrc, (uint32_t)scale_bytes, &bars[b]);
+            } else {
+                bad |= 1u << b;
+                mbar_arrive(&bars[b]);
+            }
+        }
+    };
+
+    const int pre = min(nbuf, total);
+    for (int q = 0; q < pre; ++q) load(q);
+    for (int q = 0; q < total; ++q) {
+        if (lane == 0) {
+            const int b = q % nbuf;
+            if (!mbar_wait_bounded(&bars[b], (uint32_t)((q / nbuf) & 1), abort_flag, ws, deadline)) {
+                // give up: nothing more is issued; drain what is in flight below
+            } else if (!(bad & (1u << b))) {
+                fence_proxy_async_smem();
+                const uint8_t* src = buf + (size_t)b * unit;
+                for (int j = 0; j < k; ++j) {
+                    const int dr = s_dst[warp][b][j];
+                    if (dr < 0) continue;
+                    bulk_store_hint(ring + (int64_t)dr * row_bytes, src, (uint32_t)row_bytes, stream);
+                    if (scale_bytes)
+                        bulk_store_hint(ring_scales + (int64_t)dr * scale_bytes, src + row_bytes,
+                                        (uint32_t)scale_bytes, stream);
+                }
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<kBulkLag>();
+        }
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const int qn = q - kBulkLag + nbuf;     // refill the buffer whose stores are now LAG groups old
+        if (q >= kBulkLag && qn < total) load(qn);
+    }
+    if (lane == 0) {
+        if (*abort_flag) {
+            const unsigned long long d2 = globaltimer_ns() + 1000000ull;
+            while (globaltimer_ns() < d2) {
+            }
+        }
+        bulk_wait_group_all();
+    }
+}
+
 cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                                 const int32_t* sched, const int32_t* order, int order_len,
+                                 const int32_t* sched, const int32_t* order, int order_len, int order_k,
                                  int slot_begin, int slot_count, int S, int rows_per_shard,
                                  int row_bytes, int scale_bytes, void* ring, void* ring_scales,
                                  int ring_slots, int num_sms, WsHeader* ws,
@@ -235,6 +351,24 @@ cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* cons
     const bool bulk = row_bytes % 16 == 0 && scale_bytes % 16 == 0 && nbuf >= kBulkLag + 2 &&
                       (reinterpret_cast<uintptr_t>(ring) & 15) == 0 &&
                       (scale_bytes == 0 || (reinterpret_cast<uintptr_t>(ring_scales) & 15) == 0);
+    if (bulk && order && order_k > 0 && order_k <= 32 && order_len % order_k == 0) {
+        const int nb = nbuf > kBcastMaxBuf ? kBcastMaxBuf : nbuf;
+        const size_t smem = (size_t)kBulkWarps * nb * unit + (size_t)kBulkWarps * kBcastMaxBuf * 8;
+        cudaError_t e = cudaFuncSetAttribute(dispatch_bcast_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int static_smem = kBulkWarps * (kBcastMaxBuf * 32 + 1) * 4;
+        int per_sm = (int)((227 * 1024) / (smem + static_smem + 1024));
+        if (per_sm < 1) per_sm = 1;
+        const int N = order_len / order_k;
+        int blocks = (N + kBulkWarps - 1) / kBulkWarps;
+        if (blocks > num_sms * per_sm) blocks = num_sms * per_sm;
+        dispatch_bcast_kernel<<<blocks, kBulkWarps * 32, smem, stream>>>(
+            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, order, N, order_k,
+            slot_begin, slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring,
+            (uint8_t*)ring_scales, ring_slots, nb, ws, timeout_ns);
+        return cudaGetLastError();
+    }
     if (bulk) {
         const size_t smem = (size_t)kBulkWarps * nbuf * unit + bars_bytes;
         cudaError_t e = cudaFuncSetAttribute(dispatch_bulk_kernel,
@@ -242,14 +376,13 @@ cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* cons
         if (e != cudaSuccess) return e;
         int per_sm = (int)((227 * 1024) / (smem + 1024));
         if (per_sm < 1) per_sm = 1;
-        const int npos = order ? order_len : slot_count;
-        const int nchunks = (npos + 31) / 32;
+        const int nchunks = (slot_count + 31) / 32;
         int blocks = (nchunks + kBulkWarps - 1) / kBulkWarps;
         if (blocks > num_sms * per_sm) blocks = num_sms * per_sm;
         dispatch_bulk_kernel<<<blocks, kBulkWarps * 32, smem, stream>>>(
-            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, order, npos,
-            slot_begin, slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring,
-            (uint8_t*)ring_scales, ring_slots, nbuf, ws, timeout_ns);
+            (const uint8_t* const*)shard_rows, (const uint8_t* const*)shard_scales, sched, slot_begin,
+            slot_count, S, rows_per_shard, row_bytes, scale_bytes, (uint8_t*)ring, (uint8_t*)ring_scales,
+            ring_slots, nbuf, ws, timeout_ns);
         return cudaGetLastError();
     }
     int blocks = (slot_count + kGatherWarps - 1) / kGatherWarps;

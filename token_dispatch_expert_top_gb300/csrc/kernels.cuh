@@ -31,10 +31,10 @@ cudaError_t launch_layout(const int32_t* idx, int N, int k, int E, int S, int32_
                           int32_t* offsets, int32_t* sched, int32_t* inv, int32_t* cnt_scratch,
                           int32_t* base_scratch, WsHeader* ws, cudaStream_t stream);
 
-// order (nullable, order_len entries): visit the slots in this order (the
-// inverse map, flattened: source-row order), skipping those outside the range.
+// order (nullable, order_len entries): the inverse map, flattened ([N][order_k]);
+// each token's row is read once and written to its slots in range.
 cudaError_t launch_dispatch_pull(const void* const* shard_rows, const void* const* shard_scales,
-                                 const int32_t* sched, const int32_t* order, int order_len,
+                                 const int32_t* sched, const int32_t* order, int order_len, int order_k,
                                  int slot_begin, int slot_count, int S, int rows_per_shard,
                                  int row_bytes, int scale_bytes, void* ring, void* ring_scales,
                                  int ring_slots, int num_sms, WsHeader* ws,
