@@ -229,6 +229,40 @@ def test_dispatch_pull_rows_by_schedule(M, dtype, H, token_order):
     assert not got[untouched].any()                 # nothing outside the slot range
 
 
+def test_dispatch_token_broadcast_checks_schedule_entries(M):
+    """With inv, a token's row is read once for its k slots; a slot whose schedule
+    entry names another row is skipped and reported, and every slot written gets
+    exactly the row its own schedule entry names."""
+    rng = np.random.default_rng(4)
+    N, E, k, S, H = 256, 16, 4, 4, 1024
+    w = synth.Workload("pullchk", N=N, H=H, I=128, E=E, k=k, S=S, dtype="bf16")
+    shape = M.Shape.of(w)
+    ws = _ws(M, shape)
+    rows = N // S
+    shards = [torch.randint(0, 256, (rows, 2 * H), dtype=torch.uint8, device="cuda") for _ in range(S)]
+    tab = torch.tensor([t.data_ptr() for t in shards], dtype=torch.int64, device="cuda")
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(N)]).astype(np.int32)
+    _, _, sched_np, inv_np = O.layout(idx, E, S)
+    n_bad = 37
+    t_bad = int(inv_np[n_bad, 2])                 # the token's third slot names another row
+    sched_np = sched_np.copy()
+    other = (n_bad + 100) % N
+    sched_np[t_bad] = [other // rows, other % rows]
+    T = N * k
+    ring = torch.zeros((T, 2 * H), dtype=torch.uint8, device="cuda")
+    M.moe_dispatch_pull(tab, None, shape, torch.from_numpy(sched_np).cuda(), torch.from_numpy(inv_np).cuda(),
+                        0, T, ring, None, T, ws)
+    assert M.moe_last_device_status(ws) == M.MOE_ERR_DEVICE_CHECK
+    allrows = torch.cat(shards).cpu()
+    got = ring.cpu()
+    for t in range(T):
+        if t == t_bad:
+            assert not got[t].any()
+        else:
+            src = sched_np[t, 0] * rows + sched_np[t, 1]
+            assert torch.equal(got[t], allrows[src])
+
+
 # ------------------------------------------------------------------------- combine
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_combine_matches_oracle(M, dtype):
